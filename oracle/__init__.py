@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the speculative-decoding verification step.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+never calls it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, index-order
+compensated sums); this module compiles it with gcc and wraps it with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to the sources (-O2, no fast-math, OpenMP)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True, cwd=_HERE)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_verify_sample.argtypes = [P, P, P, P, ctypes.c_double, I, I, I, P, P, P, P, P, I]
+            lib.oracle_verify_sample.restype = I
+            lib.oracle_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I]
+            lib.oracle_verify_greedy.restype = I
+            lib.oracle_verify_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, I]
+            lib.oracle_verify_tree_greedy.restype = I
+            lib.oracle_softmax_row.argtypes = [P, I, ctypes.c_double, P]
+            lib.oracle_softmax_row.restype = I
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def verify_sample(target, draft, tokens, uniforms, T, *, want_logprob=False, want_ratio=False,
+                  want_cdf=False, nthreads=0):
+    """Stochastic verification.  target [B, g+1, V], draft [B, g, V] float32
+    (bf16 inputs as exact float32), tokens [B, g], uniforms [B, g+1].
+    Returns a dict with tokens, accepted, bad and the optional diagnostics."""
+    lib = _load()
+    target = _f32(target)
+    B, g1, V = target.shape
+    g = g1 - 1
+    draft = _f32(draft) if g > 0 else None
+    tokens = _i32(tokens) if g > 0 else None
+    uniforms = _f32(uniforms)
+    assert uniforms.shape == (B, g + 1)
+    if g > 0:
+        assert draft.shape == (B, g, V) and tokens.shape == (B, g)
+    out_t = np.empty((B, g + 1), np.int32)
+    out_a = np.empty((B,), np.int32)
+    lp = np.empty((B, g, 2), np.float64) if want_logprob else None
+    ra = np.empty((B, g), np.float64) if want_ratio else None
+    cdf = np.empty((B, V), np.float64) if want_cdf else None
+    bad = lib.oracle_verify_sample(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(uniforms),
+                                   float(T), B, g, V, _ptr(out_t), _ptr(out_a), _ptr(lp),
+                                   _ptr(ra), _ptr(cdf), int(nthreads))
+    if bad < 0:
+        raise ValueError("oracle_verify_sample: invalid arguments")
+    return {"tokens": out_t, "accepted": out_a, "bad": bad, "logprob": lp, "ratio": ra, "cdf": cdf}
+
+
+def verify_greedy(target, tokens, *, nthreads=0):
+    lib = _load()
+    target = _f32(target)
+    B, g1, V = target.shape
+    g = g1 - 1
+    tokens = _i32(tokens) if g > 0 else None
+    out_t = np.empty((B, g + 1), np.int32)
+    out_a = np.empty((B,), np.int32)
+    amax = np.empty((B, g + 1), np.int32)
+    bad = lib.oracle_verify_greedy(_ptr(target), _ptr(tokens), B, g, V, _ptr(out_t), _ptr(out_a),
+                                   _ptr(amax), int(nthreads))
+    if bad < 0:
+        raise ValueError("oracle_verify_greedy: invalid arguments")
+    return {"tokens": out_t, "accepted": out_a, "argmax": amax, "bad": bad}
+
+
+def verify_tree_greedy(target, node_tokens, parents, *, nthreads=0):
+    lib = _load()
+    target = _f32(target)
+    B, N, V = target.shape
+    node_tokens = _i32(node_tokens)
+    parents = _i32(parents)
+    out_n = np.empty((B, N), np.int32)
+    out_t = np.empty((B, N), np.int32)
+    out_a = np.empty((B,), np.int32)
+    bad = lib.oracle_verify_tree_greedy(_ptr(target), _ptr(node_tokens), _ptr(parents), B, N, V,
+                                        _ptr(out_n), _ptr(out_t), _ptr(out_a), int(nthreads))
+    if bad < 0:
+        raise ValueError("oracle_verify_tree_greedy: invalid arguments")
+    return {"nodes": out_n, "tokens": out_t, "accepted": out_a, "bad": bad}
+
+
+def softmax_row(z, T):
+    lib = _load()
+    z = _f32(z)
+    out = np.empty(z.shape[0], np.float64)
+    rc = lib.oracle_softmax_row(_ptr(z), z.shape[0], float(T), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_softmax_row: row has no distribution (rc=%d)" % rc)
+    return out

@@ -1,0 +1,247 @@
+"""Seeded synthetic inputs for the verification step.
+
+This module produces logits, draft tokens, uniforms and draft trees with the
+shapes and value distributions of the five benchmark workloads.  It holds none
+of the verification arithmetic: no softmax, no accept ratio, no residual.  The
+drafter is simulated by Gumbel-max sampling (argmax of logits/T plus Gumbel
+noise), which draws from softmax(logits/T) without ever forming it, and the
+tree generator only needs the row argmax of the target logits to plant
+matching tokens.
+
+Both the CUDA path and the fp64 oracle are fed from here; nothing here
+depends on either of them.
+
+Workloads (B sequences, gamma drafts, V vocabulary, T temperature):
+
+  chain-small   B=1   gamma=4 V=1000   fp32  target N(0,2^2), draft = target + N(0,0.5^2), T=1, seed 0
+  chain-b8      B=8   gamma=7 V=151936 bf16  target N(0,3^2) + 20 boosted (+8) per row,
+                                               draft = target + N(0,1^2), T=1, seed 1
+  chain-b64     B=64  gamma=7 V=151936 bf16  as chain-b8, T=0.6, draft noise sigma_b in
+                                               (0.25, 1, 4)[b mod 3], seed 2
+  chain-b256    B=256 gamma=4 V=128256 fp32  target N(0,2.5^2), draft = 0.8 target + 0.2 N(0,2.5^2),
+                                               T=1, seed 3
+  tree-b32      B=32  N=36    V=151936 bf16  node logits as chain-b8's target, tree = root +
+                                               7-node main chain + 4 single-node branches at each
+                                               of depths 1..7, node token = argmax of the parent's
+                                               row with probability 0.7, seed 4
+
+The vocabulary 151936 is Qwen3's and gamma=7 matches the K=7 of the DLite
+reading notes (section "Experimental setup").  Every workload can be shrunk
+(B, gamma, V overrides) with the same recipe for parity tests.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "WORKLOADS", "ChainInputs", "TreeInputs", "make_chain", "make_tree",
+    "tree_topology", "to_bf16_exact", "gumbel_argmax",
+]
+
+
+@dataclasses.dataclass(frozen=True)
+class ChainWorkload:
+    name: str
+    B: int
+    gamma: int
+    V: int
+    dtype: str          # "f32" or "bf16"
+    T: float
+    seed: int
+    family: str         # "gauss" (chain-small), "boosted" (chain-b8/b64), "mixed" (chain-b256)
+    target_sigma: float
+    draft_sigma: tuple  # per-sequence draft noise (cycled over b)
+
+
+@dataclasses.dataclass(frozen=True)
+class TreeWorkload:
+    name: str
+    B: int
+    N: int
+    V: int
+    dtype: str
+    seed: int
+    depth: int          # main-chain length
+    branches: int       # single-node branches per depth
+    match_prob: float
+
+
+WORKLOADS = {
+    "chain-small": ChainWorkload("chain-small", 1, 4, 1000, "f32", 1.0, 0, "gauss", 2.0, (0.5,)),
+    "chain-b8": ChainWorkload("chain-b8", 8, 7, 151936, "bf16", 1.0, 1, "boosted", 3.0, (1.0,)),
+    "chain-b64": ChainWorkload("chain-b64", 64, 7, 151936, "bf16", 0.6, 2, "boosted", 3.0,
+                               (0.25, 1.0, 4.0)),
+    "chain-b256": ChainWorkload("chain-b256", 256, 4, 128256, "f32", 1.0, 3, "mixed", 2.5, (2.5,)),
+    "tree-b32": TreeWorkload("tree-b32", 32, 36, 151936, "bf16", 4, 7, 4, 0.7),
+}
+
+BOOSTED_PER_ROW = 20
+BOOST = 8.0
+
+
+@dataclasses.dataclass
+class ChainInputs:
+    """One verification batch.  Logit arrays are float32; for dtype "bf16"
+    every value is exactly representable in bfloat16."""
+    target: np.ndarray        # [B, gamma+1, V] float32
+    draft: np.ndarray         # [B, gamma, V]   float32
+    draft_tokens: np.ndarray  # [B, gamma] int32, sampled from softmax(draft/T)
+    greedy_tokens: np.ndarray # [B, gamma] int32, argmax of each draft row
+    uniforms: np.ndarray      # [B, gamma+1] float32 in [0, 1)
+    T: float
+    dtype: str
+    B: int
+    gamma: int
+    V: int
+    name: str
+
+    def logit_bytes(self, greedy: bool = False) -> int:
+        elt = 2 if self.dtype == "bf16" else 4
+        rows = self.B * (self.gamma + 1) + (0 if greedy else self.B * self.gamma)
+        return rows * self.V * elt
+
+
+@dataclasses.dataclass
+class TreeInputs:
+    target: np.ndarray        # [B, N, V] float32 (bf16-exact for dtype "bf16")
+    node_tokens: np.ndarray   # [B, N] int32 (node 0 holds -1: the root carries no draft)
+    parents: np.ndarray       # [B, N] int32, parents[:, 0] = -1, parents[:, n] < n
+    dtype: str
+    B: int
+    N: int
+    V: int
+    name: str
+
+    def logit_bytes(self) -> int:
+        elt = 2 if self.dtype == "bf16" else 4
+        return self.B * self.N * self.V * elt
+
+
+def to_bf16_exact(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even) and return
+    them as float32.  Finite inputs only."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32)
+
+
+def gumbel_argmax(rng: np.random.Generator, logits: np.ndarray, T: float) -> np.ndarray:
+    """Draw one index per row of `logits` ([R, V]) from softmax(logits/T) by
+    the Gumbel-max construction.  Rows are processed one at a time to bound
+    memory."""
+    out = np.empty(logits.shape[0], dtype=np.int32)
+    for r in range(logits.shape[0]):
+        u = rng.random(logits.shape[1])                 # float64 in [0, 1)
+        g = -np.log(-np.log(np.maximum(u, 1e-300)))
+        out[r] = int(np.argmax(logits[r].astype(np.float64) / T + g))
+    return out
+
+
+def _round(x: np.ndarray, dtype: str) -> np.ndarray:
+    return to_bf16_exact(x) if dtype == "bf16" else np.ascontiguousarray(x, dtype=np.float32)
+
+
+def make_chain(name: str, *, B: Optional[int] = None, gamma: Optional[int] = None,
+               V: Optional[int] = None, seed: Optional[int] = None,
+               T: Optional[float] = None) -> ChainInputs:
+    """Generate the chain workload `name` (optionally shrunk)."""
+    w = WORKLOADS[name]
+    assert isinstance(w, ChainWorkload), name
+    B = w.B if B is None else B
+    gamma = w.gamma if gamma is None else gamma
+    V = w.V if V is None else V
+    seed = w.seed if seed is None else seed
+    T = w.T if T is None else T
+    s_logits, s_noise, s_draft, s_unif = np.random.SeedSequence(seed).spawn(4)
+    r_logits = np.random.default_rng(s_logits)
+    r_noise = np.random.default_rng(s_noise)
+    r_draft = np.random.default_rng(s_draft)
+    r_unif = np.random.default_rng(s_unif)
+
+    zt = r_logits.standard_normal((B, gamma + 1, V), dtype=np.float32)
+    zt *= np.float32(w.target_sigma)
+    if w.family == "boosted":
+        k = min(BOOSTED_PER_ROW, V)
+        for b in range(B):
+            for i in range(gamma + 1):
+                idx = r_logits.choice(V, size=k, replace=False)
+                zt[b, i, idx] += np.float32(BOOST)
+    zt = _round(zt, w.dtype)
+
+    noise = r_noise.standard_normal((B, gamma, V), dtype=np.float32)
+    if w.family == "mixed":
+        # draft = 0.8 * target + 0.2 * independent N(0, sigma^2)
+        zd = np.float32(0.8) * zt[:, :gamma, :] + np.float32(0.2 * w.draft_sigma[0]) * noise
+    else:
+        sig = np.array([w.draft_sigma[b % len(w.draft_sigma)] for b in range(B)],
+                       dtype=np.float32)[:, None, None]
+        zd = zt[:, :gamma, :] + sig * noise
+    del noise
+    zd = _round(zd, w.dtype)
+
+    if gamma > 0:
+        tok = gumbel_argmax(r_draft, zd.reshape(B * gamma, V), T).reshape(B, gamma)
+        gtok = np.argmax(zd, axis=2).astype(np.int32)
+    else:
+        tok = np.zeros((B, 0), np.int32)
+        gtok = np.zeros((B, 0), np.int32)
+    u = r_unif.random((B, gamma + 1), dtype=np.float32)
+    return ChainInputs(np.ascontiguousarray(zt), np.ascontiguousarray(zd), tok, gtok, u,
+                       float(T), w.dtype, B, gamma, V, name)
+
+
+def tree_topology(depth: int, branches: int) -> np.ndarray:
+    """Parent array of the draft tree: node 0 is the root (the last verified
+    token), nodes 1..depth form the main chain (parent of node d is d-1), and
+    node depth+1+branches*(d-1)+k (k < branches) is a single-node branch that
+    is a sibling of main-chain node d (parent d-1).  depth=7, branches=4 gives
+    the 36-node tree of the tree-b32 workload."""
+    n = 1 + depth + depth * branches
+    par = np.empty(n, dtype=np.int32)
+    par[0] = -1
+    for d in range(1, depth + 1):
+        par[d] = d - 1
+        for k in range(branches):
+            par[depth + 1 + branches * (d - 1) + k] = d - 1
+    return par
+
+
+def make_tree(name: str = "tree-b32", *, B: Optional[int] = None, V: Optional[int] = None,
+              seed: Optional[int] = None, depth: Optional[int] = None,
+              branches: Optional[int] = None, match_prob: Optional[float] = None) -> TreeInputs:
+    w = WORKLOADS[name]
+    assert isinstance(w, TreeWorkload), name
+    B = w.B if B is None else B
+    V = w.V if V is None else V
+    seed = w.seed if seed is None else seed
+    depth = w.depth if depth is None else depth
+    branches = w.branches if branches is None else branches
+    mp = w.match_prob if match_prob is None else match_prob
+    par = tree_topology(depth, branches)
+    N = par.shape[0]
+    s_logits, s_tok = np.random.SeedSequence(seed).spawn(2)
+    r_logits = np.random.default_rng(s_logits)
+    r_tok = np.random.default_rng(s_tok)
+    z = r_logits.standard_normal((B, N, V), dtype=np.float32) * np.float32(3.0)
+    k = min(BOOSTED_PER_ROW, V)
+    for b in range(B):
+        for n in range(N):
+            idx = r_logits.choice(V, size=k, replace=False)
+            z[b, n, idx] += np.float32(BOOST)
+    z = _round(z, w.dtype)
+    g = np.argmax(z, axis=2)                      # planted-match reference per node row
+    tok = np.full((B, N), -1, dtype=np.int32)
+    for b in range(B):
+        for n in range(1, N):
+            gp = int(g[b, par[n]])
+            if r_tok.random() < mp or V == 1:
+                tok[b, n] = gp
+            else:
+                r = int(r_tok.integers(0, V - 1))
+                tok[b, n] = r + 1 if r >= gp else r
+    parents = np.ascontiguousarray(np.broadcast_to(par, (B, N)), dtype=np.int32)
+    return TreeInputs(np.ascontiguousarray(z), tok, parents, w.dtype, B, N, V, name)

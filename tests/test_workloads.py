@@ -1,0 +1,80 @@
+"""The seeded input generators: shapes, determinism and the stated recipes."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_59_gb300 import workloads as W
+
+
+def test_bf16_rounding_is_exact_and_nearest():
+    x = np.array([1.0, 1.00390625, 1.001953125, 3.14159, -2.71828, 1e-3], np.float32)
+    y = W.to_bf16_exact(x)
+    # exactly representable in bf16: low 16 bits clear
+    assert (y.view(np.uint32) & 0xFFFF == 0).all()
+    # nearest (ties to even): |x - y| <= half a bf16 ulp
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(x))) - 7)
+    assert (np.abs(x - y) <= ulp / 2 + 1e-12).all()
+    assert W.to_bf16_exact(np.array([1.001953125], np.float32))[0] == 1.0   # tie -> even
+
+
+def test_chain_shapes_and_determinism():
+    a = W.make_chain("chain-b8", B=2, V=3001)
+    b = W.make_chain("chain-b8", B=2, V=3001)
+    assert a.target.shape == (2, 8, 3001) and a.draft.shape == (2, 7, 3001)
+    assert a.draft_tokens.shape == (2, 7) and a.uniforms.shape == (2, 8)
+    assert (a.target == b.target).all() and (a.draft_tokens == b.draft_tokens).all()
+    assert (a.target.view(np.uint32) & 0xFFFF == 0).all()          # bf16-exact
+    assert a.uniforms.min() >= 0 and a.uniforms.max() < 1
+    assert ((a.draft_tokens >= 0) & (a.draft_tokens < 3001)).all()
+    # 20 boosted tokens per row: the top-20 of each row sit well above N(0, 3^2) bulk
+    c = W.make_chain("chain-b8", B=1, V=151936)
+    top = np.sort(c.target[0, 0])[-20:]
+    assert top.min() > 0
+
+
+def test_chain_small_recipe_statistics():
+    x = W.make_chain("chain-small", B=64)
+    assert x.target.shape == (64, 5, 1000)
+    assert abs(x.target.std() - 2.0) < 0.05
+    assert abs((x.draft - x.target[:, :4]).std() - 0.5) < 0.02
+
+
+def test_chain_b64_sigma_cycle():
+    x = W.make_chain("chain-b64", B=6, V=20000)
+    d = (x.draft - x.target[:, :7]).std(axis=(1, 2))
+    assert np.allclose(d[[0, 3]], 0.25, rtol=0.05) and np.allclose(d[[1, 4]], 1.0, rtol=0.05)
+    assert np.allclose(d[[2, 5]], 4.0, rtol=0.05)
+    assert x.T == 0.6
+
+
+def test_chain_b256_mixture():
+    x = W.make_chain("chain-b256", B=2, V=50000)
+    resid = x.draft - np.float32(0.8) * x.target[:, :4]
+    assert abs(resid.std() - 0.5) < 0.01 and x.dtype == "f32"
+
+
+def test_gumbel_draft_tokens_follow_softmax():
+    """Gumbel-max draws follow softmax(logits/T): frequency check on a tiny row."""
+    rng = np.random.default_rng(0)
+    z = np.array([[0.0, 1.0, 2.0, -1.0]] * 20000, np.float32)
+    t = W.gumbel_argmax(rng, z, 1.0)
+    f = np.bincount(t, minlength=4) / len(t)
+    p = np.exp(z[0]) / np.exp(z[0]).sum()
+    assert np.max(np.abs(f - p)) < 0.015
+
+
+def test_tree_topology_counts_36_nodes():
+    par = W.tree_topology(7, 4)
+    assert par.shape == (36,) and par[0] == -1
+    assert all(0 <= par[n] < n for n in range(1, 36))
+    assert list(par[1:8]) == list(range(7))          # main chain
+    children_of_root = [n for n in range(36) if par[n] == 0]
+    assert children_of_root == [1, 8, 9, 10, 11]
+
+
+def test_tree_match_rate():
+    t = W.make_tree(B=16, V=4000)
+    g = np.argmax(t.target, axis=2)
+    match = np.array([[t.node_tokens[b, n] == g[b, t.parents[b, n]] for n in range(1, t.N)]
+                      for b in range(t.B)])
+    assert abs(match.mean() - 0.7) < 0.06
+    assert (t.node_tokens[:, 0] == -1).all()
