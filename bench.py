@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Throughput of the speculative-decoding verification hot path on GB300.
+
+One step is one pass of the whole hot path over one batch of the chain-b64
+workload (B=64 sequences, gamma=7 drafts, V=151936, bf16 logits, T=0.6,
+draft noise sigma in {0.25, 1, 4}): stochastic verification (row statistics,
+accept decisions, residual/bonus sample), greedy verification of the same
+drafts, and greedy tree verification of the same drafts laid out as a
+chain-shaped tree.  The metric is verified rows per second, rows being
+(sequence, position) pairs: 3 * B * (gamma+1) per step.
+
+Own arm (default): inputs resident in HBM, CUDA-event timing of exactly K
+steps after W warm-up steps, 4 rotating input copies (1.17 GB, > 4x the
+129 MB L2) so every call reads cold logits.  Also reported: the end-to-end
+rate through the public calls with host buffers (pinned H2D of the inputs and
+D2H of the outputs inside the timed region), the roofline of the dominant
+kernel (the streaming row-statistics pass), clocks during the timed region and the
+fp64 CPU oracle timed on the host cores.
+
+Reference arm (--impl reference): the fp64 CPU oracle, as it stands, on a
+bounded slice of the same workload per step, timed on the host cores.
+
+Multi-GPU (torchrun, one process per GPU): every rank verifies its own
+batch (weak scaling, no collective on the data path); the slowest rank's
+time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verified rows/s & achieved HBM GB/s (fraction of GB300 roofline) at V=151936"
+UNIT = "rows/s"
+ROTATE = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def chain_tree(x):
+    """The batch's drafts as a chain-shaped draft tree: node 0 is the root,
+    node i+1 carries draft x_i and hangs under node i."""
+    B, g = x.draft_tokens.shape
+    par = np.tile(np.arange(-1, g, dtype=np.int32), (B, 1))
+    tok = np.concatenate([np.full((B, 1), -1, np.int32), x.draft_tokens], axis=1)
+    return np.ascontiguousarray(tok), np.ascontiguousarray(par)
+
+
+def step_accounting(x):
+    elt = 2 if x.dtype == "bf16" else 4
+    rows_chain = x.B * (x.gamma + 1)
+    bytes_decide = x.B * (2 * x.gamma + 1) * x.V * elt
+    bytes_greedy = x.B * (x.gamma + 1) * x.V * elt
+    return {
+        "rows": 3 * rows_chain,
+        "bytes_decide": bytes_decide,
+        "bytes_step": bytes_decide + 2 * bytes_greedy,
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    """Hash of the sources that define the decide kernel; ncu traffic figures
+    recorded under profiles/ are only reported while it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_59_gb300", "csrc")
+    for f in ("sv_common.cuh", "sv_internal.h", "sv_sample.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """dram bytes per launch of the decide kernel from the committed ncu
+    summary (profiles/decide_traffic.txt: key=value lines), or None."""
+    p = os.path.join(ROOT, "profiles", "decide_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if "=" in line and not line.lstrip().startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_hash") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the benchmark runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not win and self.samples:                       # short run: nearest samples
+            mid = 0.5 * (t0 + t1)
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(win[0][3]), "reasons": reasons, "samples": len(win)}
+
+
+# ------------------------------------------------------------------ own arm
+def run_own(args):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_59_gb300 as sv
+    from speculative_decoding_verification_59_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    x = W.make_chain(args.workload, seed=W.WORKLOADS[args.workload].seed + 1000 * rank)
+    ttok, tpar = chain_tree(x)
+    acct = step_accounting(x)
+    B, g, V = x.B, x.gamma, x.V
+    tdt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    dcode = sv.SPEC_DTYPE_BF16 if x.dtype == "bf16" else sv.SPEC_DTYPE_F32
+
+    host = {
+        "zt": torch.from_numpy(x.target).to(tdt).pin_memory(),
+        "zd": torch.from_numpy(x.draft).to(tdt).pin_memory(),
+        "x": torch.from_numpy(x.draft_tokens).pin_memory(),
+        "u": torch.from_numpy(x.uniforms).pin_memory(),
+        "tt": torch.from_numpy(ttok).pin_memory(),
+        "tp": torch.from_numpy(tpar).pin_memory(),
+    }
+    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(ROTATE)]
+    out = {
+        "s_tok": torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+        "s_acc": torch.empty((B,), dtype=torch.int32, device=dev),
+        "g_tok": torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+        "g_acc": torch.empty((B,), dtype=torch.int32, device=dev),
+        "t_nodes": torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+        "t_tok": torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+        "t_acc": torch.empty((B,), dtype=torch.int32, device=dev),
+    }
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get(B, g + 1, V)       # the chain-shaped tree has g+1 nodes
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    P = lambda t: t.data_ptr()  # noqa: E731
+
+    def check(st, what):
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, what)
+
+    def calls(s, ev=None):
+        c0, c1, c2 = copies[s % ROTATE], copies[(s + 1) % ROTATE], copies[(s + 2) % ROTATE]
+        if ev is not None:
+            ev[0].record(stream)
+        check(sv.spec_verify_sample_stats(P(c0["zt"]), P(c0["zd"]), dcode, x.T, B, g, V, wp, wb,
+                                          sh), "stats")
+        if ev is not None:
+            ev[1].record(stream)
+        check(sv.spec_verify_sample_finish(P(c0["zt"]), P(c0["zd"]), dcode, P(c0["x"]), P(c0["u"]),
+                                           x.T, B, g, V, P(out["s_tok"]), P(out["s_acc"]), None,
+                                           wp, wb, sh), "finish")
+        check(sv.spec_verify_greedy(P(c1["zt"]), dcode, P(c1["x"]), B, g, V, P(out["g_tok"]),
+                                    P(out["g_acc"]), wp, wb, sh), "greedy")
+        check(sv.spec_verify_tree_greedy(P(c2["zt"]), dcode, P(c2["tt"]), P(c2["tp"]), B, g + 1, V,
+                                         P(out["t_nodes"]), P(out["t_tok"]), P(out["t_acc"]), wp,
+                                         wb, sh), "tree")
+
+    def barrier():
+        if world > 1:
+            dist.barrier(device_ids=[local])
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    gpu_id = local
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id)
+
+    # warm-up (also settles clocks)
+    for s in range(args.warmup):
+        calls(s)
+    barrier()
+
+    # ---- device-resident timed region
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for s in range(K):
+        calls(s, evs[s])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    ms = e0.elapsed_time(e1)
+    decide_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_max = max_over_ranks(ms)
+    barrier()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    # outputs of the last step, for tau
+    s_acc = out["s_acc"].cpu().numpy()
+    g_acc = out["g_acc"].cpu().numpy()
+    tau_sample = float((s_acc + 1).mean())
+    tau_greedy = float((g_acc + 1).mean())
+
+    # ---- end-to-end through the public calls with host buffers
+    Ke = args.steps if args.e2e_steps is None else args.e2e_steps
+    stage = copies[0]
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    lp = torch.empty((B, g, 2), dtype=torch.float32, device=dev)
+    h_lp = torch.empty((B, g, 2), dtype=torch.float32).pin_memory()
+    bi = sum(v.numel() * v.element_size() for v in host.values())
+    bo = sum(v.numel() * v.element_size() for v in out.values()) + lp.numel() * 4
+
+    def e2e_step():
+        for k, v in host.items():
+            stage[k].copy_(v, non_blocking=True)
+        check(sv.spec_verify_sample(P(stage["zt"]), P(stage["zd"]), dcode, P(stage["x"]),
+                                    P(stage["u"]), x.T, B, g, V, P(out["s_tok"]), P(out["s_acc"]),
+                                    P(lp), wp, wb, sh), "sample")
+        check(sv.spec_verify_greedy(P(stage["zt"]), dcode, P(stage["x"]), B, g, V, P(out["g_tok"]),
+                                    P(out["g_acc"]), wp, wb, sh), "greedy")
+        check(sv.spec_verify_tree_greedy(P(stage["zt"]), dcode, P(stage["tt"]), P(stage["tp"]), B,
+                                         g + 1, V, P(out["t_nodes"]), P(out["t_tok"]),
+                                         P(out["t_acc"]), wp, wb, sh), "tree")
+        for k, v in out.items():
+            h_out[k].copy_(v, non_blocking=True)
+        h_lp.copy_(lp, non_blocking=True)
+
+    for _ in range(min(3, Ke)):
+        e2e_step()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1))
+    clocks.stop()
+
+    # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_timing(x, ttok, tpar, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        peak, peak_src = measured_peaks()
+        decide_mean_ms = statistics.mean(decide_ms)
+        achieved = acct["bytes_decide"] / (decide_mean_ms * 1e-3) / 1e9
+        traffic = recorded_traffic(args.workload)
+        value = world * acct["rows"] * K / (ms_max * 1e-3)
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": ms_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded generator, chain-b64 recipe)",
+            "config": {
+                "workload": args.workload,
+                "B": B, "gamma": g, "V": V, "logits": x.dtype, "temperature": x.T,
+                "step": "sample (stats+finish) + greedy + chain-shaped tree, each on its own "
+                        "rotating input copy",
+                "l2": f"{ROTATE} rotating input copies of {acct['bytes_decide'] / 1e6:.1f} MB "
+                      "(> 4x the 129 MB L2): every call reads cold logits",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "hbm_gbs_step": world * acct["bytes_step"] * K / (ms_max * 1e-3) / 1e9,
+            "rounds_per_s": world * x.B * K / (ms_max * 1e-3),
+            "tau": {"sample": tau_sample, "greedy": tau_greedy},
+            "roofline": {
+                "kernel": "sample_rowstats_kernel (spec_verify_sample_stats)",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "peak_source": f"{peak_src} hbm copy rate",
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "frac_of_8tbs_nominal": achieved / 8000.0,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": acct["bytes_decide"],
+                "launch_ms_mean": decide_mean_ms,
+            },
+            "e2e": {
+                "value": world * acct["rows"] * Ke / (e2e_ms * 1e-3),
+                "unit": UNIT,
+                "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo,
+                "steps": Ke,
+            },
+            "gpu_launches": 4 * K,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def oracle_slice(x, n, ttok, tpar, nthreads):
+    """The oracle over the first n sequences of the batch: sample, greedy and
+    the chain-shaped tree.  Returns verified rows."""
+    import oracle
+    sl = slice(0, n)
+    oracle.verify_sample(x.target[sl], x.draft[sl], x.draft_tokens[sl], x.uniforms[sl], x.T,
+                         nthreads=nthreads)
+    oracle.verify_greedy(x.target[sl], x.draft_tokens[sl], nthreads=nthreads)
+    oracle.verify_tree_greedy(x.target[sl], ttok[sl], tpar[sl], nthreads=nthreads)
+    return 3 * n * (x.gamma + 1)
+
+
+def oracle_timing(x, ttok, tpar, budget_s=10.0):
+    cores = os.cpu_count() or 1
+    n = min(x.B, max(1, cores))
+    rows, t = 0, 0.0
+    reps = 0
+    while t < budget_s and reps < 64:
+        t0 = time.perf_counter()
+        rows += oracle_slice(x, n, ttok, tpar, cores)
+        t += time.perf_counter() - t0
+        reps += 1
+    return {"value": rows / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x the first {n} sequences of the batch (sample + greedy + tree), "
+                      f"{t:.1f} s wall on {cores} threads"}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_59_gb300 import workloads as W
+    x = W.make_chain(args.workload)
+    ttok, tpar = chain_tree(x)
+    cores = os.cpu_count() or 1
+    # each step: one sequence per core, all cores, bounded so K + W steps stay within minutes
+    n = min(x.B, cores)
+    for _ in range(args.warmup):
+        oracle_slice(x, 1, ttok, tpar, 1)
+    rows, t = 0, 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        rows += oracle_slice(x, n, ttok, tpar, cores)
+        t += time.perf_counter() - t0
+    value = rows / t
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded generator, chain-b64 recipe)",
+        "config": {"workload": args.workload, "B": x.B, "gamma": x.gamma, "V": x.V,
+                   "logits": x.dtype, "temperature": x.T,
+                   "step": f"fp64 CPU oracle on {n} of the {x.B} sequences (sample + greedy + "
+                           "chain-shaped tree)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {n} sequences on {cores} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["own", "reference"], default="own")
+    ap.add_argument("--workload", default="chain-b64",
+                    choices=["chain-small", "chain-b8", "chain-b64", "chain-b256"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        args.steps = 10 if args.steps is None else args.steps
+        args.warmup = 3 if args.warmup is None else args.warmup
+        run_reference(args)
+    else:
+        args.steps = 2000 if args.steps is None else args.steps
+        args.warmup = 50 if args.warmup is None else args.warmup
+        if args.warmup < 3:
+            raise SystemExit("at least 3 warm-up steps are required")
+        run_own(args)
+
+
+if __name__ == "__main__":
+    main()

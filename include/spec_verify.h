@@ -1,0 +1,187 @@
+/*
+ * spec_verify.h - C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * The operation is the target-model verification step of speculative
+ * decoding as defined in:
+ *   [SD]     "Speculative decoding: guess a few tokens first - why the answer
+ *            stays the same" (explainer blog).  Section "What happens in one
+ *            round": the target scores all gamma drafts (plus one position)
+ *            in one batch, drafts are checked left to right and accepted with
+ *            probability min(1, p_i(x_i)/q_i(x_i)), the first rejection voids
+ *            the rest and is replaced by a sample from the residual; when all
+ *            drafts are accepted a bonus token is sampled from the next
+ *            position.  Section "Why fixing wrong guesses does not leave the
+ *            target distribution": residual p'(x) = norm(max(0, p(x) - q(x))).
+ *            The greedy paragraph: accept while the draft equals the target
+ *            argmax, replace the first mismatch by the target token.
+ *   [AdaPLD] "AdaPLD: adaptive retrieval and reuse for efficient model-free
+ *            speculative decoding", section 3.3 "Tree construction and
+ *            verification" and Algorithm 1 (BuildDraftTree / VerifyAndAccept):
+ *            a draft tree (main chain plus top-K branches) verified by the
+ *            target in one pass.
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a DEVICE pointer owned by the caller; the library never
+ *     allocates and keeps no per-call state.  Calls are asynchronous on
+ *     `stream`; results are valid once the stream reaches them.
+ *   - Logits are row-major with V contiguous, dtype SPEC_DTYPE_F32 or
+ *     SPEC_DTYPE_BF16.  Logit base pointers must be 16-byte aligned
+ *     (SPEC_ERR_MISALIGNED otherwise).  V need not be a multiple of anything.
+ *     -inf logits are legal (masked tokens); NaN/+inf logits are undefined.
+ *   - `workspace` is caller-owned device scratch of at least
+ *     spec_verify_workspace_size() bytes, 256-byte aligned.  Its first 4
+ *     bytes are the device error word (below): zero-fill the workspace once
+ *     (spec_verify_workspace_init) so that word starts clear.  Everything
+ *     else in it is rewritten by each call before it is read, so one
+ *     workspace serves calls of any mode and size.  Calls that share a
+ *     workspace must be ordered on the device (same stream, or events);
+ *     overlapping calls on one workspace race.
+ *   - Host-side argument checks return immediately without touching the
+ *     device.  Bad input that only the device can see (a draft token outside
+ *     [0, V), a row with every logit -inf, a malformed tree) marks that
+ *     sequence with num_accepted = -1 and every output token -1, and sets a
+ *     bit in the workspace error word (see spec_verify_read_error).
+ *   - B = 0 is an empty batch: SPEC_OK, nothing is launched.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad temperature */
+    SPEC_ERR_UNSUPPORTED_DTYPE = 2,
+    SPEC_ERR_MISALIGNED = 3,           /* logits or workspace not aligned as required */
+    SPEC_ERR_WORKSPACE_TOO_SMALL = 4,
+    SPEC_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
+    SPEC_ERR_DEVICE_INPUT = 6          /* reported by spec_verify_read_error only */
+} spec_status_t;
+
+typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
+
+/* Bits of the device error word. */
+#define SPEC_DEVERR_TOKEN_RANGE  1   /* a draft / node token outside [0, V) */
+#define SPEC_DEVERR_EMPTY_ROW    2   /* a logits row whose every entry is -inf (sampling) */
+#define SPEC_DEVERR_TREE_PARENT  4   /* parents[0] != -1 or parents[n] not in [0, n) */
+
+/*
+ * Bytes of workspace any of the three verification calls needs for B
+ * sequences of `gamma_or_nodes` drafts (chains) or nodes (trees) over a
+ * vocabulary of V, for either dtype.  Returns 0 for invalid sizes.
+ */
+size_t spec_verify_workspace_size(int B, int gamma_or_nodes, int V);
+
+/* Zero-fills a workspace (cudaMemsetAsync on `stream`). */
+spec_status_t spec_verify_workspace_init(void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/*
+ * Stochastic verification of B independent draft chains ([SD] "What happens in
+ * one round", steps 1-4, and the residual of "Why fixing wrong guesses ...").
+ *
+ *   target_logits [B, gamma+1, V]  target logits z^t; row i scores position i
+ *   draft_logits  [B, gamma, V]    draft logits z^d (NULL allowed if gamma == 0)
+ *   draft_tokens  [B, gamma] int32 drafted tokens x_0..x_{gamma-1}
+ *   uniforms      [B, gamma+1] f32 in [0, 1): u_i decides draft i (accepted iff
+ *                                  u_i < p_i(x_i)/q_i(x_i)); u_gamma drives the
+ *                                  single final sample (residual or bonus) by
+ *                                  inverse CDF in index order
+ *   temperature   > 0, finite; p = softmax(z^t / T), q = softmax(z^d / T)
+ *   0 <= gamma <= 256, V >= 1, B >= 0.  V is also bounded by the final pass,
+ *   which stages one row pair per thread-block cluster (16 CTAs at most) in
+ *   shared memory: V <= 16 * floor((opt-in shared memory per block - 1024) / 8),
+ *   462848 on GB300; larger V returns SPEC_ERR_INVALID_ARG.
+ * Outputs (device):
+ *   out_tokens       [B, gamma+1] int32: the k accepted drafts, the final
+ *                    token, then -1
+ *   out_num_accepted [B] int32: k in [0, gamma] (emitted tokens = k + 1)
+ *   out_logprobs     [B, gamma, 2] f32, nullable: ln p_i(x_i), ln q_i(x_i)
+ *
+ * Two kernels run: a streaming pass over every logit row (row max and
+ * sum-exp partials) and one thread-block cluster per sequence that takes the
+ * accept decisions and samples from the one rejected (or bonus) row pair.
+ */
+spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const float* uniforms, float temperature, int B, int gamma,
+                                 int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                 float* out_logprobs, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
+ * The two halves of spec_verify_sample, for callers that want to overlap or
+ * time them separately; spec_verify_sample is exactly _stats then _finish on
+ * the same stream with the same arguments and workspace.
+ *   _stats:  streams every logit row once and leaves per-row partial
+ *            statistics (running max and sum of exponentials) in the
+ *            workspace.  Writes no output.
+ *   _finish: merges those statistics, takes the accept decisions and draws
+ *            the final token of every sequence (residual after a rejection,
+ *            bonus otherwise); writes every output of spec_verify_sample.
+ * The workspace and the logits must stay unchanged between the two calls.
+ */
+spec_status_t spec_verify_sample_stats(const void* target_logits, const void* draft_logits,
+                                       spec_dtype_t dtype, float temperature, int B, int gamma,
+                                       int V, void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
+spec_status_t spec_verify_sample_finish(const void* target_logits, const void* draft_logits,
+                                        spec_dtype_t dtype, const int32_t* draft_tokens,
+                                        const float* uniforms, float temperature, int B,
+                                        int gamma, int V, int32_t* out_tokens,
+                                        int32_t* out_num_accepted, float* out_logprobs,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/*
+ * Greedy verification ([SD] greedy paragraph): g_i = argmax_j z^t[b,i,j]
+ * (lowest index among equal logits), k = first i with x_i != g_i, else gamma.
+ * Draft logits are not needed.
+ *   target_logits [B, gamma+1, V], draft_tokens [B, gamma] (NULL if gamma == 0)
+ *   out_tokens [B, gamma+1]: x_0..x_{k-1}, g_k, then -1;  out_num_accepted [B]: k
+ */
+spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
+                                 const int32_t* draft_tokens, int B, int gamma, int V,
+                                 int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Greedy verification of a draft tree ([AdaPLD] 3.3, Algorithm 1).
+ *   target_logits [B, N, V]: row n scores the continuation after node n
+ *   node_tokens   [B, N] int32: token of node n (node 0, the root, is ignored)
+ *   parents       [B, N] int32: parents[0] = -1, 0 <= parents[n] < n
+ * A node is accepted when its parent is accepted and its token equals the
+ * argmax of the parent's row (the root is accepted).  Result: the longest
+ * root path of accepted nodes (ties: lexicographically smallest node ids) and
+ * the bonus token argmax(row of the path's last node).
+ *   out_path_nodes   [B, N]: path node ids (root excluded), then -1
+ *   out_tokens       [B, N]: path tokens, then the bonus token, then -1
+ *   out_num_accepted [B]: path length
+ */
+spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dtype,
+                                      const int32_t* node_tokens, const int32_t* parents, int B,
+                                      int N, int V, int32_t* out_path_nodes, int32_t* out_tokens,
+                                      int32_t* out_num_accepted, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, returns the accumulated SPEC_DEVERR_* bits of the
+ * workspace in *code and clears them.  SPEC_OK when the read succeeded (code
+ * may still be nonzero).
+ */
+spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* spec_verify_status_string(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

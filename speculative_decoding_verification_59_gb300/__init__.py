@@ -1,0 +1,273 @@
+"""GB300 (sm_103a) speculative-decoding verification.
+
+A thin ctypes binding over the C ABI of libspecverify.so (declared in
+include/spec_verify.h).  The functions named ``spec_verify_*`` take raw device
+pointers and sizes exactly like the C calls; the ``verify_*`` helpers only
+marshal torch CUDA tensors into those calls (pointers, current stream,
+output allocation).  Every step of the verification runs in the library's
+CUDA kernels: there is no CPU or PyTorch fallback, and using the package
+without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "SPEC_OK", "SPEC_DTYPE_F32", "SPEC_DTYPE_BF16", "SpecVerifyError", "lib_path", "load_library",
+    "spec_verify_workspace_size", "spec_verify_workspace_init", "spec_verify_sample",
+    "spec_verify_sample_stats", "spec_verify_sample_finish",
+    "spec_verify_greedy", "spec_verify_tree_greedy", "spec_verify_read_error",
+    "spec_verify_status_string", "Workspace", "verify_sample", "verify_greedy", "verify_tree_greedy",
+]
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED_DTYPE = 2
+SPEC_ERR_MISALIGNED = 3
+SPEC_ERR_WORKSPACE_TOO_SMALL = 4
+SPEC_ERR_CUDA = 5
+SPEC_ERR_DEVICE_INPUT = 6
+SPEC_DTYPE_F32 = 0
+SPEC_DTYPE_BF16 = 1
+SPEC_DEVERR_TOKEN_RANGE = 1
+SPEC_DEVERR_EMPTY_ROW = 2
+SPEC_DEVERR_TREE_PARENT = 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+_lib = None
+
+# name -> (argtypes, restype); pointers travel as c_void_p, the stream as c_void_p
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "spec_verify_workspace_size": ([_I, _I, _I], _S),
+    "spec_verify_workspace_init": ([_P, _S, _P], _I),
+    "spec_verify_sample": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _S,
+                            _P], _I),
+    "spec_verify_sample_stats": ([_P, _P, _I, ctypes.c_float, _I, _I, _I, _P, _S, _P], _I),
+    "spec_verify_sample_finish": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P,
+                                   _S, _P], _I),
+    "spec_verify_greedy": ([_P, _I, _P, _I, _I, _I, _P, _P, _P, _S, _P], _I),
+    "spec_verify_tree_greedy": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
+    "spec_verify_read_error": ([_P, _P, _P], _I),
+    "spec_verify_status_string": ([_I], ctypes.c_char_p),
+}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {spec_verify_status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libspecverify.so (built in-tree by __graft_entry__.build() or
+    speculative_decoding_verification_59_gb300._build).  Raises if missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is not built; run __graft_entry__.build() first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (argt, rest) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argt
+            fn.restype = rest
+        _lib = lib
+    return _lib
+
+
+# ---- raw C-ABI calls (pointers are ints, stream is an int handle or 0) ------
+def spec_verify_workspace_size(B: int, gamma_or_nodes: int, V: int) -> int:
+    return load_library().spec_verify_workspace_size(B, gamma_or_nodes, V)
+
+
+def spec_verify_workspace_init(ws: int, nbytes: int, stream: int = 0) -> int:
+    return load_library().spec_verify_workspace_init(ws, nbytes, stream)
+
+
+def spec_verify_sample(target, draft, dtype, draft_tokens, uniforms, temperature, B, gamma, V,
+                       out_tokens, out_num_accepted, out_logprobs, ws, ws_bytes, stream) -> int:
+    return load_library().spec_verify_sample(target, draft, dtype, draft_tokens, uniforms,
+                                             temperature, B, gamma, V, out_tokens,
+                                             out_num_accepted, out_logprobs, ws, ws_bytes, stream)
+
+
+def spec_verify_sample_stats(target, draft, dtype, temperature, B, gamma, V, ws, ws_bytes,
+                             stream) -> int:
+    return load_library().spec_verify_sample_stats(target, draft, dtype, temperature, B, gamma, V,
+                                                   ws, ws_bytes, stream)
+
+
+def spec_verify_sample_finish(target, draft, dtype, draft_tokens, uniforms, temperature, B, gamma,
+                              V, out_tokens, out_num_accepted, out_logprobs, ws, ws_bytes,
+                              stream) -> int:
+    return load_library().spec_verify_sample_finish(target, draft, dtype, draft_tokens, uniforms,
+                                                    temperature, B, gamma, V, out_tokens,
+                                                    out_num_accepted, out_logprobs, ws, ws_bytes,
+                                                    stream)
+
+
+def spec_verify_greedy(target, dtype, draft_tokens, B, gamma, V, out_tokens, out_num_accepted,
+                       ws, ws_bytes, stream) -> int:
+    return load_library().spec_verify_greedy(target, dtype, draft_tokens, B, gamma, V, out_tokens,
+                                             out_num_accepted, ws, ws_bytes, stream)
+
+
+def spec_verify_tree_greedy(target, dtype, node_tokens, parents, B, N, V, out_path_nodes,
+                            out_tokens, out_num_accepted, ws, ws_bytes, stream) -> int:
+    return load_library().spec_verify_tree_greedy(target, dtype, node_tokens, parents, B, N, V,
+                                                  out_path_nodes, out_tokens, out_num_accepted,
+                                                  ws, ws_bytes, stream)
+
+
+def spec_verify_read_error(ws: int, stream: int = 0):
+    code = ctypes.c_int32(0)
+    st = load_library().spec_verify_read_error(ws, stream, ctypes.addressof(code))
+    return st, code.value
+
+
+def spec_verify_status_string(status: int) -> str:
+    try:
+        return load_library().spec_verify_status_string(status).decode()
+    except ImportError:
+        return "status %d" % status
+
+
+# ---- torch marshalling ----------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SPEC_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_DTYPE_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != SPEC_OK:
+        raise SpecVerifyError(status, what)
+
+
+class Workspace:
+    """Device scratch for the verification calls, zero-filled at creation (the
+    error word must start clear).  Grows on demand."""
+
+    def __init__(self, device=None):
+        torch = _torch()
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = None
+
+    def get(self, B: int, g: int, V: int, stream=None):
+        torch = _torch()
+        need = spec_verify_workspace_size(B, g, V)
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            _check(spec_verify_workspace_init(self.buf.data_ptr(), self.buf.numel(), _stream(stream)),
+                   "spec_verify_workspace_init")
+        return self.buf.data_ptr(), self.buf.numel()
+
+    def read_error(self, stream=None) -> int:
+        st, code = spec_verify_read_error(self.buf.data_ptr(), _stream(stream))
+        _check(st, "spec_verify_read_error")
+        return code
+
+
+_default_ws = {}
+
+
+def _ws(workspace, device):
+    if workspace is not None:
+        return workspace
+    key = str(device)
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(device)
+    return _default_ws[key]
+
+
+def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, logprobs=False,
+                  workspace: Optional[Workspace] = None, out=None, stream=None):
+    """Stochastic verification (see spec_verify_sample).  target [B, g+1, V],
+    draft [B, g, V] (same dtype), draft_tokens [B, g] int32, uniforms
+    [B, g+1] float32, all contiguous CUDA tensors.  Returns (tokens [B, g+1],
+    num_accepted [B]) or, with logprobs=True, also [B, g, 2] log-probabilities."""
+    torch = _torch()
+    B, g1, V = target.shape
+    g = g1 - 1
+    dev = target.device
+    if out is None:
+        tok = torch.empty((B, g1), dtype=torch.int32, device=dev)
+        acc = torch.empty((B,), dtype=torch.int32, device=dev)
+        lp = torch.empty((B, g, 2), dtype=torch.float32, device=dev) if logprobs else None
+    else:
+        tok, acc, lp = out
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get(B, g, V, stream)
+    st = spec_verify_sample(_ptr(target), _ptr(draft) if g > 0 else None, _dtype_code(target),
+                            _ptr(draft_tokens) if g > 0 else None, _ptr(uniforms),
+                            float(temperature), B, g, V, _ptr(tok), _ptr(acc), _ptr(lp), wp, wb,
+                            _stream(stream))
+    _check(st, "spec_verify_sample")
+    return (tok, acc, lp) if logprobs else (tok, acc)
+
+
+def verify_greedy(target, draft_tokens, *, workspace: Optional[Workspace] = None, out=None,
+                  stream=None):
+    """Greedy verification (see spec_verify_greedy).  Returns (tokens, num_accepted)."""
+    torch = _torch()
+    B, g1, V = target.shape
+    g = g1 - 1
+    dev = target.device
+    if out is None:
+        tok = torch.empty((B, g1), dtype=torch.int32, device=dev)
+        acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        tok, acc = out
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get(B, g, V, stream)
+    st = spec_verify_greedy(_ptr(target), _dtype_code(target), _ptr(draft_tokens) if g > 0 else None,
+                            B, g, V, _ptr(tok), _ptr(acc), wp, wb, _stream(stream))
+    _check(st, "spec_verify_greedy")
+    return tok, acc
+
+
+def verify_tree_greedy(target, node_tokens, parents, *, workspace: Optional[Workspace] = None,
+                       out=None, stream=None):
+    """Greedy tree verification (see spec_verify_tree_greedy).  Returns
+    (path_nodes [B, N], tokens [B, N], num_accepted [B])."""
+    torch = _torch()
+    B, N, V = target.shape
+    dev = target.device
+    if out is None:
+        nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+        tok = torch.empty((B, N), dtype=torch.int32, device=dev)
+        acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        nodes, tok, acc = out
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get(B, N, V, stream)
+    st = spec_verify_tree_greedy(_ptr(target), _dtype_code(target), _ptr(node_tokens),
+                                 _ptr(parents), B, N, V, _ptr(nodes), _ptr(tok), _ptr(acc), wp, wb,
+                                 _stream(stream))
+    _check(st, "spec_verify_tree_greedy")
+    return nodes, tok, acc

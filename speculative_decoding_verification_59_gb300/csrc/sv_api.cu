@@ -1,0 +1,175 @@
+// The C ABI of libspecverify.so: argument validation, workspace sizing and
+// dispatch to the launchers.  Declarations and their contracts are in
+// include/spec_verify.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "sv_internal.h"
+
+namespace sv {
+
+constexpr int kMaxGammaApi = 256;
+constexpr int kMaxNodesApi = 1024;
+
+cudaError_t device_info(DeviceInfo* out) {
+    // Cached per device ordinal; the values are immutable properties.
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && have[dev]) { *out = cache[dev]; return cudaSuccess; }
+    DeviceInfo d;
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) { cache[dev] = d; have[dev] = true; }
+    *out = d;
+    return cudaSuccess;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static spec_status_t check_ws(void* ws, size_t bytes, int B, int g, int V) {
+    if (!ws) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return SPEC_ERR_MISALIGNED;
+    if (bytes < ws_layout(B, g, V).total) return SPEC_ERR_WORKSPACE_TOO_SMALL;
+    return SPEC_OK;
+}
+
+static spec_status_t to_status(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int B, int gamma_or_nodes, int V) {
+    if (B < 0 || gamma_or_nodes < 0 || V <= 0) return 0;
+    return ws_layout(B, gamma_or_nodes, V).total;
+}
+
+spec_status_t spec_verify_workspace_init(void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+    if (!workspace) return SPEC_ERR_INVALID_ARG;
+    return to_status(cudaMemsetAsync(workspace, 0, workspace_bytes, stream));
+}
+
+static spec_status_t sample_common(const void* target_logits, const void* draft_logits,
+                                   spec_dtype_t dtype, const int32_t* draft_tokens,
+                                   const float* uniforms, float temperature, int B, int gamma,
+                                   int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                   float* out_logprobs, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream, int parts) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 0 || gamma > kMaxGammaApi || V <= 0) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || (gamma > 0 && !draft_logits)) return SPEC_ERR_INVALID_ARG;
+    if ((parts & kSampleFinish) &&
+        (!uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16) || (gamma > 0 && !aligned(draft_logits, 16)))
+        return SPEC_ERR_MISALIGNED;
+    spec_status_t s = check_ws(workspace, workspace_bytes, B, gamma, V);
+    if (s != SPEC_OK) return s;
+    if ((parts & kSampleFinish) && !sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
+    return to_status(launch_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                                   temperature, B, gamma, V, out_tokens, out_num_accepted,
+                                   out_logprobs, workspace, stream, parts));
+}
+
+spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const float* uniforms, float temperature, int B, int gamma,
+                                 int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                 float* out_logprobs, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    return sample_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                         B, gamma, V, out_tokens, out_num_accepted, out_logprobs, workspace,
+                         workspace_bytes, stream, kSampleStats | kSampleFinish);
+}
+
+spec_status_t spec_verify_sample_stats(const void* target_logits, const void* draft_logits,
+                                       spec_dtype_t dtype, float temperature, int B, int gamma,
+                                       int V, void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
+    return sample_common(target_logits, draft_logits, dtype, nullptr, nullptr, temperature, B,
+                         gamma, V, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream,
+                         kSampleStats);
+}
+
+spec_status_t spec_verify_sample_finish(const void* target_logits, const void* draft_logits,
+                                        spec_dtype_t dtype, const int32_t* draft_tokens,
+                                        const float* uniforms, float temperature, int B,
+                                        int gamma, int V, int32_t* out_tokens,
+                                        int32_t* out_num_accepted, float* out_logprobs,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+    return sample_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                         B, gamma, V, out_tokens, out_num_accepted, out_logprobs, workspace,
+                         workspace_bytes, stream, kSampleFinish);
+}
+
+spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
+                                 const int32_t* draft_tokens, int B, int gamma, int V,
+                                 int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 0 || gamma + 1 > kMaxNodesApi || V <= 0) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens))
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16)) return SPEC_ERR_MISALIGNED;
+    spec_status_t s = check_ws(workspace, workspace_bytes, B, gamma, V);
+    if (s != SPEC_OK) return s;
+    return to_status(launch_greedy(target_logits, dtype, draft_tokens, B, gamma, V, out_tokens,
+                                   out_num_accepted, workspace, stream));
+}
+
+spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dtype,
+                                      const int32_t* node_tokens, const int32_t* parents, int B,
+                                      int N, int V, int32_t* out_path_nodes, int32_t* out_tokens,
+                                      int32_t* out_num_accepted, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || N <= 0 || N > kMaxNodesApi || V <= 0) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !node_tokens || !parents || !out_path_nodes || !out_tokens ||
+        !out_num_accepted)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16)) return SPEC_ERR_MISALIGNED;
+    spec_status_t s = check_ws(workspace, workspace_bytes, B, N, V);
+    if (s != SPEC_OK) return s;
+    return to_status(launch_tree(target_logits, dtype, node_tokens, parents, B, N, V,
+                                 out_path_nodes, out_tokens, out_num_accepted, workspace, stream));
+}
+
+spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32_t* code) {
+    if (!workspace || !code) return SPEC_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    *code = v;
+    return SPEC_OK;
+}
+
+const char* spec_verify_status_string(spec_status_t status) {
+    switch (status) {
+        case SPEC_OK: return "ok";
+        case SPEC_ERR_INVALID_ARG: return "invalid argument";
+        case SPEC_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+        case SPEC_ERR_MISALIGNED: return "misaligned pointer (logits need 16 bytes, workspace 256)";
+        case SPEC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case SPEC_ERR_CUDA: return "CUDA runtime error";
+        case SPEC_ERR_DEVICE_INPUT: return "bad input detected on the device";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// Device helpers shared by the verification kernels: streaming loads, the
+// per-lane view of a warp chunk of logits, warp reductions and compensated
+// summation.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "sv_internal.h"
+
+namespace sv {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// 16-byte read-only streaming load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// 2^x on the special-function unit (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& v, int c) {
+    return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// One logit as float.  ELT = 2: bfloat16 bits, ELT = 4: fp32.
+template <int ELT>
+__device__ __forceinline__ float load_logit(const char* row, int j) {
+    if constexpr (ELT == 4) {
+        return __ldg(reinterpret_cast<const float*>(row) + j);
+    } else {
+        unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(row) + j);
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+}
+
+// The part of a warp chunk one lane holds.  Vectorised layout: 8 vectors of
+// 16 bytes at element offsets base + (lane + 32 t) * PV (PV = 16 / ELT),
+// requiring 16-byte aligned rows.  Scalar layout (any alignment): elements
+// base + lane + 32 i.  Either way val(i) walks the lane's elements in
+// increasing index order and out-of-row elements read as -inf.
+template <int ELT, bool VEC>
+struct LaneChunk;
+
+template <int ELT>
+struct LaneChunk<ELT, true> {
+    static constexpr int PV = 16 / ELT;
+    static constexpr int EPL = kVecPerLane * PV;
+    uint4 r[kVecPerLane];
+
+    __device__ __forceinline__ void load(const char* row, int V, int base, int lane) {
+        const uint32_t ninf = ELT == 4 ? 0xff800000u : 0xff80ff80u;
+#pragma unroll
+        for (int t = 0; t < kVecPerLane; ++t) {
+            const int e = base + (lane + 32 * t) * PV;
+            if (e < V) r[t] = ld_stream16(row + (size_t)e * ELT);
+            else r[t] = make_uint4(ninf, ninf, ninf, ninf);
+        }
+    }
+    __device__ __forceinline__ float val(int i) const {
+        const int t = i / PV, e = i % PV;
+        if constexpr (ELT == 4) {
+            return __uint_as_float(u4_get(r[t], e));
+        } else {
+            const uint32_t w = u4_get(r[t], e >> 1);
+            return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+        }
+    }
+    __device__ __forceinline__ int idx(int base, int lane, int i) const {
+        return base + (lane + 32 * (i / PV)) * PV + (i % PV);
+    }
+};
+
+template <int ELT>
+struct LaneChunk<ELT, false> {
+    static constexpr int EPL = kVecPerLane * (16 / ELT);
+    float v[EPL];
+
+    __device__ __forceinline__ void load(const char* row, int V, int base, int lane) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = base + lane + 32 * i;
+            v[i] = e < V ? load_logit<ELT>(row, e) : kNegInf;
+        }
+    }
+    __device__ __forceinline__ float val(int i) const { return v[i]; }
+    __device__ __forceinline__ int idx(int base, int lane, int i) const {
+        return base + lane + 32 * i;
+    }
+};
+
+// ---- warp reductions -------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// (value, index) order for argmax: larger value first, lower index on ties.
+__device__ __forceinline__ bool am_better(float v1, int i1, float v2, int i2) {
+    return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (am_better(ov, oi, v, i)) { v = ov; i = oi; }
+    }
+}
+
+// ---- float-float accumulation (Knuth's TwoSum) -----------------------------
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void ff_add(FF& a, float x) {
+    const float s = a.hi + x;
+    const float bb = s - a.hi;
+    const float err = (a.hi - (s - bb)) + (x - bb);
+    a.hi = s;
+    a.lo += err;
+}
+
+__device__ __forceinline__ double ff_value(const FF& a) { return (double)a.hi + (double)a.lo; }
+
+// ---- programmatic dependent launch -------------------------------------------
+// The streaming kernel lets the next kernel in the stream begin launching
+// once each of its CTAs is on its last chunk; that kernel waits (in hardware)
+// until the streaming grid has completed and its writes are visible.  Both
+// are no-ops for a kernel launched without the programmatic attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+}  // namespace sv

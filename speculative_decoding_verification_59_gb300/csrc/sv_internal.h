@@ -1,0 +1,76 @@
+// Internal declarations shared by the translation units of libspecverify.so:
+// the workspace layout, the chunking constants and the launch entry points
+// that the C ABI (sv_api.cu) dispatches to.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+// One warp streams a "warp chunk" of 128 bytes per lane (8 x 16-byte vectors):
+// 2048 bf16 or 1024 fp32 logits.  A CTA of kWarps warps covers a "block
+// chunk" of kWarps consecutive warp chunks of one row.
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kLaneBytes = 128;
+constexpr int kVecPerLane = kLaneBytes / 16;
+
+inline int elt_size(spec_dtype_t dt) { return dt == SPEC_DTYPE_BF16 ? 2 : 4; }
+inline int warp_elems(int elt) { return 32 * kLaneBytes / elt; }
+inline int block_elems(int elt) { return kWarps * warp_elems(elt); }
+inline int nseg(int V, int elt) { return (V + block_elems(elt) - 1) / block_elems(elt); }
+
+// Workspace: [error word (256 bytes reserved) | per-warp row partials].
+// The partials are fully rewritten by the streaming pass of every call before
+// the second kernel of that call reads them, so a workspace carries nothing
+// from one call to the next except the error word, which only accumulates
+// error bits until spec_verify_read_error clears it.
+struct WsLayout {
+    size_t err_off, part_off, part_count, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
+    WsLayout L;
+    L.err_off = 0;
+    L.part_off = 256;
+    // rows: sampling needs 2g+1 per sequence, greedy g+1, trees N (<= 2N+1)
+    size_t rows = (size_t)B * (size_t)(2 * (size_t)gamma_or_nodes + 1);
+    // fp32 has the smaller warp chunk, hence the most partials per row
+    L.part_count = rows * (size_t)nseg(V, 4) * kWarps;
+    L.total = L.part_off + align256(sizeof(float2) * L.part_count);
+    return L;
+}
+
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+};
+// Cached per-device properties (SM count and shared-memory limit).
+cudaError_t device_info(DeviceInfo* out);
+
+// ---- launchers (return the first CUDA error) ------------------------------
+// parts: kSampleStats (streaming row statistics), kSampleFinish (accept
+// decisions and the final residual/bonus token), or both.
+constexpr int kSampleStats = 1;
+constexpr int kSampleFinish = 2;
+cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
+                          const float* u, float T, int B, int gamma, int V, int32_t* out_tok,
+                          int32_t* out_acc, float* out_lp, void* ws, cudaStream_t st, int parts);
+
+// Whether the final sampling pass can stage a row pair of this vocabulary.
+bool sample_supported_vocab(int V);
+
+cudaError_t launch_greedy(const void* zt, spec_dtype_t dt, const int32_t* x, int B, int gamma,
+                          int V, int32_t* out_tok, int32_t* out_acc, void* ws, cudaStream_t st);
+
+cudaError_t launch_tree(const void* zt, spec_dtype_t dt, const int32_t* tok, const int32_t* par,
+                        int B, int N, int V, int32_t* out_nodes, int32_t* out_tok,
+                        int32_t* out_acc, void* ws, cudaStream_t st);
+
+}  // namespace sv

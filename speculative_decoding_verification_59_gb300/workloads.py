@@ -122,11 +122,16 @@ class TreeInputs:
 
 def to_bf16_exact(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bfloat16 (ties to even) and return
-    them as float32.  Finite inputs only."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
-    return b.astype(np.uint32).view(np.float32)
+    them as float32.  Finite inputs only (|x| < 2^128, so the 32-bit
+    arithmetic below cannot wrap)."""
+    y = np.array(x, dtype=np.float32, copy=True, order="C")
+    b = y.reshape(-1).view(np.uint32)
+    step = 1 << 22
+    for i in range(0, b.size, step):
+        c = b[i:i + step]
+        c += np.uint32(0x7FFF) + ((c >> np.uint32(16)) & np.uint32(1))
+        c &= np.uint32(0xFFFF0000)
+    return y
 
 
 def gumbel_argmax(rng: np.random.Generator, logits: np.ndarray, T: float) -> np.ndarray:
@@ -139,6 +144,22 @@ def gumbel_argmax(rng: np.random.Generator, logits: np.ndarray, T: float) -> np.
         g = -np.log(-np.log(np.maximum(u, 1e-300)))
         out[r] = int(np.argmax(logits[r].astype(np.float64) / T + g))
     return out
+
+
+def distinct_indices(rng: np.random.Generator, V: int, k: int) -> np.ndarray:
+    """k distinct indices uniform over [0, V) (without replacement), in draw order."""
+    if 2 * k > V:
+        return rng.permutation(V)[:k]
+    out, seen = [], set()
+    while len(out) < k:
+        for j in rng.integers(0, V, 2 * k):
+            j = int(j)
+            if j not in seen:
+                seen.add(j)
+                out.append(j)
+                if len(out) == k:
+                    break
+    return np.array(out, dtype=np.int64)
 
 
 def _round(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -168,7 +189,7 @@ def make_chain(name: str, *, B: Optional[int] = None, gamma: Optional[int] = Non
         k = min(BOOSTED_PER_ROW, V)
         for b in range(B):
             for i in range(gamma + 1):
-                idx = r_logits.choice(V, size=k, replace=False)
+                idx = distinct_indices(r_logits, V, k)
                 zt[b, i, idx] += np.float32(BOOST)
     zt = _round(zt, w.dtype)
 
@@ -230,7 +251,7 @@ def make_tree(name: str = "tree-b32", *, B: Optional[int] = None, V: Optional[in
     k = min(BOOSTED_PER_ROW, V)
     for b in range(B):
         for n in range(N):
-            idx = r_logits.choice(V, size=k, replace=False)
+            idx = distinct_indices(r_logits, V, k)
             z[b, n, idx] += np.float32(BOOST)
     z = _round(z, w.dtype)
     g = np.argmax(z, axis=2)                      # planted-match reference per node row

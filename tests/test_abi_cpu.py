@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/spec_verify.h declares, sizes workspaces, and rejects
+bad arguments before touching the device (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_59_gb300 as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(sv.lib_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(spec_verify_[a-z_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 7, names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in sv.SIGNATURES, n
+
+
+def test_workspace_size_monotone_and_invalid(lib):
+    a = sv.spec_verify_workspace_size(8, 7, 151936)
+    b = sv.spec_verify_workspace_size(64, 7, 151936)
+    c = sv.spec_verify_workspace_size(64, 7, 128256)
+    assert 0 < a < b and c <= b and a % 256 == 0
+    assert sv.spec_verify_workspace_size(-1, 7, 10) == 0
+    assert sv.spec_verify_workspace_size(1, 7, 0) == 0
+    assert sv.spec_verify_workspace_size(0, 7, 10) > 0
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert sv.spec_verify_status_string(s)
+    assert "unknown" in sv.spec_verify_status_string(99)
+
+
+FAKE = 1 << 20          # an aligned address that is never dereferenced
+WS = 1 << 24
+
+
+def call_sample(**kw):
+    a = dict(target=FAKE, draft=FAKE, dtype=sv.SPEC_DTYPE_BF16, draft_tokens=FAKE, uniforms=FAKE,
+             temperature=1.0, B=2, gamma=3, V=100, out_tokens=FAKE, out_num_accepted=FAKE,
+             out_logprobs=None, ws=WS, ws_bytes=0, stream=None)
+    a.update(kw)
+    return sv.spec_verify_sample(a["target"], a["draft"], a["dtype"], a["draft_tokens"],
+                                 a["uniforms"], a["temperature"], a["B"], a["gamma"], a["V"],
+                                 a["out_tokens"], a["out_num_accepted"], a["out_logprobs"], a["ws"],
+                                 a["ws_bytes"], a["stream"])
+
+
+def test_sample_argument_checks(lib):
+    assert call_sample(dtype=7) == sv.SPEC_ERR_UNSUPPORTED_DTYPE
+    assert call_sample(B=-1) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(gamma=-1) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(gamma=257) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(V=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(temperature=0.0) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(temperature=-1.0) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(temperature=float("inf")) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(temperature=float("nan")) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(B=0) == sv.SPEC_OK                    # empty batch: nothing launched
+    assert call_sample(target=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(draft=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(draft_tokens=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(uniforms=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(out_tokens=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(target=FAKE + 8) == sv.SPEC_ERR_MISALIGNED
+    assert call_sample(draft=FAKE + 2) == sv.SPEC_ERR_MISALIGNED
+    assert call_sample(ws=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call_sample(ws=WS + 16) == sv.SPEC_ERR_MISALIGNED
+    need = sv.spec_verify_workspace_size(2, 3, 100)
+    assert call_sample(ws_bytes=need - 1) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_greedy_and_tree_argument_checks(lib):
+    g = sv.spec_verify_greedy
+    assert g(FAKE, 5, FAKE, 1, 1, 10, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_UNSUPPORTED_DTYPE
+    assert g(FAKE, 0, FAKE, 1, -1, 10, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert g(FAKE, 0, None, 1, 2, 10, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert g(FAKE + 4, 0, FAKE, 1, 2, 10, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_MISALIGNED
+    assert g(FAKE, 0, FAKE, 1, 2, 10, FAKE, FAKE, WS, 16, None) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
+    assert g(FAKE, 0, FAKE, 0, 2, 10, FAKE, FAKE, WS, 16, None) == sv.SPEC_OK
+    t = sv.spec_verify_tree_greedy
+    assert t(FAKE, 1, FAKE, FAKE, 1, 0, 10, FAKE, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 1, FAKE, FAKE, 1, 1025, 10, FAKE, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 1, None, FAKE, 1, 4, 10, FAKE, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 1, FAKE, FAKE, 1, 4, 10, None, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 1, FAKE, FAKE, 1, 4, 10, FAKE, FAKE, FAKE, WS, 8, None) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
+    assert sv.spec_verify_workspace_init(None, 10, None) == sv.SPEC_ERR_INVALID_ARG
+    st, _ = sv.spec_verify_read_error(None, None)
+    assert st == sv.SPEC_ERR_INVALID_ARG
+
+
+def test_product_package_does_not_reach_the_oracle():
+    """The product path never imports the oracle (test infrastructure)."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_59_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "oracle.h" not in src, f
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(sv, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sv, "_lib", None)
+    with pytest.raises(ImportError):
+        sv.load_library()
