@@ -62,7 +62,9 @@ typedef enum {
     SPEC_ERR_MISALIGNED = 3,           /* logits or workspace not aligned as required */
     SPEC_ERR_WORKSPACE_TOO_SMALL = 4,
     SPEC_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
-    SPEC_ERR_DEVICE_INPUT = 6          /* reported by spec_verify_read_error only */
+    SPEC_ERR_DEVICE_INPUT = 6,         /* reported by spec_verify_read_error only */
+    SPEC_ERR_EXCEEDS_STATIC_SCRATCH = 7 /* spec_verify_sample_noalloc: the problem needs more than
+                                           SPEC_VERIFY_NOALLOC_SCRATCH_BYTES of scratch */
 } spec_status_t;
 
 typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
@@ -170,6 +172,41 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
                                       int N, int V, int32_t* out_path_nodes, int32_t* out_tokens,
                                       int32_t* out_num_accepted, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * spec_verify_sample for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot provide a workspace: a plugin whose host framework owns all
+ * device memory in its own pool and passes in only input and output buffers,
+ * or a decode loop that must not call cudaMalloc/cudaFree (which can
+ * synchronise the device) in the middle of a step.  Arguments, outputs and
+ * results are those of spec_verify_sample without the workspace; the same
+ * kernels run.  The call allocates nothing and calls no allocating routine.
+ *
+ * Scratch: a fixed array of SPEC_VERIFY_NOALLOC_SCRATCH_BYTES (4 MiB) that the
+ * library places in the device memory of every GPU it is loaded on, held
+ * until the process exits.  Problems whose scratch need,
+ * spec_verify_workspace_size(B, gamma, V), exceeds it are rejected with
+ * SPEC_ERR_EXCEEDS_STATIC_SCRATCH before anything is launched (the five
+ * benchmark workloads need at most about 2.4 MB).
+ *
+ * The first call on each device, made while that device is current, looks up
+ * the array's device address (cudaGetSymbolAddress, which may also load the
+ * library's kernels onto that device); make that first call before any stream
+ * capture.  Every call on a device shares the one array, so calls whose work
+ * overlaps on the GPU (different streams without ordering, or host threads
+ * racing on one device) race on it and give undefined results; order them.
+ * Bad input is reported per sequence (num_accepted = -1, tokens -1) only: the
+ * device error word of the workspace calls is not readable for this entry.
+ */
+#define SPEC_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+spec_status_t spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                         spec_dtype_t dtype, const int32_t* draft_tokens,
+                                         const float* uniforms, float temperature, int B,
+                                         int gamma, int V, int32_t* out_tokens,
+                                         int32_t* out_num_accepted, float* out_logprobs,
+                                         cudaStream_t stream);
 
 /*
  * Synchronises `stream`, returns the accumulated SPEC_DEVERR_* bits of the

@@ -17,7 +17,7 @@ from typing import Optional
 __all__ = [
     "SPEC_OK", "SPEC_DTYPE_F32", "SPEC_DTYPE_BF16", "SpecVerifyError", "lib_path", "load_library",
     "spec_verify_workspace_size", "spec_verify_workspace_init", "spec_verify_sample",
-    "spec_verify_sample_stats", "spec_verify_sample_finish",
+    "spec_verify_sample_stats", "spec_verify_sample_finish", "spec_verify_sample_noalloc",
     "spec_verify_greedy", "spec_verify_tree_greedy", "spec_verify_read_error",
     "spec_verify_status_string", "Workspace", "verify_sample", "verify_greedy", "verify_tree_greedy",
 ]
@@ -29,6 +29,8 @@ SPEC_ERR_MISALIGNED = 3
 SPEC_ERR_WORKSPACE_TOO_SMALL = 4
 SPEC_ERR_CUDA = 5
 SPEC_ERR_DEVICE_INPUT = 6
+SPEC_ERR_EXCEEDS_STATIC_SCRATCH = 7
+SPEC_VERIFY_NOALLOC_SCRATCH_BYTES = 4 << 20
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
 SPEC_DEVERR_TOKEN_RANGE = 1
@@ -49,6 +51,8 @@ SIGNATURES = {
     "spec_verify_sample_stats": ([_P, _P, _I, ctypes.c_float, _I, _I, _I, _P, _S, _P], _I),
     "spec_verify_sample_finish": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P,
                                    _S, _P], _I),
+    "spec_verify_sample_noalloc": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P,
+                                    _P], _I),
     "spec_verify_greedy": ([_P, _I, _P, _I, _I, _I, _P, _P, _P, _S, _P], _I),
     "spec_verify_tree_greedy": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
     "spec_verify_read_error": ([_P, _P, _P], _I),
@@ -111,6 +115,15 @@ def spec_verify_sample_finish(target, draft, dtype, draft_tokens, uniforms, temp
                                                     temperature, B, gamma, V, out_tokens,
                                                     out_num_accepted, out_logprobs, ws, ws_bytes,
                                                     stream)
+
+
+def spec_verify_sample_noalloc(target, draft, dtype, draft_tokens, uniforms, temperature, B, gamma,
+                               V, out_tokens, out_num_accepted, out_logprobs, stream) -> int:
+    """spec_verify_sample without a workspace, for callers that cannot
+    allocate device memory (see include/spec_verify.h)."""
+    return load_library().spec_verify_sample_noalloc(target, draft, dtype, draft_tokens, uniforms,
+                                                     temperature, B, gamma, V, out_tokens,
+                                                     out_num_accepted, out_logprobs, stream)
 
 
 def spec_verify_greedy(target, dtype, draft_tokens, B, gamma, V, out_tokens, out_num_accepted,

@@ -168,6 +168,8 @@ const char* spec_verify_status_string(spec_status_t status) {
         case SPEC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case SPEC_ERR_CUDA: return "CUDA runtime error";
         case SPEC_ERR_DEVICE_INPUT: return "bad input detected on the device";
+        case SPEC_ERR_EXCEEDS_STATIC_SCRATCH:
+            return "problem needs more scratch than the fixed array of spec_verify_sample_noalloc";
     }
     return "unknown status";
 }
