@@ -73,6 +73,8 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 #define SPEC_DEVERR_TOKEN_RANGE  1   /* a draft / node token outside [0, V) */
 #define SPEC_DEVERR_EMPTY_ROW    2   /* a logits row whose every entry is -inf (sampling) */
 #define SPEC_DEVERR_TREE_PARENT  4   /* parents[0] != -1 or parents[n] not in [0, n) */
+#define SPEC_DEVERR_TIMEOUT      8   /* a bounded wait inside a kernel ran out (internal error;
+                                        the affected results are not valid) */
 
 /*
  * Bytes of workspace any of the three verification calls needs for B
@@ -96,20 +98,20 @@ spec_status_t spec_verify_workspace_init(void* workspace, size_t workspace_bytes
  *                                  u_i < p_i(x_i)/q_i(x_i)); u_gamma drives the
  *                                  single final sample (residual or bonus) by
  *                                  inverse CDF in index order
- *   temperature   > 0, finite; p = softmax(z^t / T), q = softmax(z^d / T)
- *   0 <= gamma <= 256, V >= 1, B >= 0.  V is also bounded by the final pass,
- *   which stages one row pair per thread-block cluster (16 CTAs at most) in
- *   shared memory: V <= 16 * floor((opt-in shared memory per block - 1024) / 8),
- *   462848 on GB300; larger V returns SPEC_ERR_INVALID_ARG.
+ *   temperature   finite, >= 1e-20; p = softmax(z^t / T), q = softmax(z^d / T)
+ *   0 <= gamma <= 256, 1 <= V <= 2097152, B >= 0.  (The final sample scans
+ *   the 8192-element chunk totals of a row in one 256-thread CTA, hence the
+ *   bound on V; larger V returns SPEC_ERR_INVALID_ARG.)
  * Outputs (device):
  *   out_tokens       [B, gamma+1] int32: the k accepted drafts, the final
  *                    token, then -1
  *   out_num_accepted [B] int32: k in [0, gamma] (emitted tokens = k + 1)
  *   out_logprobs     [B, gamma, 2] f32, nullable: ln p_i(x_i), ln q_i(x_i)
  *
- * Two kernels run: a streaming pass over every logit row (row max and
- * sum-exp partials) and one thread-block cluster per sequence that takes the
- * accept decisions and samples from the one rejected (or bonus) row pair.
+ * A streaming pass over every logit row (row max and sum-exp partials) is
+ * followed by four small kernels: the accept decisions (one CTA per
+ * sequence), the chunk sums of the exponentials and of the residual weights
+ * of the one rejected (or bonus) row pair, and the inverse-CDF search.
  */
 spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
                                  spec_dtype_t dtype, const int32_t* draft_tokens,

@@ -36,6 +36,7 @@ SPEC_DTYPE_BF16 = 1
 SPEC_DEVERR_TOKEN_RANGE = 1
 SPEC_DEVERR_EMPTY_ROW = 2
 SPEC_DEVERR_TREE_PARENT = 4
+SPEC_DEVERR_TIMEOUT = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libspecverify.so")

@@ -10,6 +10,7 @@ namespace sv {
 
 constexpr int kMaxGammaApi = 256;
 constexpr int kMaxNodesApi = 1024;
+constexpr float kMinTemperature = 1e-20f;   // log2(e)/T stays a finite float
 
 cudaError_t device_info(DeviceInfo* out) {
     // Cached per device ordinal; the values are immutable properties.
@@ -65,7 +66,7 @@ static spec_status_t sample_common(const void* target_logits, const void* draft_
                                    cudaStream_t stream, int parts) {
     if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
     if (B < 0 || gamma < 0 || gamma > kMaxGammaApi || V <= 0) return SPEC_ERR_INVALID_ARG;
-    if (!(temperature > 0.f) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature >= kMinTemperature) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
     if (B == 0) return SPEC_OK;
     if (!target_logits || (gamma > 0 && !draft_logits)) return SPEC_ERR_INVALID_ARG;
     if ((parts & kSampleFinish) &&

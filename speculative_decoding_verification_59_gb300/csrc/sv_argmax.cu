@@ -13,6 +13,7 @@
 // Ties: the lowest index among equal raw logits wins (values compared as
 // floats, so -0.0 == +0.0; NaN logits are undefined).
 #include "sv_common.cuh"
+#include "sv_stream.cuh"
 
 namespace sv {
 
@@ -225,12 +226,29 @@ static cudaError_t launch_decide(void (*kfn)(DecideArgs), const DecideArgs& d, i
 }
 
 static cudaError_t stream_argmax(const void* zt, int elt, int B, int rows, int V, float2* parts,
-                                 cudaStream_t st) {
+                                 int* err, cudaStream_t st) {
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    // 16-byte rows: bulk-copy ring; otherwise the register path
+    RingArgs ra = {};
+    ra.zt = static_cast<const char*>(zt);
+    ra.zd = nullptr;
+    ra.gamma = -1;
+    ra.rows_per_seq = rows;
+    ra.V = V;
+    ra.nseg = nseg(V, elt);
+    ra.total_chunks = (long long)B * rows * ra.nseg;
+    ra.parts = parts;
+    ra.err = err;
+    bool used = false;
+    e = elt == 2 ? launch_ring<2, true>(ra, di, st, &used) : launch_ring<4, true>(ra, di, st, &used);
+    if (e != cudaSuccess || used) return e;
     ArgmaxArgs a;
-    a.zt = static_cast<const char*>(zt);
+    a.zt = ra.zt;
     a.V = V;
-    a.nseg = nseg(V, elt);
-    a.total_chunks = (long long)B * rows * a.nseg;
+    a.nseg = ra.nseg;
+    a.total_chunks = ra.total_chunks;
     a.parts = parts;
     const bool vec = ((size_t)V * elt) % 16 == 0;
     if (elt == 2) return vec ? launch_argmax_t<2, true>(a, st) : launch_argmax_t<2, false>(a, st);
@@ -253,7 +271,7 @@ cudaError_t launch_greedy(const void* zt, spec_dtype_t dt, const int32_t* x, int
                           int V, int32_t* out_tok, int32_t* out_acc, void* ws, cudaStream_t st) {
     const int elt = elt_size(dt);
     DecideArgs d = decide_args(elt, gamma + 1, V, ws, gamma, B);
-    cudaError_t e = stream_argmax(zt, elt, B, gamma + 1, V, const_cast<float2*>(d.parts), st);
+    cudaError_t e = stream_argmax(zt, elt, B, gamma + 1, V, const_cast<float2*>(d.parts), d.err, st);
     if (e != cudaSuccess) return e;
     d.x = x;
     d.gamma = gamma;
@@ -267,7 +285,7 @@ cudaError_t launch_tree(const void* zt, spec_dtype_t dt, const int32_t* tok, con
                         int32_t* out_acc, void* ws, cudaStream_t st) {
     const int elt = elt_size(dt);
     DecideArgs d = decide_args(elt, N, V, ws, N, B);
-    cudaError_t e = stream_argmax(zt, elt, B, N, V, const_cast<float2*>(d.parts), st);
+    cudaError_t e = stream_argmax(zt, elt, B, N, V, const_cast<float2*>(d.parts), d.err, st);
     if (e != cudaSuccess) return e;
     d.tok = tok;
     d.par = par;

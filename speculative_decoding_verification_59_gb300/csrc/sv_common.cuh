@@ -147,6 +147,68 @@ __device__ __forceinline__ void ff_add(FF& a, float x) {
 
 __device__ __forceinline__ double ff_value(const FF& a) { return (double)a.hi + (double)a.lo; }
 
+// Sum of two float-float values (exact TwoSum of the leading parts, then the
+// trailing parts), renormalised.  Symmetric in its operands.
+__device__ __forceinline__ FF ff_combine(FF a, FF b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    float e = (a.hi - (s - bb)) + (b.hi - bb);
+    e += a.lo + b.lo;
+    const float hi = s + e;
+    return FF{hi, e - (hi - s)};
+}
+
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
+    return FF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+
+__device__ __forceinline__ FF ff_shfl_up(FF a, int o) {
+    return FF{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+
+// Canonical (non-overlapping) form of an accumulated float-float value.
+__device__ __forceinline__ FF ff_norm(FF a) {
+    const float s = a.hi + a.lo;
+    return FF{s, a.lo - (s - a.hi)};
+}
+
+// a < b for canonical float-float values.
+__device__ __forceinline__ bool ff_lt(FF a, FF b) {
+    return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+// u * a for a float u and a canonical float-float a.
+__device__ __forceinline__ FF ff_scale(float u, FF a) {
+    const float p = u * a.hi;
+    const float e = fmaf(u, a.hi, -p) + u * a.lo;
+    return ff_norm(FF{p, e});
+}
+
+// a / b for canonical float-float values (one correction step).
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+    const float q = a.hi / b.hi;
+    const float r = (fmaf(-q, b.hi, a.hi) + a.lo) - q * b.lo;
+    return ff_norm(FF{q, r / b.hi});
+}
+
+// Warp sum of float-float values; every lane receives lane 0's result.
+__device__ __forceinline__ FF warp_sum_ff(FF a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = ff_combine(a, ff_shfl_xor(a, o));
+    return FF{__shfl_sync(0xffffffffu, a.hi, 0), __shfl_sync(0xffffffffu, a.lo, 0)};
+}
+
+// Inclusive warp scan of float-float values in lane order.
+__device__ __forceinline__ FF warp_incl_scan_ff(FF a) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const FF y = ff_shfl_up(a, o);
+        if (lane >= o) a = ff_combine(y, a);
+    }
+    return a;
+}
+
 // ---- programmatic dependent launch -------------------------------------------
 // The streaming kernel lets the next kernel in the stream begin launching
 // once each of its CTAs is on its last chunk; that kernel waits (in hardware)

@@ -24,13 +24,30 @@ inline int warp_elems(int elt) { return 32 * kLaneBytes / elt; }
 inline int block_elems(int elt) { return kWarps * warp_elems(elt); }
 inline int nseg(int V, int elt) { return (V + block_elems(elt) - 1) / block_elems(elt); }
 
-// Workspace: [error word (256 bytes reserved) | per-warp row partials].
-// The partials are fully rewritten by the streaming pass of every call before
-// the second kernel of that call reads them, so a workspace carries nothing
-// from one call to the next except the error word, which only accumulates
-// error bits until spec_verify_read_error clears it.
+// Elements of one row per CTA in the final-sample kernels: 32 contiguous
+// elements per thread of a 256-thread CTA (four 16-byte vectors of bf16,
+// eight of fp32).
+constexpr int kFinalPerThread = 32;
+constexpr int kFinalChunkThreads = 256;
+constexpr int kFinalChunk = kFinalPerThread * kFinalChunkThreads;
+inline int final_chunks(int V) { return (V + kFinalChunk - 1) / kFinalChunk; }
+
+// Per-sequence result of the accept decisions, read by the final-sample kernels.
+struct SampleDesc {
+    int k;        // rejection index (< gamma), gamma when all drafts were accepted, -1: bad input
+    float mt;     // max logit of target row k
+    float md;     // max logit of draft row k (rejection only)
+    int pad;
+};
+
+// Workspace: [error word (256 bytes reserved) | per-warp row partials |
+// SampleDesc[B] | per-chunk normaliser sums | per-chunk residual sums].
+// Every region after the error word is fully rewritten by the kernels of a
+// call before another kernel of that call reads it, so a workspace carries
+// nothing from one call to the next except the error word, which only
+// accumulates error bits until spec_verify_read_error clears it.
 struct WsLayout {
-    size_t err_off, part_off, part_count, total;
+    size_t err_off, part_off, part_count, desc_off, zsum_off, wsum_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -43,7 +60,11 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     size_t rows = (size_t)B * (size_t)(2 * (size_t)gamma_or_nodes + 1);
     // fp32 has the smaller warp chunk, hence the most partials per row
     L.part_count = rows * (size_t)nseg(V, 4) * kWarps;
-    L.total = L.part_off + align256(sizeof(float2) * L.part_count);
+    L.desc_off = L.part_off + align256(sizeof(float2) * L.part_count);
+    const size_t chunks = (size_t)B * (size_t)final_chunks(V);
+    L.zsum_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
+    L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * chunks);
+    L.total = L.wsum_off + align256(2 * sizeof(float) * chunks);
     return L;
 }
 

@@ -61,7 +61,7 @@ extern "C" spec_status_t spec_verify_sample_noalloc(
     // Same argument rules as spec_verify_sample, checked on the host first.
     if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
     if (B < 0 || gamma < 0 || gamma > 256 || V <= 0) return SPEC_ERR_INVALID_ARG;
-    if (!(temperature > 0.f) || !(temperature < __builtin_huge_valf())) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature >= 1e-20f) || !(temperature < __builtin_huge_valf())) return SPEC_ERR_INVALID_ARG;
     if (B == 0) return SPEC_OK;
     if (!target_logits || !uniforms || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
     if (gamma > 0 && (!draft_logits || !draft_tokens)) return SPEC_ERR_INVALID_ARG;

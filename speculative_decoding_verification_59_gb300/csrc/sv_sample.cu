@@ -1,39 +1,46 @@
-// Stochastic verification: the two kernels behind spec_verify_sample.
+// Stochastic verification: the kernels behind spec_verify_sample.
 //
 // Source: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", section "What happens in one round" (steps 1-4) and section
 // "Why fixing wrong guesses does not leave the target distribution" (residual
 // p'(x) = norm(max(0, p(x) - q(x)))).
 //
-// Pass 1 (sample_rowstats_kernel) streams every logit once.  A persistent
-// grid walks block chunks (row, segment) of the 2*gamma+1 rows of every
-// sequence; each warp reduces its warp chunk to (max m, sum 2^((z - m)
-// log2(e)/T)) and writes that pair to the workspace.  Nothing else happens
-// in this pass, so it is a pure HBM stream.
+// Pass 1 streams every logit once (ring_stream_kernel in sv_stream.cuh for
+// 16-byte rows, sample_rowstats_kernel below otherwise): each warp chunk of
+// each of the 2*gamma+1 rows of every sequence becomes a partial (max m,
+// sum 2^((z - m) log2(e)/T)).
 //
-// Pass 2 (sample_final_kernel) runs one thread-block cluster per sequence.
-// Every CTA of the cluster first merges the sequence's partials into row
-// statistics and takes the accept decisions left to right (u_i <
-// p_i(x_i)/q_i(x_i), in the log domain, in double); all CTAs reach the same
-// rejection index k.  The cluster then draws the final token from the single
-// row pair it comes from: target and draft row k after a rejection (weights
-// max(0, p_k - q_k)), or target row gamma when every draft was accepted
-// (weights p_gamma).  Because the token is an inverse CDF over ~10^5 entries,
-// both normalisers are recomputed from the very exponentials that form the
-// weights, summed in float-float / double and combined across the cluster
-// through distributed shared memory; the search walks exactly the prefix sums
-// whose totals picked the owning thread.
-#include <cooperative_groups.h>
-
+// Pass 2 draws the final token of every sequence from the single row pair it
+// comes from -- target and draft row k after a rejection at k (weights
+// max(0, p_k - q_k)), target row gamma when every draft was accepted (weights
+// p_gamma) -- by inverse CDF in index order.  Four small kernels, chained with
+// programmatic dependent launch, keep every sequence in flight at once:
+//   sample_decide_kernel  one CTA per sequence: row statistics from the
+//                         partials, accept decisions u_i < p_i(x_i)/q_i(x_i)
+//                         left to right, all outputs but the final token;
+//   sample_zsum_kernel    one CTA per 8192-element chunk of row k: sums of the
+//                         exponentials of the target and draft chunk;
+//   sample_wsum_kernel    one CTA per chunk (rejections only): the ratio of the
+//                         two row normalisers from all chunk sums, then the
+//                         chunk's residual weight total;
+//   sample_search_kernel  one CTA per sequence: prefix over the chunk totals,
+//                         the owning chunk, its weights recomputed and scanned,
+//                         the owning element.
+// The weights are formed from the very exponentials whose sums normalise them,
+// all sums are float-float (about 48 bits), and a chunk's total and the scan
+// that later searches inside it come from the same block-scan code, so the
+// intervals of chunks, threads and elements tile [0, S) exactly.
 #include "sv_common.cuh"
-
-namespace cg = cooperative_groups;
+#include "sv_stream.cuh"
 
 namespace sv {
 
+#ifndef SV_FINAL_EXACT_EXP
+#define SV_FINAL_EXACT_EXP 1
+#endif
+
 constexpr int kMaxGamma = 256;                 // rows per sequence <= 2*256+1
-constexpr int kFinalThreads = 512;
-constexpr int kFinalStaticSmem = 16384;        // static shared memory reserve of pass 2
+constexpr int kDecideThreadsS = 512;
 
 struct StatsArgs {
     const char* zt;
@@ -54,8 +61,11 @@ struct FinalArgs {
     float T, invT, s;
     int B, gamma, V;
     int nseg, rows_per_seq;
-    int L;              // elements per CTA slice (multiple of 8)
+    int C;              // 2048-element chunks per row
     const float2* parts;
+    SampleDesc* desc;
+    float4* zsum;       // [B, C]: (Za.hi, Za.lo, Zb.hi, Zb.lo) of each chunk
+    float2* wsum;       // [B, C]: residual weight total of each chunk
     int32_t* out_tok;
     int32_t* out_acc;
     float* out_lp;
@@ -104,13 +114,24 @@ __global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const StatsAr
 }
 
 // ---------------------------------------------------------------- pass 2
-// exp((z - m) / T) with the argument carried in two floats, so the only
-// roundings left are expf's own and the final product.  -inf logits give 0.
+constexpr int kCT = kFinalChunkThreads;        // threads per chunk CTA (kFinalPerThread elements each)
+constexpr int kCW = kCT / 32;
+
+// exp((z - m) / T) for the final pass.  The default (SV_FINAL_EXACT_EXP=1)
+// carries (z - m)/T as two floats into expf, leaving only expf's own rounding
+// and one product: measured over 1e5 rows of the B=8, T=1 workload it halves
+// the mismatches against the fp64 reference compared with the cheaper
+// SV_FINAL_EXACT_EXP=0 form, 2^(z*s - m*s) from one fused multiply-add and the
+// special-function unit (m*s is rounded once per row, a common factor that the
+// normalisation cancels).
 template <int ELT>
-__device__ __forceinline__ float exp_scaled(float z, float m, float T, float invT) {
+__device__ __forceinline__ float final_exp(float z, float m, float ms, bool wide, const FinalArgs& a) {
+#if SV_FINAL_EXACT_EXP
+    (void)ms;
+    (void)wide;
     float d_hi, d_lo;
     if constexpr (ELT == 2) {
-        d_hi = z - m;                  // exact: both are bfloat16 values
+        d_hi = z - m;
         d_lo = 0.f;
     } else {
         d_hi = z - m;
@@ -118,71 +139,91 @@ __device__ __forceinline__ float exp_scaled(float z, float m, float T, float inv
         d_lo = (z - (d_hi - bb)) + (-m - bb);
     }
     if (d_hi == kNegInf) return 0.f;
-    const float y = d_hi * invT;
-    const float rem = fmaf(-y, T, d_hi) + d_lo;
-    const float ylo = rem * invT;
+    const float y = d_hi * a.invT;
+    const float rem = fmaf(-y, a.T, d_hi) + d_lo;
     const float e = expf(y);
-    return fmaf(e, ylo, e);
+    return fmaf(e, rem * a.invT, e);
+#else
+    // wide (|m * s| beyond 1e30, only for extreme temperatures): subtract
+    // first so no intermediate overflows
+    return ex2_approx(wide ? (z - m) * a.s : fmaf(z, a.s, -ms));
+#endif
 }
 
-__device__ __forceinline__ double block_sum_double(double v, double* red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_sum(v);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    double t = 0.0;
-    if (warp == 0) {
-        t = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0;
-        t = warp_sum(t);
-        if (lane == 0) red[0] = t;
-    }
-    __syncthreads();
-    t = red[0];
-    __syncthreads();
-    return t;
-}
+constexpr int kPT = kFinalPerThread;
 
-// Inclusive scan of one double per thread (block of kFinalThreads) into incl[].
-__device__ __forceinline__ void block_incl_scan_double(double v, double* incl, double* wsum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    double x = v;
+// The kPT logits of row `row` at [j0, j0 + kPT); entries at or beyond V are
+// -inf.  All loads are issued before any is used.
+template <int ELT, bool VEC>
+__device__ __forceinline__ void load_seg(const char* row, int V, int j0, float (&z)[kPT]) {
+    if constexpr (VEC) {
+        constexpr int PV = 16 / ELT;                      // V is a multiple of PV
+        uint4 q[kPT / PV];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        double w = lane < kFinalThreads / 32 ? wsum[lane] : 0.0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
+        for (int h = 0; h < kPT / PV; ++h) {
+            const int jj = j0 + PV * h;
+            q[h] = jj < V ? ld_stream16(row + (size_t)jj * ELT)
+                          : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
         }
-        if (lane < kFinalThreads / 32) wsum[lane] = w;    // inclusive warp totals
+#pragma unroll
+        for (int h = 0; h < kPT / PV; ++h)
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                if constexpr (ELT == 2) {
+                    const uint32_t w = u4_get(q[h], e >> 1);
+                    z[PV * h + e] = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+                } else {
+                    const uint32_t w = u4_get(q[h], e);
+                    // -inf padding for fp32 vectors past V
+                    z[PV * h + e] = (j0 + PV * h < V) ? __uint_as_float(w) : kNegInf;
+                }
+            }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kPT; ++e) z[e] = (j0 + e < V) ? load_logit<ELT>(row, j0 + e) : kNegInf;
     }
-    __syncthreads();
-    incl[threadIdx.x] = (warp > 0 ? wsum[warp - 1] : 0.0) + x;
-    __syncthreads();
 }
 
-// Per-thread float-float sum over a contiguous segment [lo, hi) of w.
-__device__ __forceinline__ double seg_sum(const float* w, int lo, int hi) {
-    FF acc{0.f, 0.f};
-    for (int j = lo; j < hi; ++j) ff_add(acc, w[j]);
-    return ff_value(acc);
+// Inclusive scan of one float-float value per thread over a kCT-thread block
+// in thread order; *total receives the block total.  Deterministic: the same
+// inputs give the same bits in every CTA.
+__device__ __forceinline__ FF block_incl_scan_ff(FF v, FF* wtot, FF* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    FF x = warp_incl_scan_ff(v);
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        FF y = lane < kCW ? wtot[lane] : FF{0.f, 0.f};
+        y = warp_incl_scan_ff(y);
+        if (lane < kCW) wtot[lane] = y;
+    }
+    __syncthreads();
+    const FF r = warp > 0 ? ff_combine(wtot[warp - 1], x) : x;
+    *total = wtot[kCW - 1];
+    __syncthreads();
+    return r;
+}
+
+// Exclusive counterpart of an inclusive block scan result r (thread order).
+__device__ __forceinline__ FF block_excl_from_incl(FF r, const FF* wtot_scanned) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const FF up = ff_shfl_up(r, 1);
+    if (lane > 0) return up;
+    return warp > 0 ? wtot_scanned[warp - 1] : FF{0.f, 0.f};
 }
 
 struct DecideSmem {
     float M[2 * kMaxGamma + 1];       // row max
-    double lnZ[2 * kMaxGamma + 1];    // ln sum exp((z - M)/T)
-    double lp[kMaxGamma], lq[kMaxGamma];
+    float lnZ[2 * kMaxGamma + 1];     // ln sum exp((z - M)/T)
+    float lp[kMaxGamma], lq[kMaxGamma];
     int bad, k;
 };
 
 // Row statistics of sequence b from the pass-1 partials and the accept
-// decisions.  Identical in every CTA of the cluster (same data, same order).
+// decisions.  Single precision throughout (GB300's double-precision rate is a
+// small fraction of its float rate): ln p_i(x_i) and ln q_i(x_i) carry errors
+// of ~1e-6, far inside the 1e-4 decision margin and the 1e-5 bar on returned
+// probabilities.
 template <int ELT>
 __device__ void sample_decide(const FinalArgs& a, int b, DecideSmem& sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -192,39 +233,39 @@ __device__ void sample_decide(const FinalArgs& a, int b, DecideSmem& sm) {
     if (threadIdx.x == 0) sm.bad = 0;
     __syncthreads();
 
-    // M = max m_p, Z = sum Z_p 2^((m_p - M) s) over the row's warp partials.
+    // M = max m_p, Z = sum Z_p 2^((m_p - M) s) over the row's warp partials
+    // (float-float per lane, then across the warp).
     for (int r = warp; r < a.rows_per_seq; r += nwarps) {
         const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
         float m = kNegInf;
         for (int p = lane; p < P; p += 32) m = fmaxf(m, pr[p].x);
         m = warp_max(m);
-        double z = 0.0;
+        FF z{0.f, 0.f};
         if (m != kNegInf) {
             for (int p = lane; p < P; p += 32) {
                 const float2 q = pr[p];
-                if (q.x != kNegInf) z += (double)q.y * (double)ex2_approx((q.x - m) * a.s);
+                if (q.x != kNegInf) ff_add(z, q.y * ex2_approx((q.x - m) * a.s));
             }
         }
-        z = warp_sum(z);
+        z = ff_norm(warp_sum_ff(z));
         if (lane == 0) {
             sm.M[r] = m;
-            sm.lnZ[r] = m == kNegInf ? 0.0 : log(z);
+            sm.lnZ[r] = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
         }
     }
     __syncthreads();
 
     // Validate the drafts, gather z[x_i] and form ln p_i(x_i), ln q_i(x_i).
-    const double invT = 1.0 / (double)a.T;
     for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
         const int xi = a.x[(size_t)b * a.gamma + i];
         if (xi < 0 || xi >= a.V) {
             atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
-            sm.lp[i] = sm.lq[i] = 0.0;
+            sm.lp[i] = sm.lq[i] = 0.f;
         } else {
             const float ztx = load_logit<ELT>(seq_row(a.zt, a.zd, a.gamma, b, i, rowbytes), xi);
             const float zdx = load_logit<ELT>(seq_row(a.zt, a.zd, a.gamma, b, a.gamma + 1 + i, rowbytes), xi);
-            sm.lp[i] = ((double)ztx - (double)sm.M[i]) * invT - sm.lnZ[i];
-            sm.lq[i] = ((double)zdx - (double)sm.M[a.gamma + 1 + i]) * invT - sm.lnZ[a.gamma + 1 + i];
+            sm.lp[i] = (ztx - sm.M[i]) * a.invT - sm.lnZ[i];
+            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) * a.invT - sm.lnZ[a.gamma + 1 + i];
         }
     }
     for (int r = threadIdx.x; r < a.rows_per_seq; r += blockDim.x)
@@ -237,12 +278,12 @@ __device__ void sample_decide(const FinalArgs& a, int b, DecideSmem& sm) {
             // Left to right; the first rejection voids the remaining drafts.
             k = a.gamma;
             for (int i = 0; i < a.gamma; ++i) {
-                const double lp = sm.lp[i], lq = sm.lq[i];
-                double r;
-                if (lp == -CUDART_INF) r = 0.0;
-                else if (lq == -CUDART_INF) r = CUDART_INF;
-                else r = exp(lp - lq);
-                if (!((double)a.u[(size_t)b * (a.gamma + 1) + i] < r)) { k = i; break; }
+                const float lp = sm.lp[i], lq = sm.lq[i];
+                float r;
+                if (lp == kNegInf) r = 0.f;
+                else if (lq == kNegInf) r = CUDART_INF_F;
+                else r = expf(lp - lq);
+                if (!(a.u[(size_t)b * (a.gamma + 1) + i] < r)) { k = i; break; }
             }
         }
         sm.k = k;
@@ -250,167 +291,204 @@ __device__ void sample_decide(const FinalArgs& a, int b, DecideSmem& sm) {
     __syncthreads();
 }
 
-template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const FinalArgs a) {
-    extern __shared__ float4 dyn_smem[];
-    float* ea = reinterpret_cast<float*>(dyn_smem);       // exp of target row (weights p)
-    float* eb = ea + a.L;                                 // exp of draft row, then residual weights
+template <int ELT>
+__global__ void __launch_bounds__(kDecideThreadsS) sample_decide_kernel(const FinalArgs a) {
     __shared__ DecideSmem dsm;
-    __shared__ double s_red[32];
-    __shared__ double s_incl[kFinalThreads];
-    __shared__ double s_wsum[32];
-    __shared__ double s_za, s_zb, s_S[2];
-
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int CS = (int)cluster.num_blocks();
-    const int b = blockIdx.y;
-    const int tid = threadIdx.x;
-
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_trigger();
     pdl_wait();                                           // pass-1 partials are visible from here
     sample_decide<ELT>(a, b, dsm);
     const int k = dsm.k;
-    if (rank == 0) {
-        // Accepted drafts, count, padding and log-probabilities; the final
-        // slot k is written by the thread that owns the sampled token.
-        if (tid == 0) {
-            a.out_acc[b] = k;
-            if (dsm.bad) atomicOr(a.err, dsm.bad);
-        }
-        for (int i = tid; i <= a.gamma; i += kFinalThreads)
-            if (k < 0 || i != k)
-                a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
-        if (a.out_lp)
-            for (int i = tid; i < a.gamma; i += kFinalThreads) {
-                float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
-                o[0] = k >= 0 ? (float)dsm.lp[i] : CUDART_NAN_F;
-                o[1] = k >= 0 ? (float)dsm.lq[i] : CUDART_NAN_F;
-            }
+    if (tid == 0) {
+        a.out_acc[b] = k;
+        if (dsm.bad) atomicOr(a.err, dsm.bad);
+        SampleDesc d;
+        d.k = k;
+        d.mt = k >= 0 ? dsm.M[k] : 0.f;
+        d.md = (k >= 0 && k < a.gamma) ? dsm.M[a.gamma + 1 + k] : 0.f;
+        d.pad = 0;
+        a.desc[b] = d;
     }
-    if (k < 0) return;                                    // bad sequence: the whole cluster leaves
+    // Accepted drafts, padding and log-probabilities; slot k is written by
+    // the search kernel.
+    for (int i = tid; i <= a.gamma; i += blockDim.x)
+        if (k < 0 || i != k)
+            a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
+    if (a.out_lp)
+        for (int i = tid; i < a.gamma; i += blockDim.x) {
+            float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
+            o[0] = k >= 0 ? dsm.lp[i] : CUDART_NAN_F;
+            o[1] = k >= 0 ? dsm.lq[i] : CUDART_NAN_F;
+        }
+}
 
-    const bool rej = k < a.gamma;
-    const float mt = dsm.M[k];
-    const float md = rej ? dsm.M[a.gamma + 1 + k] : 0.f;
+// The exponentials of this thread's kPT elements of chunk c of the
+// sequence's target row k (ea) and draft row k (eb, rejections only).
+template <int ELT, bool VEC>
+__device__ __forceinline__ void chunk_exps(const FinalArgs& a, int b, const SampleDesc& d, int c,
+                                           float (&ea)[kPT], float (&eb)[kPT]) {
+    const bool rej = d.k < a.gamma;
     const size_t rowbytes = (size_t)a.V * ELT;
-    const char* rt = a.zt + ((size_t)b * (a.gamma + 1) + k) * rowbytes;
-    const char* rd = rej ? a.zd + ((size_t)b * a.gamma + k) * rowbytes : nullptr;
-    const int j0 = rank * a.L;
-    const int n = max(0, min(a.V - j0, a.L));
-
-    // Phase A: stage exponentials of the slice and sum them.
-    FF sa{0.f, 0.f}, sb{0.f, 0.f};
-    int jtail = 0;
-    if constexpr (VEC) {
-        constexpr int PV = 16 / ELT;
-        const int nv = n / PV;                            // n is a multiple of PV except at the row end
-        for (int v = tid; v < nv; v += kFinalThreads) {
-            const uint4 qt = ld_stream16(rt + (size_t)(j0 + v * PV) * ELT);
-            uint4 qd = make_uint4(0, 0, 0, 0);
-            if (rej) qd = ld_stream16(rd + (size_t)(j0 + v * PV) * ELT);
+    const int j0 = c * kFinalChunk + threadIdx.x * kPT;
+    const float mts = d.mt * a.s, mds = d.md * a.s;
+    const bool wt = !(fabsf(mts) < 1e30f), wd = !(fabsf(mds) < 1e30f);
+    float zt[kPT], zd[kPT];
+    load_seg<ELT, VEC>(a.zt + ((size_t)b * (a.gamma + 1) + d.k) * rowbytes, a.V, j0, zt);
+    if (rej) load_seg<ELT, VEC>(a.zd + ((size_t)b * a.gamma + d.k) * rowbytes, a.V, j0, zd);
 #pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                float zt_, zd_;
-                if constexpr (ELT == 4) {
-                    zt_ = __uint_as_float(u4_get(qt, e));
-                    zd_ = __uint_as_float(u4_get(qd, e));
-                } else {
-                    const uint32_t wt = u4_get(qt, e >> 1), wd = u4_get(qd, e >> 1);
-                    zt_ = __uint_as_float((e & 1) ? (wt & 0xffff0000u) : (wt << 16));
-                    zd_ = __uint_as_float((e & 1) ? (wd & 0xffff0000u) : (wd << 16));
-                }
-                const float et = exp_scaled<ELT>(zt_, mt, a.T, a.invT);
-                ea[v * PV + e] = et;
-                ff_add(sa, et);
-                if (rej) {
-                    const float ed = exp_scaled<ELT>(zd_, md, a.T, a.invT);
-                    eb[v * PV + e] = ed;
-                    ff_add(sb, ed);
-                }
+    for (int e = 0; e < kPT; ++e) {
+        ea[e] = zt[e] == kNegInf ? 0.f : final_exp<ELT>(zt[e], d.mt, mts, wt, a);
+        eb[e] = (rej && zd[e] != kNegInf) ? final_exp<ELT>(zd[e], d.md, mds, wd, a) : 0.f;
+    }
+}
+
+// Residual weight max(0, p_k - q_k) scaled by Za: ea - (Za/Zb) eb, with the
+// ratio as a float-float pair (Rhi, Rlo).
+__device__ __forceinline__ float resid(float ea, float eb, float Rhi, float Rlo) {
+    return fmaxf(fmaf(-Rlo, eb, fmaf(-Rhi, eb, ea)), 0.f);
+}
+
+__device__ __forceinline__ FF sum_seg(const float (&w)[kPT]) {
+    FF acc{0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < kPT; ++e) ff_add(acc, w[e]);
+    return ff_norm(acc);
+}
+
+// The ratio Za / Zb of the two row normalisers of sequence b, from the chunk
+// sums (block-wide, identical in every CTA that calls it).
+__device__ __forceinline__ FF normaliser_ratio(const FinalArgs& a, int b, FF* wtot) {
+    FF za{0.f, 0.f}, zb{0.f, 0.f};
+    if ((int)threadIdx.x < a.C) {
+        const float4 q = a.zsum[(size_t)b * a.C + threadIdx.x];
+        za = FF{q.x, q.y};
+        zb = FF{q.z, q.w};
+    }
+    FF Za, Zb;
+    block_incl_scan_ff(za, wtot, &Za);
+    block_incl_scan_ff(zb, wtot, &Zb);
+    return ff_div(Za, Zb);
+}
+
+template <int ELT, bool VEC>
+__global__ void __launch_bounds__(kCT) sample_zsum_kernel(const FinalArgs a) {
+    __shared__ FF wtot[kCW];
+    const int c = blockIdx.x, b = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
+    const SampleDesc d = a.desc[b];
+    if (d.k < 0) return;
+    float ea[kPT], eb[kPT];
+    chunk_exps<ELT, VEC>(a, b, d, c, ea, eb);
+    FF Za, Zb;
+    block_incl_scan_ff(sum_seg(ea), wtot, &Za);
+    block_incl_scan_ff(sum_seg(eb), wtot, &Zb);
+    if (threadIdx.x == 0) a.zsum[(size_t)b * a.C + c] = make_float4(Za.hi, Za.lo, Zb.hi, Zb.lo);
+}
+
+template <int ELT, bool VEC>
+__global__ void __launch_bounds__(kCT) sample_wsum_kernel(const FinalArgs a) {
+    __shared__ FF wtot[kCW];
+    const int c = blockIdx.x, b = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
+    const SampleDesc d = a.desc[b];
+    if (d.k < 0 || d.k >= a.gamma) return;               // bonus rows use the exponential sums
+    const FF R = normaliser_ratio(a, b, wtot);
+    float ea[kPT], eb[kPT], w[kPT];
+    chunk_exps<ELT, VEC>(a, b, d, c, ea, eb);
+#pragma unroll
+    for (int e = 0; e < kPT; ++e) w[e] = resid(ea[e], eb[e], R.hi, R.lo);
+    FF W;
+    block_incl_scan_ff(sum_seg(w), wtot, &W);
+    if (threadIdx.x == 0) a.wsum[(size_t)b * a.C + c] = make_float2(W.hi, W.lo);
+}
+
+template <int ELT, bool VEC>
+__global__ void __launch_bounds__(kCT) sample_search_kernel(const FinalArgs a) {
+    __shared__ FF wtot[kCW];
+    __shared__ int s_sel, s_last;
+    __shared__ FF s_lo;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    const SampleDesc d = a.desc[b];
+    if (d.k < 0) return;
+    bool rej = d.k < a.gamma;
+    const FF R = rej ? normaliser_ratio(a, b, wtot) : FF{0.f, 0.f};
+
+    // Chunk totals and their prefix; fall back to p_k if the residual is empty.
+    FF T{0.f, 0.f}, S{0.f, 0.f}, incl{0.f, 0.f};
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        T = FF{0.f, 0.f};
+        if (tid < a.C) {
+            if (rej) {
+                const float2 q = a.wsum[(size_t)b * a.C + tid];
+                T = FF{q.x, q.y};
+            } else {
+                const float4 q = a.zsum[(size_t)b * a.C + tid];
+                T = FF{q.x, q.y};
             }
         }
-        jtail = nv * PV;
+        incl = block_incl_scan_ff(T, wtot, &S);
+        if (S.hi > 0.f || !rej) break;
+        rej = false;                                      // p_k equals q_k to rounding
     }
-    for (int j = jtail + tid; j < n; j += kFinalThreads) {
-        const float et = exp_scaled<ELT>(load_logit<ELT>(rt, j0 + j), mt, a.T, a.invT);
-        ea[j] = et;
-        ff_add(sa, et);
-        if (rej) {
-            const float ed = exp_scaled<ELT>(load_logit<ELT>(rd, j0 + j), md, a.T, a.invT);
-            eb[j] = ed;
-            ff_add(sb, ed);
-        }
-    }
-    const double za_part = block_sum_double(ff_value(sa), s_red);
-    const double zb_part = rej ? block_sum_double(ff_value(sb), s_red) : 0.0;
-    if (tid == 0) { s_za = za_part; s_zb = zb_part; }
-    cluster.sync();
-    double Za = 0.0, Zb = 0.0;
-    for (int r = 0; r < CS; ++r) {                        // same order in every CTA
-        Za += *cluster.map_shared_rank(&s_za, r);
-        Zb += *cluster.map_shared_rank(&s_zb, r);
-    }
+    if (!(S.hi > 0.f)) return;                            // unreachable for rows with a finite logit
+    const FF excl = block_excl_from_incl(incl, wtot);
+    FF target = ff_scale(a.u[(size_t)b * (a.gamma + 1) + a.gamma], S);
+    if (!ff_lt(target, S))                                // u >= 1 clamps to the last token with mass
+        target = ff_norm(FF{S.hi, S.lo - fabsf(S.hi) * 1.4210855e-14f});
 
-    // Phase B: weights.  p_k - q_k scaled by Za is ea - (Za/Zb) eb; the ratio is
-    // applied as a float-float pair so the subtraction sees it to ~1e-14.
-    float* w = ea;
-    if (rej) {
-        const double R = Za / Zb;
-        const float Rhi = (float)R;
-        const float Rlo = (float)(R - (double)Rhi);
-        for (int j = tid; j < n; j += kFinalThreads) {
-            const float t = fmaf(-Rhi, eb[j], ea[j]);
-            eb[j] = fmaxf(fmaf(-Rlo, eb[j], t), 0.f);
-        }
-        w = eb;
-    }
+    // The owning chunk: the one whose interval [excl, incl) holds the target.
+    // The intervals tile [0, S) exactly, so there is one; the last chunk with
+    // mass stands in should rounding ever leave a gap.
+    if (tid == 0) { s_sel = -1; s_last = -1; }
+    __syncthreads();
+    bool has = tid < a.C && T.hi > 0.f;
+    if (has && !ff_lt(target, excl) && ff_lt(target, incl)) { s_sel = tid; s_lo = excl; }
+    if (has) atomicMax(&s_last, tid);
+    __syncthreads();
+    if (s_sel < 0 && tid == s_last) { s_sel = tid; s_lo = excl; }
+    __syncthreads();
+    const int cs = s_sel;
+    const FF P = s_lo;
     __syncthreads();
 
-    const int E = (n + kFinalThreads - 1) / kFinalThreads;   // contiguous elements per thread
-    const int lo = min(n, tid * E), hi = min(n, lo + E);
-    int slot = 0;
-    double S = 0.0, P = 0.0;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const double ts = seg_sum(w, lo, hi);
-        block_incl_scan_double(ts, s_incl, s_wsum);
-        if (tid == 0) s_S[slot] = s_incl[kFinalThreads - 1];
-        cluster.sync();
-        double acc = 0.0;
-        P = 0.0;
-        for (int r = 0; r < CS; ++r) {
-            const double Sr = *cluster.map_shared_rank(&s_S[slot], r);
-            if (r == rank) P = acc;
-            acc = acc + Sr;
-        }
-        S = acc;
-        if (S > 0.0 || !rej || attempt == 1) break;
-        // No positive residual mass (p_k equals q_k to rounding): fall back to p_k.
-        w = ea;
-        slot = 1;
-    }
-
-    // Inverse CDF: the token is the first j whose prefix sum exceeds u * S.
-    // Thread intervals [P + incl(t-1), P + incl(t)) tile [0, S) exactly.
-    if (S > 0.0) {
-        double target = (double)a.u[(size_t)b * (a.gamma + 1) + a.gamma] * S;
-        if (!(target < S)) target = nextafter(S, 0.0);    // u >= 1 clamps to the last token with mass
-        const double Bt = P + (tid > 0 ? s_incl[tid - 1] : 0.0);
-        const double Et = P + s_incl[tid];
-        if (Et > Bt && Bt <= target && target < Et) {
-            FF run{0.f, 0.f};
-            int pick = -1, last = -1;
-            for (int j = lo; j < hi; ++j) {
-                ff_add(run, w[j]);
-                if (w[j] > 0.f) {
-                    last = j;
-                    if (pick < 0 && Bt + ff_value(run) > target) pick = j;
-                }
+    // Inside the chunk: the same weights and the same scan that produced its
+    // total, so the thread intervals tile [P, P + T_cs) exactly.
+    float ea[kPT], eb[kPT], w[kPT];
+    chunk_exps<ELT, VEC>(a, b, d, cs, ea, eb);
+#pragma unroll
+    for (int e = 0; e < kPT; ++e) w[e] = rej ? resid(ea[e], eb[e], R.hi, R.lo) : ea[e];
+    const FF ts = sum_seg(w);
+    FF tot;
+    const FF ti = block_incl_scan_ff(ts, wtot, &tot);
+    const FF te = block_excl_from_incl(ti, wtot);
+    const FF lo = ff_combine(P, te), hi = ff_combine(P, ti);
+    if (tid == 0) { s_sel = -1; s_last = -1; }
+    __syncthreads();
+    has = ts.hi > 0.f;
+    if (has && !ff_lt(target, lo) && ff_lt(target, hi)) s_sel = tid;
+    if (has) atomicMax(&s_last, tid);
+    __syncthreads();
+    const int owner = s_sel >= 0 ? s_sel : s_last;
+    if (tid == owner) {
+        // first element whose inclusive prefix exceeds the target; the last
+        // element with mass if rounding leaves none
+        FF run{0.f, 0.f};
+        int pick = -1, last = -1;
+#pragma unroll
+        for (int e = 0; e < kPT; ++e) {
+            ff_add(run, w[e]);
+            if (w[e] > 0.f) {
+                last = e;
+                if (pick < 0 && ff_lt(target, ff_combine(lo, ff_norm(run)))) pick = e;
             }
-            if (pick < 0) pick = last;
-            if (pick >= 0) a.out_tok[(size_t)b * (a.gamma + 1) + k] = j0 + pick;
         }
+        if (pick < 0) pick = last;
+        if (pick >= 0)
+            a.out_tok[(size_t)b * (a.gamma + 1) + d.k] = cs * kFinalChunk + tid * kPT + pick;
     }
-    cluster.sync();                                       // keep shared memory alive for remote readers
 }
 
 // ---------------------------------------------------------------- launch
@@ -430,48 +508,32 @@ static cudaError_t launch_stats_t(const StatsArgs& sa, const DeviceInfo& di, cud
     return cudaGetLastError();
 }
 
-template <int ELT, bool VEC>
-static cudaError_t launch_final_t(const FinalArgs& fa, int CS, size_t smem, bool pdl, cudaStream_t st) {
-    auto kfn = sample_final_kernel<ELT, VEC>;
-    static size_t smem_set = 0;                           // largest opt-in requested so far
-    if (smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+// Launch with programmatic stream serialisation: the kernel may start while
+// its predecessor drains and waits (griddepcontrol.wait) for its results.
+template <typename K>
+static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const FinalArgs& fa, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CS, fa.B, 1);
-    cfg.blockDim = dim3(kFinalThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kfn, fa);
 }
 
-// Cluster size for the final pass: enough CTAs per sequence to fill the GPU
-// when B is small, and slices (two float rows each) that fit in shared memory.
-static bool final_geometry(int B, int V, const DeviceInfo& di, int* CS_out, int* L_out) {
-    const int max_L = (di.max_smem_optin - kFinalStaticSmem) / 8;
-    int CS = 1;
-    while (CS < 16 && ((long long)CS * max_L < V ||
-                       ((long long)CS * B < di.sm_count && V / (CS * 2) >= 4096)))
-        CS *= 2;
-    int Ls = (V + CS - 1) / CS;
-    Ls = (Ls + 7) & ~7;
-    if (Ls > max_L) return false;
-    *CS_out = CS;
-    *L_out = Ls;
-    return true;
+template <int ELT, bool VEC>
+static cudaError_t launch_final_t(const FinalArgs& fa, cudaStream_t st) {
+    cudaError_t e = launch_pdl(sample_decide_kernel<ELT>, dim3(fa.B), kDecideThreadsS, fa, st);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(fa.C, fa.B), kCT, fa, st);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(sample_wsum_kernel<ELT, VEC>, dim3(fa.C, fa.B), kCT, fa, st);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(sample_search_kernel<ELT, VEC>, dim3(fa.B), kCT, fa, st);
 }
 
 cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
@@ -498,13 +560,27 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
         sa.rows_per_seq = 2 * gamma + 1;
         sa.total_chunks = (long long)B * sa.rows_per_seq * sa.nseg;
         sa.parts = parts_buf;
-        if (elt == 2) e = vec ? launch_stats_t<2, true>(sa, di, st) : launch_stats_t<2, false>(sa, di, st);
-        else e = vec ? launch_stats_t<4, true>(sa, di, st) : launch_stats_t<4, false>(sa, di, st);
+        RingArgs ra;
+        ra.zt = sa.zt;
+        ra.zd = sa.zd;
+        ra.gamma = gamma;
+        ra.rows_per_seq = sa.rows_per_seq;
+        ra.V = V;
+        ra.nseg = sa.nseg;
+        ra.total_chunks = sa.total_chunks;
+        ra.s = s;
+        ra.parts = parts_buf;
+        ra.err = reinterpret_cast<int*>(w + L.err_off);
+        bool used = false;
+        e = elt == 2 ? launch_ring<2, false>(ra, di, st, &used) : launch_ring<4, false>(ra, di, st, &used);
         if (e != cudaSuccess) return e;
+        if (!used) {
+            if (elt == 2) e = vec ? launch_stats_t<2, true>(sa, di, st) : launch_stats_t<2, false>(sa, di, st);
+            else e = vec ? launch_stats_t<4, true>(sa, di, st) : launch_stats_t<4, false>(sa, di, st);
+            if (e != cudaSuccess) return e;
+        }
     }
     if (parts & kSampleFinish) {
-        int CS = 1, Ls = 0;
-        if (!final_geometry(B, V, di, &CS, &Ls)) return cudaErrorInvalidValue;
         FinalArgs fa;
         fa.zt = static_cast<const char*>(zt);
         fa.zd = static_cast<const char*>(zd);
@@ -518,25 +594,24 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
         fa.V = V;
         fa.nseg = nseg(V, elt);
         fa.rows_per_seq = 2 * gamma + 1;
-        fa.L = Ls;
+        fa.C = final_chunks(V);
         fa.parts = parts_buf;
+        fa.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
+        fa.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
+        fa.wsum = reinterpret_cast<float2*>(w + L.wsum_off);
         fa.out_tok = out_tok;
         fa.out_acc = out_acc;
         fa.out_lp = out_lp;
         fa.err = reinterpret_cast<int*>(w + L.err_off);
-        const size_t smem = (size_t)Ls * 2 * sizeof(float);
-        const bool pdl = (parts & kSampleStats) != 0;     // chained right behind pass 1
-        if (elt == 2) e = vec ? launch_final_t<2, true>(fa, CS, smem, pdl, st) : launch_final_t<2, false>(fa, CS, smem, pdl, st);
-        else e = vec ? launch_final_t<4, true>(fa, CS, smem, pdl, st) : launch_final_t<4, false>(fa, CS, smem, pdl, st);
+        if (elt == 2) e = vec ? launch_final_t<2, true>(fa, st) : launch_final_t<2, false>(fa, st);
+        else e = vec ? launch_final_t<4, true>(fa, st) : launch_final_t<4, false>(fa, st);
     }
     return e;
 }
 
 bool sample_supported_vocab(int V) {
-    DeviceInfo di;
-    if (device_info(&di) != cudaSuccess) return true;     // reported by the launch instead
-    int CS, Ls;
-    return final_geometry(1, V, di, &CS, &Ls);
+    // the search kernel scans all chunk totals of a row in one CTA
+    return final_chunks(V) <= kFinalChunkThreads;
 }
 
 }  // namespace sv

@@ -235,3 +235,29 @@ def test_split_stats_finish_equals_composite(sv):
                                         acc2.data_ptr(), lp2.data_ptr(), wp, wb, st) == sv.SPEC_OK
     torch.cuda.synchronize()
     assert torch.equal(tok1, tok2) and torch.equal(acc1, acc2) and torch.equal(lp1, lp2)
+
+
+def test_sample_largest_vocabulary_and_beyond(sv):
+    """A vocabulary of 1M works; above 2097152 (256 chunks of 8192, the most
+    the search kernel scans) the call is refused with SPEC_ERR_INVALID_ARG."""
+    x = W.make_chain("chain-b8", B=1, gamma=2, V=1 << 20)
+    check_sample(sv, x)
+    big = 2097153
+    fake = 1 << 20
+    ws = sv.Workspace()
+    wp, wb = ws.get(1, 1, big)
+    st = sv.spec_verify_sample(fake, fake, sv.SPEC_DTYPE_BF16, fake, fake, 1.0, 1, 1, big, fake,
+                               fake, None, wp, wb, None)
+    assert st == sv.SPEC_ERR_INVALID_ARG
+
+
+def test_no_device_error_on_valid_inputs(sv):
+    """Valid calls of every mode leave the device error word clear (no bad
+    input, and no bounded wait inside a kernel ever ran out)."""
+    ws = sv.Workspace()
+    a = W.make_chain("chain-b64", B=8, V=151936)
+    t = W.make_tree(B=4, V=151936)
+    check_sample(sv, a, ws=ws)
+    check_greedy(sv, a.target, a.dtype, a.draft_tokens, ws=ws)
+    check_tree(sv, t, ws=ws)
+    assert ws.read_error() == 0

@@ -1,0 +1,75 @@
+"""Sampling parity rate on the four chain workloads at full size.
+
+The parity contract for stochastic verification: accept counts and tokens
+equal the fp64 oracle's, except where the oracle's own margin is below 1e-4
+(|u - p/q| for an accept decision, or u's distance to the CDF interval of
+the token the GPU drew); such excused differences must stay under 0.01 % of
+rows, rows being (sequence, position) pairs B * (gamma + 1).  Each workload's
+logits and drafts are generated once; every round draws fresh uniforms, so
+decisions and final samples vary from round to round.  About 1e5 rows per
+workload make the rate meaningful at the 1e-4 level.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verification_59_gb300 import workloads as W
+
+from parity import compare_sample
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+RATE_BAR = 1e-4
+ROWS_TARGET = 100_000
+OUT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verification_59_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("name", ["chain-small", "chain-b8", "chain-b64", "chain-b256"])
+def test_sampling_mismatch_rate(sv, name):
+    x = W.make_chain(name)
+    dt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    zt = torch.from_numpy(x.target).cuda().to(dt)
+    zd = torch.from_numpy(x.draft).cuda().to(dt)
+    xt = torch.from_numpy(x.draft_tokens).cuda()
+    rows_per_round = x.B * (x.gamma + 1)
+    rounds = max(1, -(-ROWS_TARGET // rows_per_round))
+    rng = np.random.default_rng(12345)
+    ws = sv.Workspace()
+    excused = exact = rows = 0
+    failures = []
+    accepted = []
+    for _ in range(rounds):
+        u = rng.random((x.B, x.gamma + 1), dtype=np.float32)
+        tok, acc = sv.verify_sample(zt, zd, xt, torch.from_numpy(u).cuda(), x.T, workspace=ws)
+        tok, acc = tok.cpu().numpy(), acc.cpu().numpy()
+        ref = oracle.verify_sample(x.target, x.draft, x.draft_tokens, u, x.T, want_ratio=True,
+                                   want_cdf=True)
+        res = compare_sample(tok, acc, ref, x.draft_tokens, u)
+        failures += res["failures"]
+        excused += res["excused"]
+        exact += res["exact"]
+        rows += res["rows"]
+        accepted.append(acc.mean())
+    rate = excused / rows
+    summary = {"workload": name, "rounds": rounds, "rows": rows, "sequences": rounds * x.B,
+               "exact_final_tokens": exact, "excused": excused, "hard_failures": len(failures),
+               "excused_rate_per_row": rate, "bar": RATE_BAR,
+               "mean_tokens_per_round": float(np.mean(accepted)) + 1.0}
+    print(json.dumps(summary))
+    if os.path.isdir(OUT):
+        with open(os.path.join(OUT, f"rate_{name}.json"), "w") as f:
+            json.dump(summary, f)
+    assert not failures, failures[:5]
+    assert rate < RATE_BAR, summary
