@@ -90,7 +90,7 @@ def kernel_source_hash():
     recorded under profiles/ are only reported while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_59_gb300", "csrc")
-    for f in ("sv_common.cuh", "sv_internal.h", "sv_sample.cu"):
+    for f in ("sv_common.cuh", "sv_internal.h", "sv_tma.cuh", "sv_decide.cuh", "sv_stream.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -357,7 +357,7 @@ def run_own(args):
             "rounds_per_s": world * x.B * K / (ms_max * 1e-3),
             "tau": {"sample": tau_sample, "greedy": tau_greedy},
             "roofline": {
-                "kernel": "sample_rowstats_kernel (spec_verify_sample_stats)",
+                "kernel": "ring_stream_kernel<bf16, sample> (spec_verify_sample_stats)",
                 "bound": "hbm",
                 "achieved": achieved,
                 "peak": peak,
@@ -376,7 +376,7 @@ def run_own(args):
                 "d2h_bytes_per_step": bo,
                 "steps": Ke,
             },
-            "gpu_launches": 4 * K,
+            "gpu_launches": 9 * K,
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -34,8 +34,8 @@
  *     bytes are the device error word (below): zero-fill the workspace once
  *     (spec_verify_workspace_init) so that word starts clear.  Everything
  *     else in it is rewritten by each call before it is read, so one
- *     workspace serves calls of any mode and size.  Calls that share a
- *     workspace must be ordered on the device (same stream, or events);
+ *     workspace serves calls of any mode and size in turn.  Calls that share
+ *     a workspace must be ordered on the device (same stream, or events);
  *     overlapping calls on one workspace race.
  *   - Host-side argument checks return immediately without touching the
  *     device.  Bad input that only the device can see (a draft token outside
@@ -109,9 +109,9 @@ spec_status_t spec_verify_workspace_init(void* workspace, size_t workspace_bytes
  *   out_logprobs     [B, gamma, 2] f32, nullable: ln p_i(x_i), ln q_i(x_i)
  *
  * A streaming pass over every logit row (row max and sum-exp partials) is
- * followed by four small kernels: the accept decisions (one CTA per
- * sequence), the chunk sums of the exponentials and of the residual weights
- * of the one rejected (or bonus) row pair, and the inverse-CDF search.
+ * followed by four small kernels: the accept decisions, the chunk sums of the
+ * exponentials and of the residual weights of the one rejected (or bonus)
+ * row pair, and the inverse-CDF search.
  */
 spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
                                  spec_dtype_t dtype, const int32_t* draft_tokens,
@@ -127,9 +127,9 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
  *   _stats:  streams every logit row once and leaves per-row partial
  *            statistics (running max and sum of exponentials) in the
  *            workspace.  Writes no output.
- *   _finish: merges those statistics, takes the accept decisions and draws
- *            the final token of every sequence (residual after a rejection,
- *            bonus otherwise); writes every output of spec_verify_sample.
+ *   _finish: takes the accept decisions from those statistics and draws the
+ *            final token of every sequence (residual after a rejection, bonus
+ *            otherwise); writes every output of spec_verify_sample.
  * The workspace and the logits must stay unchanged between the two calls.
  */
 spec_status_t spec_verify_sample_stats(const void* target_logits, const void* draft_logits,

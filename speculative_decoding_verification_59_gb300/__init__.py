@@ -184,8 +184,8 @@ def _check(status: int, what: str):
 
 
 class Workspace:
-    """Device scratch for the verification calls, zero-filled at creation (the
-    error word must start clear).  Grows on demand."""
+    """Device scratch for the verification calls, zero-filled when it is
+    (re)allocated so the error word starts clear.  Grows on demand."""
 
     def __init__(self, device=None):
         torch = _torch()

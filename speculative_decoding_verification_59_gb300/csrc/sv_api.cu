@@ -119,7 +119,8 @@ spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
                                  int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
     if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || gamma < 0 || gamma + 1 > kMaxNodesApi || V <= 0) return SPEC_ERR_INVALID_ARG;
+    if (B < 0 || gamma < 0 || gamma + 1 > kMaxNodesApi || V <= 0)
+        return SPEC_ERR_INVALID_ARG;
     if (B == 0) return SPEC_OK;
     if (!target_logits || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens))
         return SPEC_ERR_INVALID_ARG;

@@ -1,0 +1,312 @@
+// Per-sequence decisions from the streaming pass's per-warp partials.
+//
+// Sources: "Speculative decoding: guess a few tokens first - why the answer
+// stays the same", section "What happens in one round" step 3 (accept x_i
+// with probability min(1, p_i(x_i)/q_i(x_i)), left to right, the first
+// rejection voiding the rest) and its greedy paragraph (accept while the
+// draft equals the target argmax); "AdaPLD: adaptive retrieval and reuse for
+// efficient model-free speculative decoding", section 3.3 and Algorithm 1
+// (VerifyAndAccept over the draft tree).
+//
+// A decision is taken by a group of kGroup threads (a whole 256-thread CTA)
+// synchronised on named barrier 1; gt is the thread's index in the group.
+// Each runs in its own kernel, one CTA per sequence (sv_argmax.cu for greedy
+// chains and trees, sv_sample.cu for sampling).
+#pragma once
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr int kGroup = kThreads;                 // 256
+constexpr int kMaxGamma = 256;                   // sampling: rows per sequence <= 513
+constexpr int kMaxNodes = 1024;                  // greedy chains and trees: rows <= 1024
+
+enum : int { kModeSample = 0, kModeGreedy = 1, kModeTree = 2 };
+
+struct VerifyArgs {
+    const char* zt;            // target logits
+    const char* zd;            // draft logits (sampling)
+    const int32_t* x;          // draft tokens (chains) / node tokens (trees)
+    const int32_t* par;        // parents (trees)
+    const float* u;            // uniforms (sampling)
+    float T, invT, s, s_lo;    // temperature, 1/T, log2(e)/T as a float-float pair (s, s_lo)
+    int gamma;                 // drafts per sequence (chains)
+    int rows_per_seq;          // 2*gamma+1 (sampling), gamma+1 (greedy), N (tree)
+    int V, nseg;
+    long long total_chunks;
+    int B;
+    int C;                     // sampling: final-pass chunks per row
+    float2* parts;             // per-warp-chunk partials
+    SampleDesc* desc;          // sampling: rejection index and row maxima
+    float4* zsum;              // sampling: [B, C] (Za.hi, Za.lo, Zb.hi, Zb.lo) per chunk
+    float2* wsum;              // sampling: [B, C] residual weight total per chunk
+    int* err;
+    int32_t* out_tok;
+    int32_t* out_acc;
+    float* out_lp;             // sampling, nullable
+    int32_t* out_nodes;        // trees
+};
+
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Row r of sequence b of a sampling batch: r <= gamma is target row r, r > gamma
+// is draft row r-gamma-1.
+__device__ __forceinline__ const char* sample_row(const VerifyArgs& a, int b, int r, size_t rowbytes) {
+    return r <= a.gamma ? a.zt + ((size_t)b * (a.gamma + 1) + r) * rowbytes
+                        : a.zd + ((size_t)b * a.gamma + (r - a.gamma - 1)) * rowbytes;
+}
+
+// ---------------------------------------------------------------- sampling
+struct SampleDecideSmem {
+    float M[2 * kMaxGamma + 1];       // row max
+    float lnZ[2 * kMaxGamma + 1];     // ln sum exp((z - M)/T)
+    float lp[kMaxGamma], lq[kMaxGamma];
+    int bad, k;
+};
+
+// Row statistics from the partials (M = max m_p, Z = sum Z_p 2^((m_p - M) s),
+// float-float) and the accept decisions u_i < p_i(x_i)/q_i(x_i) in single
+// precision (GB300's double-precision rate is a small fraction of its float
+// rate): ln p_i(x_i) and ln q_i(x_i) carry errors of ~1e-6, far inside the
+// 1e-4 decision margin and the 1e-5 bar on returned probabilities.  Leaves
+// the rejection index in sm.k (-1: bad input) and the row statistics in sm.
+template <int ELT>
+__device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
+    const int lane = gt & 31, gw = gt >> 5;
+    const int P = a.nseg * kWarps;
+    const size_t rowbytes = (size_t)a.V * ELT;
+    // Issue the gathers of z[x_i] first: their latency overlaps the merges.
+    int xi = -1;
+    float ztx = 0.f, zdx = 0.f;
+    if (gt < a.gamma) {
+        xi = a.x[(size_t)b * a.gamma + gt];
+        if (xi >= 0 && xi < a.V) {
+            ztx = load_logit<ELT>(sample_row(a, b, gt, rowbytes), xi);
+            zdx = load_logit<ELT>(sample_row(a, b, a.gamma + 1 + gt, rowbytes), xi);
+        }
+    }
+    if (gt == 0) sm.bad = 0;
+    group_sync();
+    // Row r: M = max m_p, Z = sum Z_p 2^((m_p - M) s) over its warp partials,
+    // each lane holding up to kHeld of them in registers (float-float sum).
+    constexpr int kHeld = 8;
+    for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
+        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
+        float2 q[kHeld];
+#pragma unroll
+        for (int h = 0; h < kHeld; ++h) {
+            const int p = lane + 32 * h;
+            q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
+        }
+        float m = kNegInf;
+#pragma unroll
+        for (int h = 0; h < kHeld; ++h) m = fmaxf(m, q[h].x);
+        for (int p = lane + 32 * kHeld; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
+        m = warp_max(m);
+        FF z{0.f, 0.f};
+        if (m != kNegInf) {
+#pragma unroll
+            for (int h = 0; h < kHeld; ++h)
+                if (q[h].x != kNegInf) ff_add(z, q[h].y * ex2_approx((q[h].x - m) * a.s));
+            for (int p = lane + 32 * kHeld; p < P; p += 32) {
+                const float2 t = __ldcg(&pr[p]);
+                if (t.x != kNegInf) ff_add(z, t.y * ex2_approx((t.x - m) * a.s));
+            }
+        }
+        z = ff_norm(warp_sum_ff(z));
+        if (lane == 0) {
+            sm.M[r] = m;
+            sm.lnZ[r] = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
+        }
+    }
+    group_sync();
+    for (int i = gt; i < a.gamma; i += kGroup) {
+        if (i != gt) {                                     // gamma > kGroup: late gathers
+            xi = a.x[(size_t)b * a.gamma + i];
+            if (xi >= 0 && xi < a.V) {
+                ztx = load_logit<ELT>(sample_row(a, b, i, rowbytes), xi);
+                zdx = load_logit<ELT>(sample_row(a, b, a.gamma + 1 + i, rowbytes), xi);
+            }
+        }
+        if (xi < 0 || xi >= a.V) {
+            atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
+            sm.lp[i] = sm.lq[i] = 0.f;
+        } else {
+            sm.lp[i] = (ztx - sm.M[i]) * a.invT - sm.lnZ[i];
+            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) * a.invT - sm.lnZ[a.gamma + 1 + i];
+        }
+    }
+    for (int r = gt; r < a.rows_per_seq; r += kGroup)
+        if (sm.M[r] == kNegInf) atomicOr(&sm.bad, SPEC_DEVERR_EMPTY_ROW);
+    group_sync();
+    if (gt == 0) {
+        int k = -1;
+        if (!sm.bad) {
+            k = a.gamma;                                   // left to right; first rejection wins
+            for (int i = 0; i < a.gamma; ++i) {
+                const float lp = sm.lp[i], lq = sm.lq[i];
+                float r;
+                if (lp == kNegInf) r = 0.f;
+                else if (lq == kNegInf) r = CUDART_INF_F;
+                else r = expf(lp - lq);
+                if (!(a.u[(size_t)b * (a.gamma + 1) + i] < r)) { k = i; break; }
+            }
+        }
+        sm.k = k;
+    }
+    group_sync();
+}
+
+// Every output of the sampling decision but the final token, and the
+// SampleDesc the final-sample kernels read.
+static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt, const SampleDecideSmem& sm) {
+    const int k = sm.k;
+    if (gt == 0) {
+        if (sm.bad) atomicOr(a.err, sm.bad);
+        a.out_acc[b] = k;
+        SampleDesc d;
+        d.k = k;
+        d.mt = k >= 0 ? sm.M[k] : 0.f;
+        d.md = (k >= 0 && k < a.gamma) ? sm.M[a.gamma + 1 + k] : 0.f;
+        d.pad = 0;
+        a.desc[b] = d;
+    }
+    // accepted drafts and padding; slot k belongs to the search kernel
+    for (int i = gt; i <= a.gamma; i += kGroup)
+        if (k < 0 || i != k)
+            a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
+    if (a.out_lp)
+        for (int i = gt; i < a.gamma; i += kGroup) {
+            float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
+            o[0] = k >= 0 ? sm.lp[i] : CUDART_NAN_F;
+            o[1] = k >= 0 ? sm.lq[i] : CUDART_NAN_F;
+        }
+}
+
+// ---------------------------------------------------------- greedy and trees
+struct ArgmaxDecideSmem {
+    int g[kMaxNodes];                 // row argmax
+    int depth[kMaxNodes];             // trees: longest accepted continuation
+    int best[kMaxNodes];              // trees: child that continues it
+    int k, len, bad;
+};
+
+// Argmax of every row of sequence b from the (value, index) partials.
+__device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, int gt, int* g) {
+    const int lane = gt & 31, gw = gt >> 5;
+    const int P = a.nseg * kWarps;
+    for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
+        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
+        float bv = kNegInf;
+        int bi = 0x7fffffff;
+        for (int p = lane; p < P; p += 32) {
+            const float2 q = __ldcg(&pr[p]);
+            const int qi = __float_as_int(q.y);
+            if (am_better(q.x, qi, bv, bi)) { bv = q.x; bi = qi; }
+        }
+        warp_argmax(bv, bi);
+        if (lane == 0) g[r] = bi;
+    }
+    group_sync();
+}
+
+// Greedy chain: k = first i with x_i != argmax of row i, else gamma; output
+// x_0..x_{k-1} then the target argmax of row k.
+static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
+    const int G = a.gamma;
+    merge_argmax_rows(a, b, gt, sm.g);
+    if (gt == 0) {
+        int bad = 0;
+        for (int i = 0; i < G; ++i) {
+            const int xi = a.x[(size_t)b * G + i];
+            if (xi < 0 || xi >= a.V) bad = 1;
+        }
+        int k = G;
+        if (bad) {
+            atomicOr(a.err, SPEC_DEVERR_TOKEN_RANGE);
+            k = -1;
+        } else {
+            for (int i = 0; i < G; ++i)
+                if (a.x[(size_t)b * G + i] != sm.g[i]) { k = i; break; }
+        }
+        sm.k = k;
+        a.out_acc[b] = k;
+    }
+    group_sync();
+    const int k = sm.k;
+    for (int i = gt; i <= G; i += kGroup) {
+        int v = -1;
+        if (k >= 0) v = i < k ? a.x[(size_t)b * G + i] : (i == k ? sm.g[k] : -1);
+        a.out_tok[(size_t)b * (G + 1) + i] = v;
+    }
+}
+
+// Draft tree: a node is accepted when its parent is and its token is the
+// argmax of the parent's row; output the longest accepted root path (ties:
+// lowest node ids) and the argmax of the path's last node.
+static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
+    const int N = a.rows_per_seq;
+    const int32_t* tok = a.x + (size_t)b * N;
+    const int32_t* par = a.par + (size_t)b * N;
+    if (gt == 0) sm.bad = 0;
+    merge_argmax_rows(a, b, gt, sm.g);                     // ends with group_sync
+    for (int n = gt; n < N; n += kGroup) {
+        const int p = par[n];
+        if (n == 0 ? p != -1 : (p < 0 || p >= n)) atomicOr(&sm.bad, SPEC_DEVERR_TREE_PARENT);
+        if (n > 0) {
+            const int t = tok[n];
+            if (t < 0 || t >= a.V) atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
+        }
+        sm.depth[n] = 0;
+        sm.best[n] = -1;
+    }
+    group_sync();
+    int32_t* on = a.out_nodes + (size_t)b * N;
+    int32_t* ot = a.out_tok + (size_t)b * N;
+    if (gt == 0) {
+        int len = -1;
+        if (sm.bad) {
+            atomicOr(a.err, sm.bad);
+        } else {
+            // Children have larger ids than their parent, so one descending
+            // sweep finalises each node before its parent reads it; on equal
+            // length the lower child id wins.  Nodes whose parent is not
+            // accepted are never reached from the root, which enforces the
+            // parent condition.
+            for (int n = N - 1; n >= 1; --n) {
+                const int p = par[n];
+                if (tok[n] != sm.g[p]) continue;
+                if (1 + sm.depth[n] >= sm.depth[p]) { sm.depth[p] = 1 + sm.depth[n]; sm.best[p] = n; }
+            }
+            len = 0;
+            int cur = 0;
+            while (sm.best[cur] >= 0) {
+                cur = sm.best[cur];
+                on[len] = cur;
+                ot[len] = tok[cur];
+                ++len;
+            }
+            ot[len] = sm.g[cur];
+        }
+        sm.len = len;
+        a.out_acc[b] = len;
+    }
+    group_sync();
+    const int len = sm.len;
+    for (int n = gt; n < N; n += kGroup) {
+        if (len < 0 || n >= len) on[n] = -1;
+        if (len < 0 || n > len) ot[n] = -1;
+    }
+}
+
+// The contiguous range of block chunks [*c0, *c1) that CTA `cta` of `ncta`
+// streams, balanced to within one chunk.
+__device__ __forceinline__ void cta_range(unsigned total, unsigned cta, unsigned ncta, unsigned* c0,
+                                          unsigned* c1) {
+    const unsigned q = total / ncta, r = total % ncta;
+    *c0 = cta * q + min(cta, r);
+    *c1 = *c0 + q + (cta < r ? 1u : 0u);
+}
+
+}  // namespace sv

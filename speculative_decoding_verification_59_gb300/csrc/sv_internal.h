@@ -42,10 +42,10 @@ struct SampleDesc {
 
 // Workspace: [error word (256 bytes reserved) | per-warp row partials |
 // SampleDesc[B] | per-chunk normaliser sums | per-chunk residual sums].
-// Every region after the error word is fully rewritten by the kernels of a
-// call before another kernel of that call reads it, so a workspace carries
-// nothing from one call to the next except the error word, which only
-// accumulates error bits until spec_verify_read_error clears it.
+// Every region after the error word is rewritten by the kernels of a call
+// before another kernel of that call reads it, so a workspace carries nothing
+// from one call to the next except the error word, which only accumulates
+// error bits until spec_verify_read_error clears it.
 struct WsLayout {
     size_t err_off, part_off, part_count, desc_off, zsum_off, wsum_off, total;
 };
@@ -76,7 +76,7 @@ struct DeviceInfo {
 cudaError_t device_info(DeviceInfo* out);
 
 // ---- launchers (return the first CUDA error) ------------------------------
-// parts: kSampleStats (streaming row statistics), kSampleFinish (accept
+// parts: kSampleStats (streaming row statistics), kSampleFinish (the accept
 // decisions and the final residual/bonus token), or both.
 constexpr int kSampleStats = 1;
 constexpr int kSampleFinish = 2;
@@ -84,7 +84,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
                           const float* u, float T, int B, int gamma, int V, int32_t* out_tok,
                           int32_t* out_acc, float* out_lp, void* ws, cudaStream_t st, int parts);
 
-// Whether the final sampling pass can stage a row pair of this vocabulary.
+// Whether the final sampling pass supports this vocabulary size.
 bool sample_supported_vocab(int V);
 
 cudaError_t launch_greedy(const void* zt, spec_dtype_t dt, const int32_t* x, int B, int gamma,

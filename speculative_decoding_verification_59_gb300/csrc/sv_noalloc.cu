@@ -72,10 +72,10 @@ extern "C" spec_status_t spec_verify_sample_noalloc(
     if (!sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
-    // The partials are rewritten by the streaming kernel before the second
-    // kernel reads them, so nothing in the scratch has to start at zero; the
-    // error word in its first bytes only ever gains bits and is not reported
-    // by this entry point (bad sequences still come back with -1).
+    // Every region the kernels read is written earlier in the same call, so
+    // nothing in the scratch has to start at zero; the error word in its first
+    // bytes only ever gains bits and is not reported by this entry point (bad
+    // sequences still come back with -1).
     cudaError_t e = launch_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                                   temperature, B, gamma, V, out_tokens, out_num_accepted,
                                   out_logprobs, scratch, stream, kSampleStats | kSampleFinish);

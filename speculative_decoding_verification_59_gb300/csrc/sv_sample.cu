@@ -5,19 +5,19 @@
 // "Why fixing wrong guesses does not leave the target distribution" (residual
 // p'(x) = norm(max(0, p(x) - q(x)))).
 //
-// Pass 1 streams every logit once (ring_stream_kernel in sv_stream.cuh for
-// 16-byte rows, sample_rowstats_kernel below otherwise): each warp chunk of
-// each of the 2*gamma+1 rows of every sequence becomes a partial (max m,
-// sum 2^((z - m) log2(e)/T)).
+// Pass 1 streams every logit once (sv_stream.cuh): each warp chunk of each of
+// the 2*gamma+1 rows of every sequence becomes a partial (max m, sum
+// 2^((z - m) log2(e)/T)).
 //
-// Pass 2 draws the final token of every sequence from the single row pair it
-// comes from -- target and draft row k after a rejection at k (weights
-// max(0, p_k - q_k)), target row gamma when every draft was accepted (weights
-// p_gamma) -- by inverse CDF in index order.  Four small kernels, chained with
-// programmatic dependent launch, keep every sequence in flight at once:
+// Pass 2 takes the accept decisions (sv_decide.cuh) and draws the final token
+// of every sequence from the single row pair it comes from -- target and
+// draft row k after a rejection at k (weights max(0, p_k - q_k)), target row
+// gamma when every draft was accepted (weights p_gamma) -- by inverse CDF in
+// index order.  Four kernels, chained with programmatic dependent launch,
+// keep every sequence in flight at once:
 //   sample_decide_kernel  one CTA per sequence: row statistics from the
-//                         partials, accept decisions u_i < p_i(x_i)/q_i(x_i)
-//                         left to right, all outputs but the final token;
+//                         partials, the accept decisions, every output but
+//                         the final token;
 //   sample_zsum_kernel    one CTA per 8192-element chunk of row k: sums of the
 //                         exponentials of the target and draft chunk;
 //   sample_wsum_kernel    one CTA per chunk (rejections only): the ratio of the
@@ -30,125 +30,62 @@
 // all sums are float-float (about 48 bits), and a chunk's total and the scan
 // that later searches inside it come from the same block-scan code, so the
 // intervals of chunks, threads and elements tile [0, S) exactly.
-#include "sv_common.cuh"
 #include "sv_stream.cuh"
 
 namespace sv {
 
 #ifndef SV_FINAL_EXACT_EXP
-#define SV_FINAL_EXACT_EXP 1
+#define SV_FINAL_EXACT_EXP 0
 #endif
 
-constexpr int kMaxGamma = 256;                 // rows per sequence <= 2*256+1
-constexpr int kDecideThreadsS = 512;
-
-struct StatsArgs {
-    const char* zt;
-    const char* zd;
-    float s;            // log2(e) / T
-    int gamma, V;
-    int nseg;           // block chunks per row
-    int rows_per_seq;   // 2 * gamma + 1
-    long long total_chunks;
-    float2* parts;
-};
-
-struct FinalArgs {
-    const char* zt;
-    const char* zd;
-    const int32_t* x;
-    const float* u;
-    float T, invT, s;
-    int B, gamma, V;
-    int nseg, rows_per_seq;
-    int C;              // 2048-element chunks per row
-    const float2* parts;
-    SampleDesc* desc;
-    float4* zsum;       // [B, C]: (Za.hi, Za.lo, Zb.hi, Zb.lo) of each chunk
-    float2* wsum;       // [B, C]: residual weight total of each chunk
-    int32_t* out_tok;
-    int32_t* out_acc;
-    float* out_lp;
-    int* err;
-};
-
-// Row r of sequence b: r <= gamma is target row r, r > gamma is draft row r-gamma-1.
-__device__ __forceinline__ const char* seq_row(const char* zt, const char* zd, int gamma, int b,
-                                               int r, size_t rowbytes) {
-    return r <= gamma ? zt + ((size_t)b * (gamma + 1) + r) * rowbytes
-                      : zd + ((size_t)b * gamma + (r - gamma - 1)) * rowbytes;
-}
-
-template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kThreads) sample_rowstats_kernel(const StatsArgs a) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int WE = 32 * kLaneBytes / ELT;              // elements per warp chunk
-    const int P = a.nseg * kWarps;
-    const size_t rowbytes = (size_t)a.V * ELT;
-
-    for (long long c = blockIdx.x; c < a.total_chunks; c += gridDim.x) {
-        if (c + gridDim.x >= a.total_chunks) pdl_trigger();
-        const int seg = (int)(c % a.nseg);
-        const long long rr = c / a.nseg;
-        const int b = (int)(rr / a.rows_per_seq);
-        const int r = (int)(rr % a.rows_per_seq);
-        const char* row = seq_row(a.zt, a.zd, a.gamma, b, r, rowbytes);
-        const int base = (seg * kWarps + warp) * WE;
-
-        float m = kNegInf, z = 0.f;
-        if (base < a.V) {
-            LaneChunk<ELT, VEC> ch;
-            ch.load(row, a.V, base, lane);
-#pragma unroll
-            for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i) m = fmaxf(m, ch.val(i));
-            m = warp_max(m);
-            if (m != kNegInf) {
-#pragma unroll
-                for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i)
-                    z += ex2_approx((ch.val(i) - m) * a.s);
-                z = warp_sum(z);
-            }
-        }
-        if (lane == 0) a.parts[(size_t)rr * P + seg * kWarps + warp] = make_float2(m, z);
-    }
-}
 
 // ---------------------------------------------------------------- pass 2
 constexpr int kCT = kFinalChunkThreads;        // threads per chunk CTA (kFinalPerThread elements each)
 constexpr int kCW = kCT / 32;
 
-// exp((z - m) / T) for the final pass.  The default (SV_FINAL_EXACT_EXP=1)
-// carries (z - m)/T as two floats into expf, leaving only expf's own rounding
-// and one product: measured over 1e5 rows of the B=8, T=1 workload it halves
-// the mismatches against the fp64 reference compared with the cheaper
-// SV_FINAL_EXACT_EXP=0 form, 2^(z*s - m*s) from one fused multiply-add and the
-// special-function unit (m*s is rounded once per row, a common factor that the
-// normalisation cancels).
+// exp((z - m) / T) for the final pass, as 2^x with x = (z - m) log2(e)/T
+// carried in two floats: x_hi into the special-function unit, x_lo through
+// the first-order factor (1 + x_lo ln 2).  Measured against exact values on
+// GB300 the result has a relative error of mean -4.9e-8 and RMS 6.4e-8 over
+// bf16 logits in [-25, 0] -- the mean is a common factor of every weight,
+// which the normalisation cancels, and the rest matches expf's 3.8e-8 RMS at
+// less than half its instruction count.  SV_FINAL_EXACT_EXP=1 selects expf
+// with a two-float argument instead (for accuracy studies).
+constexpr float kLn2 = 0.6931471805599453f;
+
 template <int ELT>
-__device__ __forceinline__ float final_exp(float z, float m, float ms, bool wide, const FinalArgs& a) {
-#if SV_FINAL_EXACT_EXP
-    (void)ms;
-    (void)wide;
-    float d_hi, d_lo;
-    if constexpr (ELT == 2) {
-        d_hi = z - m;
-        d_lo = 0.f;
-    } else {
-        d_hi = z - m;
+__device__ __forceinline__ float final_exp(float z, float m, const VerifyArgs& a) {
+    float d_hi = z - m, d_lo = 0.f;                       // exact for two bf16 values
+    if constexpr (ELT == 4) {
         const float bb = d_hi - z;
         d_lo = (z - (d_hi - bb)) + (-m - bb);
     }
+#if SV_FINAL_EXACT_EXP
     if (d_hi == kNegInf) return 0.f;
     const float y = d_hi * a.invT;
     const float rem = fmaf(-y, a.T, d_hi) + d_lo;
     const float e = expf(y);
     return fmaf(e, rem * a.invT, e);
 #else
-    // wide (|m * s| beyond 1e30, only for extreme temperatures): subtract
-    // first so no intermediate overflows
-    return ex2_approx(wide ? (z - m) * a.s : fmaf(z, a.s, -ms));
+    const float xh = d_hi * a.s;
+    if (xh == kNegInf) return 0.f;                        // masked logit, or far below the max
+    const float xl = fmaf(d_hi, a.s, -xh) + fmaf(d_hi, a.s_lo, d_lo * a.s);
+    const float c = ex2_approx(xh);
+    return fmaf(c, xl * kLn2, c);
 #endif
 }
+
+// Kahan-compensated running sum (four float operations per term).
+struct KSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const float y = x - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+    }
+    __device__ __forceinline__ FF value() const { return ff_norm(FF{s, -c}); }
+};
 
 constexpr int kPT = kFinalPerThread;
 
@@ -212,133 +149,68 @@ __device__ __forceinline__ FF block_excl_from_incl(FF r, const FF* wtot_scanned)
     return warp > 0 ? wtot_scanned[warp - 1] : FF{0.f, 0.f};
 }
 
-struct DecideSmem {
-    float M[2 * kMaxGamma + 1];       // row max
-    float lnZ[2 * kMaxGamma + 1];     // ln sum exp((z - M)/T)
-    float lp[kMaxGamma], lq[kMaxGamma];
-    int bad, k;
-};
-
-// Row statistics of sequence b from the pass-1 partials and the accept
-// decisions.  Single precision throughout (GB300's double-precision rate is a
-// small fraction of its float rate): ln p_i(x_i) and ln q_i(x_i) carry errors
-// of ~1e-6, far inside the 1e-4 decision margin and the 1e-5 bar on returned
-// probabilities.
-template <int ELT>
-__device__ void sample_decide(const FinalArgs& a, int b, DecideSmem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int P = a.nseg * kWarps;
-    const size_t rowbytes = (size_t)a.V * ELT;
-    if (threadIdx.x == 0) sm.bad = 0;
-    __syncthreads();
-
-    // M = max m_p, Z = sum Z_p 2^((m_p - M) s) over the row's warp partials
-    // (float-float per lane, then across the warp).
-    for (int r = warp; r < a.rows_per_seq; r += nwarps) {
-        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
-        float m = kNegInf;
-        for (int p = lane; p < P; p += 32) m = fmaxf(m, pr[p].x);
-        m = warp_max(m);
-        FF z{0.f, 0.f};
-        if (m != kNegInf) {
-            for (int p = lane; p < P; p += 32) {
-                const float2 q = pr[p];
-                if (q.x != kNegInf) ff_add(z, q.y * ex2_approx((q.x - m) * a.s));
+// The kPT logits of row `row` this thread holds in chunk c, lane-interleaved
+// 16-byte vectors (coalesced): vector h is number tid + kCT h of the chunk.
+// Entries at or beyond V are -inf.
+template <int ELT, bool VEC>
+__device__ __forceinline__ void load_interleaved(const char* row, int V, int c, float (&z)[kPT]) {
+    constexpr int PV = 16 / ELT;
+    const int j00 = c * kFinalChunk;
+    if constexpr (VEC) {
+        uint4 q[kPT / PV];
+#pragma unroll
+        for (int h = 0; h < kPT / PV; ++h) {
+            const int jj = j00 + ((int)threadIdx.x + kCT * h) * PV;
+            q[h] = jj < V ? ld_stream16(row + (size_t)jj * ELT)
+                          : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+        }
+#pragma unroll
+        for (int h = 0; h < kPT / PV; ++h)
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                if constexpr (ELT == 2) {
+                    const uint32_t w = u4_get(q[h], e >> 1);
+                    z[PV * h + e] = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+                } else {
+                    const int jj = j00 + ((int)threadIdx.x + kCT * h) * PV;
+                    z[PV * h + e] = jj < V ? __uint_as_float(u4_get(q[h], e)) : kNegInf;
+                }
             }
-        }
-        z = ff_norm(warp_sum_ff(z));
-        if (lane == 0) {
-            sm.M[r] = m;
-            sm.lnZ[r] = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
-        }
-    }
-    __syncthreads();
-
-    // Validate the drafts, gather z[x_i] and form ln p_i(x_i), ln q_i(x_i).
-    for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
-        const int xi = a.x[(size_t)b * a.gamma + i];
-        if (xi < 0 || xi >= a.V) {
-            atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
-            sm.lp[i] = sm.lq[i] = 0.f;
-        } else {
-            const float ztx = load_logit<ELT>(seq_row(a.zt, a.zd, a.gamma, b, i, rowbytes), xi);
-            const float zdx = load_logit<ELT>(seq_row(a.zt, a.zd, a.gamma, b, a.gamma + 1 + i, rowbytes), xi);
-            sm.lp[i] = (ztx - sm.M[i]) * a.invT - sm.lnZ[i];
-            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) * a.invT - sm.lnZ[a.gamma + 1 + i];
-        }
-    }
-    for (int r = threadIdx.x; r < a.rows_per_seq; r += blockDim.x)
-        if (sm.M[r] == kNegInf) atomicOr(&sm.bad, SPEC_DEVERR_EMPTY_ROW);
-    __syncthreads();
-
-    if (threadIdx.x == 0) {
-        int k = -1;
-        if (!sm.bad) {
-            // Left to right; the first rejection voids the remaining drafts.
-            k = a.gamma;
-            for (int i = 0; i < a.gamma; ++i) {
-                const float lp = sm.lp[i], lq = sm.lq[i];
-                float r;
-                if (lp == kNegInf) r = 0.f;
-                else if (lq == kNegInf) r = CUDART_INF_F;
-                else r = expf(lp - lq);
-                if (!(a.u[(size_t)b * (a.gamma + 1) + i] < r)) { k = i; break; }
+    } else {
+#pragma unroll
+        for (int h = 0; h < kPT / PV; ++h)
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                const int j = j00 + ((int)threadIdx.x + kCT * h) * PV + e;
+                z[PV * h + e] = j < V ? load_logit<ELT>(row, j) : kNegInf;
             }
-        }
-        sm.k = k;
     }
-    __syncthreads();
-}
-
-template <int ELT>
-__global__ void __launch_bounds__(kDecideThreadsS) sample_decide_kernel(const FinalArgs a) {
-    __shared__ DecideSmem dsm;
-    const int b = blockIdx.x, tid = threadIdx.x;
-    pdl_trigger();
-    pdl_wait();                                           // pass-1 partials are visible from here
-    sample_decide<ELT>(a, b, dsm);
-    const int k = dsm.k;
-    if (tid == 0) {
-        a.out_acc[b] = k;
-        if (dsm.bad) atomicOr(a.err, dsm.bad);
-        SampleDesc d;
-        d.k = k;
-        d.mt = k >= 0 ? dsm.M[k] : 0.f;
-        d.md = (k >= 0 && k < a.gamma) ? dsm.M[a.gamma + 1 + k] : 0.f;
-        d.pad = 0;
-        a.desc[b] = d;
-    }
-    // Accepted drafts, padding and log-probabilities; slot k is written by
-    // the search kernel.
-    for (int i = tid; i <= a.gamma; i += blockDim.x)
-        if (k < 0 || i != k)
-            a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
-    if (a.out_lp)
-        for (int i = tid; i < a.gamma; i += blockDim.x) {
-            float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
-            o[0] = k >= 0 ? dsm.lp[i] : CUDART_NAN_F;
-            o[1] = k >= 0 ? dsm.lq[i] : CUDART_NAN_F;
-        }
 }
 
 // The exponentials of this thread's kPT elements of chunk c of the
-// sequence's target row k (ea) and draft row k (eb, rejections only).
-template <int ELT, bool VEC>
-__device__ __forceinline__ void chunk_exps(const FinalArgs& a, int b, const SampleDesc& d, int c,
+// sequence's target row k (ea) and draft row k (eb, rejections only), in the
+// interleaved layout (CONTIG = false) or as one contiguous run (CONTIG = true,
+// index order, for the search).
+template <int ELT, bool VEC, bool CONTIG>
+__device__ __forceinline__ void chunk_exps(const VerifyArgs& a, int b, const SampleDesc& d, int c,
                                            float (&ea)[kPT], float (&eb)[kPT]) {
     const bool rej = d.k < a.gamma;
     const size_t rowbytes = (size_t)a.V * ELT;
-    const int j0 = c * kFinalChunk + threadIdx.x * kPT;
-    const float mts = d.mt * a.s, mds = d.md * a.s;
-    const bool wt = !(fabsf(mts) < 1e30f), wd = !(fabsf(mds) < 1e30f);
+    const char* rt = a.zt + ((size_t)b * (a.gamma + 1) + d.k) * rowbytes;
+    const char* rd = a.zd + ((size_t)b * a.gamma + d.k) * rowbytes;
     float zt[kPT], zd[kPT];
-    load_seg<ELT, VEC>(a.zt + ((size_t)b * (a.gamma + 1) + d.k) * rowbytes, a.V, j0, zt);
-    if (rej) load_seg<ELT, VEC>(a.zd + ((size_t)b * a.gamma + d.k) * rowbytes, a.V, j0, zd);
+    if constexpr (CONTIG) {
+        const int j0 = c * kFinalChunk + threadIdx.x * kPT;
+        load_seg<ELT, VEC>(rt, a.V, j0, zt);
+        if (rej) load_seg<ELT, VEC>(rd, a.V, j0, zd);
+    } else {
+        load_interleaved<ELT, VEC>(rt, a.V, c, zt);
+        if (rej) load_interleaved<ELT, VEC>(rd, a.V, c, zd);
+    }
 #pragma unroll
     for (int e = 0; e < kPT; ++e) {
-        ea[e] = zt[e] == kNegInf ? 0.f : final_exp<ELT>(zt[e], d.mt, mts, wt, a);
-        eb[e] = (rej && zd[e] != kNegInf) ? final_exp<ELT>(zd[e], d.md, mds, wd, a) : 0.f;
+        ea[e] = final_exp<ELT>(zt[e], d.mt, a);
+        eb[e] = rej ? final_exp<ELT>(zd[e], d.md, a) : 0.f;
     }
 }
 
@@ -349,15 +221,15 @@ __device__ __forceinline__ float resid(float ea, float eb, float Rhi, float Rlo)
 }
 
 __device__ __forceinline__ FF sum_seg(const float (&w)[kPT]) {
-    FF acc{0.f, 0.f};
+    KSum acc;
 #pragma unroll
-    for (int e = 0; e < kPT; ++e) ff_add(acc, w[e]);
-    return ff_norm(acc);
+    for (int e = 0; e < kPT; ++e) acc.add(w[e]);
+    return acc.value();
 }
 
 // The ratio Za / Zb of the two row normalisers of sequence b, from the chunk
 // sums (block-wide, identical in every CTA that calls it).
-__device__ __forceinline__ FF normaliser_ratio(const FinalArgs& a, int b, FF* wtot) {
+__device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* wtot) {
     FF za{0.f, 0.f}, zb{0.f, 0.f};
     if ((int)threadIdx.x < a.C) {
         const float4 q = a.zsum[(size_t)b * a.C + threadIdx.x];
@@ -370,16 +242,27 @@ __device__ __forceinline__ FF normaliser_ratio(const FinalArgs& a, int b, FF* wt
     return ff_div(Za, Zb);
 }
 
+// One CTA per sequence: the accept decisions and every output but the final
+// token, and the SampleDesc the chunk kernels read.
+template <int ELT>
+__global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs a) {
+    __shared__ SampleDecideSmem dsm;
+    pdl_trigger();
+    pdl_wait();                                           // the stream's partials are visible
+    decide_sample<ELT>(a, blockIdx.x, threadIdx.x, dsm);
+    write_sample_decision(a, blockIdx.x, threadIdx.x, dsm);
+}
+
 template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_zsum_kernel(const FinalArgs a) {
+__global__ void __launch_bounds__(kCT) sample_zsum_kernel(const VerifyArgs a) {
     __shared__ FF wtot[kCW];
-    const int c = blockIdx.x, b = blockIdx.y;
+    const int b = blockIdx.x, c = blockIdx.y;
     pdl_trigger();
     pdl_wait();
     const SampleDesc d = a.desc[b];
     if (d.k < 0) return;
     float ea[kPT], eb[kPT];
-    chunk_exps<ELT, VEC>(a, b, d, c, ea, eb);
+    chunk_exps<ELT, VEC, false>(a, b, d, c, ea, eb);
     FF Za, Zb;
     block_incl_scan_ff(sum_seg(ea), wtot, &Za);
     block_incl_scan_ff(sum_seg(eb), wtot, &Zb);
@@ -387,16 +270,16 @@ __global__ void __launch_bounds__(kCT) sample_zsum_kernel(const FinalArgs a) {
 }
 
 template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_wsum_kernel(const FinalArgs a) {
+__global__ void __launch_bounds__(kCT) sample_wsum_kernel(const VerifyArgs a) {
     __shared__ FF wtot[kCW];
-    const int c = blockIdx.x, b = blockIdx.y;
+    const int b = blockIdx.x, c = blockIdx.y;
     pdl_trigger();
     pdl_wait();
     const SampleDesc d = a.desc[b];
     if (d.k < 0 || d.k >= a.gamma) return;               // bonus rows use the exponential sums
     const FF R = normaliser_ratio(a, b, wtot);
     float ea[kPT], eb[kPT], w[kPT];
-    chunk_exps<ELT, VEC>(a, b, d, c, ea, eb);
+    chunk_exps<ELT, VEC, false>(a, b, d, c, ea, eb);
 #pragma unroll
     for (int e = 0; e < kPT; ++e) w[e] = resid(ea[e], eb[e], R.hi, R.lo);
     FF W;
@@ -405,7 +288,7 @@ __global__ void __launch_bounds__(kCT) sample_wsum_kernel(const FinalArgs a) {
 }
 
 template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_search_kernel(const FinalArgs a) {
+__global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) {
     __shared__ FF wtot[kCW];
     __shared__ int s_sel, s_last;
     __shared__ FF s_lo;
@@ -457,7 +340,7 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const FinalArgs a) {
     // Inside the chunk: the same weights and the same scan that produced its
     // total, so the thread intervals tile [P, P + T_cs) exactly.
     float ea[kPT], eb[kPT], w[kPT];
-    chunk_exps<ELT, VEC>(a, b, d, cs, ea, eb);
+    chunk_exps<ELT, VEC, true>(a, b, d, cs, ea, eb);
 #pragma unroll
     for (int e = 0; e < kPT; ++e) w[e] = rej ? resid(ea[e], eb[e], R.hi, R.lo) : ea[e];
     const FF ts = sum_seg(w);
@@ -492,26 +375,10 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const FinalArgs a) {
 }
 
 // ---------------------------------------------------------------- launch
-template <int ELT, bool VEC>
-static cudaError_t launch_stats_t(const StatsArgs& sa, const DeviceInfo& di, cudaStream_t st) {
-    static int occ = 0;                                   // blocks per SM, per template instance
-    if (occ == 0) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sample_rowstats_kernel<ELT, VEC>,
-                                                          kThreads, 0) != cudaSuccess || o < 1)
-            o = 1;
-        occ = o;
-    }
-    long long g = (long long)di.sm_count * occ;
-    if (sa.total_chunks < g) g = sa.total_chunks;
-    sample_rowstats_kernel<ELT, VEC><<<(int)g, kThreads, 0, st>>>(sa);
-    return cudaGetLastError();
-}
-
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor drains and waits (griddepcontrol.wait) for its results.
 template <typename K>
-static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const FinalArgs& fa, cudaStream_t st) {
+static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const VerifyArgs& a, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(threads, 1, 1);
@@ -522,18 +389,18 @@ static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const FinalArgs& fa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kfn, fa);
+    return cudaLaunchKernelEx(&cfg, kfn, a);
 }
 
 template <int ELT, bool VEC>
-static cudaError_t launch_final_t(const FinalArgs& fa, cudaStream_t st) {
-    cudaError_t e = launch_pdl(sample_decide_kernel<ELT>, dim3(fa.B), kDecideThreadsS, fa, st);
+static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st) {
+    cudaError_t e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, a, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(fa.C, fa.B), kCT, fa, st);
+    e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(sample_wsum_kernel<ELT, VEC>, dim3(fa.C, fa.B), kCT, fa, st);
+    e = launch_pdl(sample_wsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
     if (e != cudaSuccess) return e;
-    return launch_pdl(sample_search_kernel<ELT, VEC>, dim3(fa.B), kCT, fa, st);
+    return launch_pdl(sample_search_kernel<ELT, VEC>, dim3(a.B), kCT, a, st);
 }
 
 cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
@@ -546,65 +413,40 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     const bool vec = ((size_t)V * elt) % 16 == 0;
     const WsLayout L = ws_layout(B, gamma, V);
     char* w = static_cast<char*>(ws);
-    float2* parts_buf = reinterpret_cast<float2*>(w + L.part_off);
-    const float s = (float)(1.4426950408889634 / (double)T);
+
+    VerifyArgs a = {};
+    a.zt = static_cast<const char*>(zt);
+    a.zd = static_cast<const char*>(zd);
+    a.x = x;
+    a.u = u;
+    a.T = T;
+    a.invT = 1.0f / T;
+    const double sd = 1.4426950408889634 / (double)T;
+    a.s = (float)sd;
+    a.s_lo = (float)(sd - (double)a.s);
+    a.gamma = gamma;
+    a.rows_per_seq = 2 * gamma + 1;
+    a.V = V;
+    a.nseg = nseg(V, elt);
+    a.total_chunks = (long long)B * a.rows_per_seq * a.nseg;
+    a.B = B;
+    a.C = final_chunks(V);
+    a.parts = reinterpret_cast<float2*>(w + L.part_off);
+    a.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
+    a.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
+    a.wsum = reinterpret_cast<float2*>(w + L.wsum_off);
+    a.err = reinterpret_cast<int*>(w + L.err_off);
+    a.out_tok = out_tok;
+    a.out_acc = out_acc;
+    a.out_lp = out_lp;
 
     if (parts & kSampleStats) {
-        StatsArgs sa;
-        sa.zt = static_cast<const char*>(zt);
-        sa.zd = static_cast<const char*>(zd);
-        sa.s = s;
-        sa.gamma = gamma;
-        sa.V = V;
-        sa.nseg = nseg(V, elt);
-        sa.rows_per_seq = 2 * gamma + 1;
-        sa.total_chunks = (long long)B * sa.rows_per_seq * sa.nseg;
-        sa.parts = parts_buf;
-        RingArgs ra;
-        ra.zt = sa.zt;
-        ra.zd = sa.zd;
-        ra.gamma = gamma;
-        ra.rows_per_seq = sa.rows_per_seq;
-        ra.V = V;
-        ra.nseg = sa.nseg;
-        ra.total_chunks = sa.total_chunks;
-        ra.s = s;
-        ra.parts = parts_buf;
-        ra.err = reinterpret_cast<int*>(w + L.err_off);
-        bool used = false;
-        e = elt == 2 ? launch_ring<2, false>(ra, di, st, &used) : launch_ring<4, false>(ra, di, st, &used);
+        e = elt == 2 ? launch_stream<2, kModeSample>(a, di, st) : launch_stream<4, kModeSample>(a, di, st);
         if (e != cudaSuccess) return e;
-        if (!used) {
-            if (elt == 2) e = vec ? launch_stats_t<2, true>(sa, di, st) : launch_stats_t<2, false>(sa, di, st);
-            else e = vec ? launch_stats_t<4, true>(sa, di, st) : launch_stats_t<4, false>(sa, di, st);
-            if (e != cudaSuccess) return e;
-        }
     }
     if (parts & kSampleFinish) {
-        FinalArgs fa;
-        fa.zt = static_cast<const char*>(zt);
-        fa.zd = static_cast<const char*>(zd);
-        fa.x = x;
-        fa.u = u;
-        fa.T = T;
-        fa.invT = 1.0f / T;
-        fa.s = s;
-        fa.B = B;
-        fa.gamma = gamma;
-        fa.V = V;
-        fa.nseg = nseg(V, elt);
-        fa.rows_per_seq = 2 * gamma + 1;
-        fa.C = final_chunks(V);
-        fa.parts = parts_buf;
-        fa.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
-        fa.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
-        fa.wsum = reinterpret_cast<float2*>(w + L.wsum_off);
-        fa.out_tok = out_tok;
-        fa.out_acc = out_acc;
-        fa.out_lp = out_lp;
-        fa.err = reinterpret_cast<int*>(w + L.err_off);
-        if (elt == 2) e = vec ? launch_final_t<2, true>(fa, st) : launch_final_t<2, false>(fa, st);
-        else e = vec ? launch_final_t<4, true>(fa, st) : launch_final_t<4, false>(fa, st);
+        if (elt == 2) e = vec ? launch_final_t<2, true>(a, st) : launch_final_t<2, false>(a, st);
+        else e = vec ? launch_final_t<4, true>(a, st) : launch_final_t<4, false>(a, st);
     }
     return e;
 }

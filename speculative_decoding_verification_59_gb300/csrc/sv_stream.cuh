@@ -1,20 +1,25 @@
-// Persistent streaming kernel over logit rows with a bulk-copy (TMA) ring.
+// The streaming pass over the logit rows of every verification mode: per-warp
+// partials that the decision step (sv_decide.cuh) merges per sequence.
 //
-// Used by the row-statistics pass of stochastic verification and by the
-// argmax pass of greedy / tree verification, for rows whose byte length is a
-// multiple of 16 (so every 32 KB block chunk of a row is a legal bulk copy).
-//
-// Each CTA has one producer warp and kWarps consumer warps.  Lane 0 of the
-// producer walks the CTA's block chunks (row, segment) and issues one
+// ring_stream_kernel (rows whose byte length is a multiple of 16): a
+// persistent CTA has one producer warp and kWarps consumer warps.  Lane 0 of
+// the producer walks the CTA's block chunks (row, segment) and issues one
 // cp.async.bulk per chunk into a ring of kStages shared-memory stages, each
 // guarded by a "full" mbarrier (copy landed) and an "empty" mbarrier (all
 // consumer warps done).  Consumer warp w reduces the w-th 4 KB warp chunk of
-// the stage -- (max m, sum 2^((z - m) s)) for row statistics, (value, lowest
-// index) for argmax -- and writes one partial per warp chunk, at the same
-// workspace position the register-path kernels use.
+// the stage -- (max m, sum 2^((z - m) s)) for sampling, (value, lowest index)
+// for greedy and tree verification -- and writes one partial per warp chunk.
+//
+// reg_stream_kernel (any row alignment): the same partials from register
+// loads, one CTA of kThreads per block chunk in a persistent loop.
+//
+// Each CTA streams one contiguous range of block chunks (measured faster on
+// GB300 than dealing chunks round-robin).  Nothing here waits on another CTA:
+// the decisions run in the next kernel of the stream.
 #pragma once
 
 #include "sv_common.cuh"
+#include "sv_decide.cuh"
 #include "sv_tma.cuh"
 
 namespace sv {
@@ -23,25 +28,14 @@ constexpr int kStages = 3;
 constexpr int kRingThreads = (kWarps + 1) * 32;
 constexpr int kStageBytes = kWarps * 32 * kLaneBytes;     // 32 KB block chunk
 
-struct RingArgs {
-    const char* zt;
-    const char* zd;       // draft rows (row statistics of a sampling batch), else null
-    int gamma;            // >= 0: rows are the 2*gamma+1 rows of each sampling sequence
-    int rows_per_seq;
-    int V;
-    int nseg;
-    long long total_chunks;
-    float s;              // log2(e) / T (row statistics)
-    float2* parts;
-    int* err;
-};
-
-__device__ __forceinline__ const char* ring_row(const RingArgs& a, unsigned rr, size_t rowbytes) {
-    if (a.gamma < 0) return a.zt + (size_t)rr * rowbytes;
-    const unsigned b = rr / (unsigned)a.rows_per_seq;
-    const int r = (int)(rr - b * (unsigned)a.rows_per_seq);
-    return r <= a.gamma ? a.zt + ((size_t)b * (a.gamma + 1) + r) * rowbytes
-                        : a.zd + ((size_t)b * a.gamma + (r - a.gamma - 1)) * rowbytes;
+template <int MODE>
+__device__ __forceinline__ const char* stream_row(const VerifyArgs& a, unsigned rr, size_t rowbytes) {
+    if constexpr (MODE == kModeSample) {
+        const unsigned b = rr / (unsigned)a.rows_per_seq;
+        return sample_row(a, (int)b, (int)(rr - b * (unsigned)a.rows_per_seq), rowbytes);
+    } else {
+        return a.zt + (size_t)rr * rowbytes;
+    }
 }
 
 // The lane's 128 bytes of a warp chunk in shared memory; bytes past
@@ -84,59 +78,42 @@ __device__ __forceinline__ float lane_max(const uint4 (&v)[kVecPerLane]) {
     }
 }
 
-// Row statistics of one warp chunk held in shared memory: the chunk max m and
-// sum_j 2^(z_j s - m s).  m s is rounded once for the whole chunk, a common
-// factor the merge of partials absorbs within ~1e-6.
+// Row statistics of one warp chunk: its max m and sum_j 2^(z_j s - m s).  m s
+// is rounded once for the whole chunk, a common factor the merge of partials
+// absorbs within ~1e-6.
 template <int ELT>
-__device__ __forceinline__ float2 warp_rowstats(const unsigned char* chunk, int valid_bytes, float s) {
-    uint4 v[kVecPerLane];
-    lane_words<ELT>(chunk, valid_bytes, v);
+__device__ __forceinline__ float2 warp_rowstats(const uint4 (&v)[kVecPerLane], float s) {
     const float m = warp_max(lane_max<ELT>(v));
     float z = 0.f;
     if (m != kNegInf) {
         const float ms = m * s;
-        if (fabsf(ms) < 1e30f) {
+        const bool wide = !(fabsf(ms) < 1e30f);            // extreme temperature: no overflow
 #pragma unroll
-            for (int t = 0; t < kVecPerLane; ++t)
+        for (int t = 0; t < kVecPerLane; ++t)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t w = u4_get(v[t], c);
-                    if constexpr (ELT == 2) {
-                        z += ex2_approx(fmaf(bf16_lo(w), s, -ms));
-                        z += ex2_approx(fmaf(bf16_hi(w), s, -ms));
-                    } else {
-                        z += ex2_approx(fmaf(__uint_as_float(w), s, -ms));
-                    }
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t w = u4_get(v[t], c);
+                if constexpr (ELT == 2) {
+                    const float lo = bf16_lo(w), hi = bf16_hi(w);
+                    z += ex2_approx(wide ? (lo - m) * s : fmaf(lo, s, -ms));
+                    z += ex2_approx(wide ? (hi - m) * s : fmaf(hi, s, -ms));
+                } else {
+                    const float x = __uint_as_float(w);
+                    z += ex2_approx(wide ? (x - m) * s : fmaf(x, s, -ms));
                 }
-        } else {                                           // extreme temperature: no overflow
-#pragma unroll
-            for (int t = 0; t < kVecPerLane; ++t)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t w = u4_get(v[t], c);
-                    if constexpr (ELT == 2) {
-                        z += ex2_approx((bf16_lo(w) - m) * s);
-                        z += ex2_approx((bf16_hi(w) - m) * s);
-                    } else {
-                        z += ex2_approx((__uint_as_float(w) - m) * s);
-                    }
-                }
-        }
+            }
         z = warp_sum(z);
     }
     return make_float2(m, z);
 }
 
-// (value, lowest index) of one warp chunk held in shared memory; base is the
-// row index of the chunk's first element.  The warp first agrees on the
+// (value, lowest index) of one warp chunk whose first element is row index
+// base, valid_bytes of it inside the row.  The warp first agrees on the
 // chunk maximum; only lanes holding it search for its first position.
 template <int ELT>
-__device__ __forceinline__ float2 warp_argmax_chunk(const unsigned char* chunk, int valid_bytes,
-                                                    int base) {
+__device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane], int valid_bytes, int base) {
     const int lane = threadIdx.x & 31;
     constexpr int PV = 16 / ELT;
-    uint4 v[kVecPerLane];
-    lane_words<ELT>(chunk, valid_bytes, v);
     const float lm = lane_max<ELT>(v);
     const float m = warp_max(lm);
     int bi = 0x7fffffff;
@@ -161,13 +138,14 @@ __device__ __forceinline__ float2 warp_argmax_chunk(const unsigned char* chunk, 
     return make_float2(m + 0.0f, __int_as_float(bi));
 }
 
-template <int ELT, bool ARGMAX>
-__global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const RingArgs a) {
+template <int ELT, int MODE>
+__global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t rowbytes = (size_t)a.V * ELT;
     const int P = a.nseg * kWarps;
+    const unsigned total = (unsigned)a.total_chunks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -181,10 +159,10 @@ __global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const RingArg
     if (warp == 0) {
         // ---- producer: one lane issues the bulk copies
         if (lane == 0) {
-            const unsigned total = (unsigned)a.total_chunks;
-            unsigned issued = 0;
+            unsigned c0, c1, issued = 0;
+            cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
             bool ok = true;
-            for (unsigned c = blockIdx.x; c < total; c += gridDim.x, ++issued) {
+            for (unsigned c = c0; c < c1; ++c, ++issued) {
                 const int st = (int)(issued % kStages);
                 const unsigned use = issued / kStages;
                 if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) { ok = false; break; }
@@ -192,9 +170,10 @@ __global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const RingArg
                 const int seg = (int)(c - rr * (unsigned)a.nseg);
                 const size_t off = (size_t)seg * kStageBytes;
                 const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
-                if (c + gridDim.x >= total) pdl_trigger();
+                if (c + 1 == c1) pdl_trigger();
                 mbar_arrive_expect_tx(&full[st], bytes);
-                bulk_g2s(ring + (size_t)st * kStageBytes, ring_row(a, rr, rowbytes) + off, bytes, &full[st]);
+                bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, rr, rowbytes) + off, bytes,
+                         &full[st]);
             }
             if (!ok) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
             // Do not leave while a copy may still be writing this CTA's shared memory.
@@ -208,59 +187,128 @@ __global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const RingArg
         return;
     }
 
-    // ---- consumers
+    // ---- consumers.  A timed-out wait flags the error and stops the warp
+    // from touching the ring.
     const int cw = warp - 1;
-    const unsigned total = (unsigned)a.total_chunks;
-    unsigned it = 0;
-    for (unsigned c = blockIdx.x; c < total; c += gridDim.x, ++it) {
+    unsigned c0, c1, it = 0;
+    cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
+    bool ok = true;
+    for (unsigned c = c0; c < c1; ++c, ++it) {
         const int st = (int)(it % kStages);
-        if (!wait_bounded(&full[st], (it / kStages) & 1u)) {
-            if (lane == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
-            return;
-        }
+        if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
         const unsigned rr = c / (unsigned)a.nseg;
         const int seg = (int)(c - rr * (unsigned)a.nseg);
         const size_t off = (size_t)seg * kStageBytes;
         const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
         const int wb = bytes - cw * (32 * kLaneBytes);            // valid bytes of this warp chunk
-        const unsigned char* chunk = ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes);
+        const bool use = __all_sync(0xffffffffu, ok) && wb > 0;
         float2 part;
-        if constexpr (ARGMAX) {
-            part = wb > 0 ? warp_argmax_chunk<ELT>(chunk, wb, (int)(off / ELT) + cw * (32 * kLaneBytes / ELT))
-                          : make_float2(kNegInf, __int_as_float(0x7fffffff));
+        if (use) {
+            uint4 v[kVecPerLane];
+            lane_words<ELT>(ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes), wb, v);
+            if constexpr (MODE == kModeSample) part = warp_rowstats<ELT>(v, a.s);
+            else part = warp_argmax_chunk<ELT>(v, wb, (int)(off / ELT) + cw * (32 * kLaneBytes / ELT));
         } else {
-            part = wb > 0 ? warp_rowstats<ELT>(chunk, wb, a.s) : make_float2(kNegInf, 0.f);
+            part = MODE == kModeSample ? make_float2(kNegInf, 0.f)
+                                       : make_float2(kNegInf, __int_as_float(0x7fffffff));
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&empty[st]);
+            if (ok) mbar_arrive(&empty[st]);
             a.parts[(size_t)rr * P + seg * kWarps + cw] = part;
         }
     }
+    if (!ok && lane == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
 }
 
-// Launches the ring kernel (persistent grid); true when it applies (rows a
-// multiple of 16 bytes), false when the caller must use the register path.
-template <int ELT, bool ARGMAX>
-cudaError_t launch_ring(const RingArgs& a, const DeviceInfo& di, cudaStream_t st, bool* used) {
-    *used = false;
-    if (((size_t)a.V * ELT) % 16 != 0) return cudaSuccess;
-    if (a.total_chunks >= (1ll << 31)) return cudaSuccess;   // 32-bit chunk indices in the ring
-    auto kfn = ring_stream_kernel<ELT, ARGMAX>;
-    const int smem = kStages * kStageBytes;
+template <int ELT, bool VEC, int MODE>
+__global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int WE = 32 * kLaneBytes / ELT;                  // elements per warp chunk
+    const int P = a.nseg * kWarps;
+    const size_t rowbytes = (size_t)a.V * ELT;
+    const unsigned total = (unsigned)a.total_chunks;
+
+    unsigned c0, c1;
+    cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
+    for (unsigned c = c0; c < c1; ++c) {
+        if (c + 1 == c1) pdl_trigger();
+        const unsigned rr = c / (unsigned)a.nseg;
+        const int seg = (int)(c - rr * (unsigned)a.nseg);
+        const char* row = stream_row<MODE>(a, rr, rowbytes);
+        const int base = (seg * kWarps + warp) * WE;
+        float2 part;
+        if constexpr (MODE == kModeSample) {
+            float m = kNegInf, z = 0.f;
+            if (base < a.V) {
+                LaneChunk<ELT, VEC> ch;
+                ch.load(row, a.V, base, lane);
+#pragma unroll
+                for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i) m = fmaxf(m, ch.val(i));
+                m = warp_max(m);
+                if (m != kNegInf) {
+#pragma unroll
+                    for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i)
+                        z += ex2_approx((ch.val(i) - m) * a.s);
+                    z = warp_sum(z);
+                }
+            }
+            part = make_float2(m, z);
+        } else {
+            float bv = kNegInf;
+            int bi = 0x7fffffff;
+            if (base < a.V) {
+                LaneChunk<ELT, VEC> ch;
+                ch.load(row, a.V, base, lane);
+                // lane elements come in increasing index order: strict '>'
+                // keeps the first maximum; +0.0f folds -0.0 into +0.0
+                bv = ch.val(0) + 0.0f;
+                bi = ch.idx(base, lane, 0);
+#pragma unroll
+                for (int i = 1; i < LaneChunk<ELT, VEC>::EPL; ++i) {
+                    const float v = ch.val(i) + 0.0f;
+                    if (v > bv) { bv = v; bi = ch.idx(base, lane, i); }
+                }
+                if (bi >= a.V) bi = 0x7fffffff;            // only padding seen
+                warp_argmax(bv, bi);
+            }
+            part = make_float2(bv, __int_as_float(bi));
+        }
+        if (lane == 0) a.parts[(size_t)rr * P + seg * kWarps + warp] = part;
+    }
+}
+
+// Launches the streaming pass of MODE over the rows of a (persistent grid):
+// the bulk-copy ring for 16-byte rows, the register path otherwise.
+template <int ELT, int MODE>
+cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_t st) {
+    if (((size_t)a.V * ELT) % 16 == 0) {
+        auto kfn = ring_stream_kernel<ELT, MODE>;
+        const int smem = kStages * kStageBytes;
+        static int occ = 0;
+        if (occ == 0) {
+            cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            int o = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kRingThreads, smem) != cudaSuccess || o < 1)
+                o = 1;
+            occ = o;
+        }
+        long long g = (long long)di.sm_count * occ;
+        if (a.total_chunks < g) g = a.total_chunks;
+        kfn<<<(int)g, kRingThreads, smem, st>>>(a);
+        return cudaGetLastError();
+    }
+    auto kfn = reg_stream_kernel<ELT, false, MODE>;
     static int occ = 0;
     if (occ == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kRingThreads, smem) != cudaSuccess || o < 1)
-            o = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kThreads, 0) != cudaSuccess || o < 1) o = 1;
         occ = o;
     }
     long long g = (long long)di.sm_count * occ;
     if (a.total_chunks < g) g = a.total_chunks;
-    kfn<<<(int)g, kRingThreads, smem, st>>>(a);
-    *used = true;
+    kfn<<<(int)g, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
