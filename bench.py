@@ -54,6 +54,28 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def rank_seed(workload_seed, rank):
+    """Each replica verifies its own batch: rank r draws from seed + 1000 r."""
+    return workload_seed + 1000 * rank
+
+
+def max_over_ranks(v, world, device=None):
+    """The largest per-rank value (the slowest replica's time) over the group."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_step, steps, ms_max):
+    """Whole-job throughput: the units all replicas processed over the slowest
+    replica's time (every replica runs the same number of steps)."""
+    return world * units_per_step * steps / (ms_max * 1e-3)
+
+
 def chain_tree(x):
     """The batch's drafts as a chain-shaped draft tree: node 0 is the root,
     node i+1 carries draft x_i and hangs under node i."""
@@ -66,12 +88,12 @@ def chain_tree(x):
 def step_accounting(x):
     elt = 2 if x.dtype == "bf16" else 4
     rows_chain = x.B * (x.gamma + 1)
-    bytes_decide = x.B * (2 * x.gamma + 1) * x.V * elt
+    bytes_stats = x.B * (2 * x.gamma + 1) * x.V * elt
     bytes_greedy = x.B * (x.gamma + 1) * x.V * elt
     return {
         "rows": 3 * rows_chain,
-        "bytes_decide": bytes_decide,
-        "bytes_step": bytes_decide + 2 * bytes_greedy,
+        "bytes_stats": bytes_stats,
+        "bytes_step": bytes_stats + 2 * bytes_greedy,
     }
 
 
@@ -86,7 +108,7 @@ def measured_peaks():
 
 
 def kernel_source_hash():
-    """Hash of the sources that define the decide kernel; ncu traffic figures
+    """Hash of the sources that define the row-statistics stream kernel; ncu traffic figures
     recorded under profiles/ are only reported while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_59_gb300", "csrc")
@@ -97,9 +119,9 @@ def kernel_source_hash():
 
 
 def recorded_traffic(workload):
-    """dram bytes per launch of the decide kernel from the committed ncu
-    summary (profiles/decide_traffic.txt: key=value lines), or None."""
-    p = os.path.join(ROOT, "profiles", "decide_traffic.txt")
+    """dram bytes per launch of the row-statistics stream kernel from the committed ncu
+    summary (profiles/stats_traffic.txt: key=value lines), or None."""
+    p = os.path.join(ROOT, "profiles", "stats_traffic.txt")
     if not os.path.exists(p):
         return None
     kv = {}
@@ -182,7 +204,7 @@ def run_own(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    x = W.make_chain(args.workload, seed=W.WORKLOADS[args.workload].seed + 1000 * rank)
+    x = W.make_chain(args.workload, seed=rank_seed(W.WORKLOADS[args.workload].seed, rank))
     ttok, tpar = chain_tree(x)
     acct = step_accounting(x)
     B, g, V = x.B, x.gamma, x.V
@@ -197,7 +219,8 @@ def run_own(args):
         "tt": torch.from_numpy(ttok).pin_memory(),
         "tp": torch.from_numpy(tpar).pin_memory(),
     }
-    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(ROTATE)]
+    rot = args.rotate
+    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(rot)]
     out = {
         "s_tok": torch.empty((B, g + 1), dtype=torch.int32, device=dev),
         "s_acc": torch.empty((B,), dtype=torch.int32, device=dev),
@@ -218,7 +241,7 @@ def run_own(args):
             raise sv.SpecVerifyError(st, what)
 
     def calls(s, ev=None):
-        c0, c1, c2 = copies[s % ROTATE], copies[(s + 1) % ROTATE], copies[(s + 2) % ROTATE]
+        c0, c1, c2 = copies[s % rot], copies[(s + 1) % rot], copies[(s + 2) % rot]
         if ev is not None:
             ev[0].record(stream)
         check(sv.spec_verify_sample_stats(P(c0["zt"]), P(c0["zd"]), dcode, x.T, B, g, V, wp, wb,
@@ -238,13 +261,6 @@ def run_own(args):
         if world > 1:
             dist.barrier(device_ids=[local])
         torch.cuda.synchronize(dev)
-
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     gpu_id = local
     try:
@@ -273,8 +289,8 @@ def run_own(args):
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     ms = e0.elapsed_time(e1)
-    decide_ms = [a.elapsed_time(b) for a, b in evs]
-    ms_max = max_over_ranks(ms)
+    stats_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_max = max_over_ranks(ms, world, dev)
     barrier()
     clk = clocks.summary(t_wall0, t_wall1)
 
@@ -317,7 +333,7 @@ def run_own(args):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1))
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
@@ -327,10 +343,10 @@ def run_own(args):
 
     if rank == 0:
         peak, peak_src = measured_peaks()
-        decide_mean_ms = statistics.mean(decide_ms)
-        achieved = acct["bytes_decide"] / (decide_mean_ms * 1e-3) / 1e9
+        stats_mean_ms = statistics.mean(stats_ms)
+        achieved = acct["bytes_stats"] / (stats_mean_ms * 1e-3) / 1e9
         traffic = recorded_traffic(args.workload)
-        value = world * acct["rows"] * K / (ms_max * 1e-3)
+        value = job_rate(world, acct["rows"], K, ms_max)
         line = {
             "metric": METRIC,
             "value": value,
@@ -349,12 +365,12 @@ def run_own(args):
                 "B": B, "gamma": g, "V": V, "logits": x.dtype, "temperature": x.T,
                 "step": "sample (stats+finish) + greedy + chain-shaped tree, each on its own "
                         "rotating input copy",
-                "l2": f"{ROTATE} rotating input copies of {acct['bytes_decide'] / 1e6:.1f} MB "
-                      "(> 4x the 129 MB L2): every call reads cold logits",
+                "l2": f"{rot} rotating input copies of {acct['bytes_stats'] / 1e6:.1f} MB "
+                      f"({rot * acct['bytes_stats'] / 129e6:.1f}x the 129 MB L2 in all)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             },
-            "hbm_gbs_step": world * acct["bytes_step"] * K / (ms_max * 1e-3) / 1e9,
-            "rounds_per_s": world * x.B * K / (ms_max * 1e-3),
+            "hbm_gbs_step": job_rate(world, acct["bytes_step"], K, ms_max) / 1e9,
+            "rounds_per_s": job_rate(world, x.B, K, ms_max),
             "tau": {"sample": tau_sample, "greedy": tau_greedy},
             "roofline": {
                 "kernel": "ring_stream_kernel<bf16, sample> (spec_verify_sample_stats)",
@@ -366,11 +382,11 @@ def run_own(args):
                 "frac": achieved / peak,
                 "frac_of_8tbs_nominal": achieved / 8000.0,
                 "traffic": traffic,
-                "algorithmic_bytes_per_launch": acct["bytes_decide"],
-                "launch_ms_mean": decide_mean_ms,
+                "algorithmic_bytes_per_launch": acct["bytes_stats"],
+                "launch_ms_mean": stats_mean_ms,
             },
             "e2e": {
-                "value": world * acct["rows"] * Ke / (e2e_ms * 1e-3),
+                "value": job_rate(world, acct["rows"], Ke, e2e_ms),
                 "unit": UNIT,
                 "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo,
@@ -467,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--rotate", type=int, default=ROTATE,
+                    help="input copies the calls rotate over (1 keeps profiler captures small)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps

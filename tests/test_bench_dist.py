@@ -1,0 +1,75 @@
+"""Multi-replica host logic of bench.py on CPU (gloo, world size 2).
+
+Verification shards by sequence with no exchange, so several GPUs run
+independent replicas: each rank verifies its own seeded batch, the slowest
+rank's time is the job's time, and the job's rate counts every rank's rows.
+These tests run that logic as two gloo ranks without a GPU.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from speculative_decoding_verification_59_gb300 import workloads as W  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # per-rank times: rank 1 is the slow one
+        ms = [12.5, 20.0][rank]
+        ms_max = bench.max_over_ranks(ms, world, "cpu")
+        x = W.make_chain("chain-small", seed=bench.rank_seed(W.WORKLOADS["chain-small"].seed, rank))
+        rows = bench.step_accounting(x)["rows"]
+        rate = bench.job_rate(world, rows, 10, ms_max)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"ms_max": ms_max, "rate": rate, "rows": rows,
+                       "target_sum": float(np.asarray(x.target, dtype=np.float64).sum())}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_share_max_time_and_sum_rows(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    r = [json.load(open(tmp_path / f"rank{i}.json")) for i in range(world)]
+    # both ranks see the slowest rank's time
+    assert r[0]["ms_max"] == r[1]["ms_max"] == 20.0
+    # whole-job rate: both ranks' rows over the slowest time
+    expect = world * r[0]["rows"] * 10 / 20.0e-3
+    assert r[0]["rate"] == pytest.approx(expect) and r[1]["rate"] == pytest.approx(expect)
+    # each replica verified its own batch
+    assert r[0]["target_sum"] != r[1]["target_sum"]
+
+
+def test_single_rank_helpers_need_no_process_group():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.job_rate(1, 1536, 100, 50.0) == pytest.approx(1536 * 100 / 0.05)
+    assert bench.rank_seed(2, 0) == 2 and bench.rank_seed(2, 3) == 3002
+
+
+def test_reference_arm_on_nonzero_rank_exits_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "1"], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert p.returncode == 0
+    assert p.stdout.strip() == ""
