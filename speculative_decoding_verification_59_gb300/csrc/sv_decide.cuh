@@ -24,6 +24,18 @@ constexpr int kMaxNodes = 1024;                  // greedy chains and trees: row
 
 enum : int { kModeSample = 0, kModeGreedy = 1, kModeTree = 2 };
 
+// Row-statistics partials take their exponent arguments as z s - fl(m s)
+// while |fl(m s)| < kFmaArgLimit (2^24: the rounding residual of m s is then
+// at most 1 in magnitude), else as (z - m) s.
+constexpr float kFmaArgLimit = 16777216.f;
+
+// The residual m s - fl(m s) that a partial with maximum m carries in every
+// exponent (0 for partials past the limit).
+__device__ __forceinline__ float partial_residual(float m, float s) {
+    const float ms = m * s;
+    return fabsf(ms) < kFmaArgLimit ? fmaf(m, s, -ms) : 0.f;
+}
+
 struct VerifyArgs {
     const char* zt;            // target logits
     const char* zd;            // draft logits (sampling)
@@ -39,8 +51,8 @@ struct VerifyArgs {
     int C;                     // sampling: final-pass chunks per row
     float2* parts;             // per-warp-chunk partials
     SampleDesc* desc;          // sampling: rejection index and row maxima
-    float4* zsum;              // sampling: [B, C] (Za.hi, Za.lo, Zb.hi, Zb.lo) per chunk
-    float2* wsum;              // sampling: [B, C] residual weight total per chunk
+    float4* zsum;              // sampling: [B, C, 8] (Za.hi, Za.lo, Zb.hi, Zb.lo) per segment
+    float2* wsum;              // sampling: [B, C, 8] residual weight total per segment
     int* err;
     int32_t* out_tok;
     int32_t* out_acc;
@@ -88,8 +100,9 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
     }
     if (gt == 0) sm.bad = 0;
     group_sync();
-    // Row r: M = max m_p, Z = sum Z_p 2^((m_p - M) s) over its warp partials,
-    // each lane holding up to kHeld of them in registers (float-float sum).
+    // Row r: M = max m_p, Z = sum Z_p 2^((m_p - M) s - r_p) over its warp
+    // partials, r_p = partial_residual(m_p), each lane holding up to kHeld of
+    // them in registers (float-float sum).
     constexpr int kHeld = 8;
     for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
         const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
@@ -108,10 +121,12 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
         if (m != kNegInf) {
 #pragma unroll
             for (int h = 0; h < kHeld; ++h)
-                if (q[h].x != kNegInf) ff_add(z, q[h].y * ex2_approx((q[h].x - m) * a.s));
+                if (q[h].x != kNegInf)
+                    ff_add(z, q[h].y * ex2_approx(fmaf(q[h].x - m, a.s, -partial_residual(q[h].x, a.s))));
             for (int p = lane + 32 * kHeld; p < P; p += 32) {
                 const float2 t = __ldcg(&pr[p]);
-                if (t.x != kNegInf) ff_add(z, t.y * ex2_approx((t.x - m) * a.s));
+                if (t.x != kNegInf)
+                    ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
             }
         }
         z = ff_norm(warp_sum_ff(z));
@@ -133,8 +148,8 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
             sm.lp[i] = sm.lq[i] = 0.f;
         } else {
-            sm.lp[i] = (ztx - sm.M[i]) * a.invT - sm.lnZ[i];
-            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) * a.invT - sm.lnZ[a.gamma + 1 + i];
+            sm.lp[i] = (ztx - sm.M[i]) / a.T - sm.lnZ[i];
+            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) / a.T - sm.lnZ[a.gamma + 1 + i];
         }
     }
     for (int r = gt; r < a.rows_per_seq; r += kGroup)

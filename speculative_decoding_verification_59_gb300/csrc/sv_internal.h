@@ -31,6 +31,9 @@ constexpr int kFinalPerThread = 32;
 constexpr int kFinalChunkThreads = 256;
 constexpr int kFinalChunk = kFinalPerThread * kFinalChunkThreads;
 inline int final_chunks(int V) { return (V + kFinalChunk - 1) / kFinalChunk; }
+// Each warp of a final-pass CTA sums one "segment" of kFinalChunk / 8
+// consecutive elements; the workspace keeps one total per segment.
+constexpr int kFinalSegs = kFinalChunkThreads / 32;
 
 // Per-sequence result of the accept decisions, read by the final-sample kernels.
 struct SampleDesc {
@@ -41,7 +44,7 @@ struct SampleDesc {
 };
 
 // Workspace: [error word (256 bytes reserved) | per-warp row partials |
-// SampleDesc[B] | per-chunk normaliser sums | per-chunk residual sums].
+// SampleDesc[B] | per-segment normaliser sums | per-segment residual sums].
 // Every region after the error word is rewritten by the kernels of a call
 // before another kernel of that call reads it, so a workspace carries nothing
 // from one call to the next except the error word, which only accumulates
@@ -61,10 +64,10 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     // fp32 has the smaller warp chunk, hence the most partials per row
     L.part_count = rows * (size_t)nseg(V, 4) * kWarps;
     L.desc_off = L.part_off + align256(sizeof(float2) * L.part_count);
-    const size_t chunks = (size_t)B * (size_t)final_chunks(V);
+    const size_t segs = (size_t)B * (size_t)final_chunks(V) * kFinalSegs;
     L.zsum_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
-    L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * chunks);
-    L.total = L.wsum_off + align256(2 * sizeof(float) * chunks);
+    L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * segs);
+    L.total = L.wsum_off + align256(2 * sizeof(float) * segs);
     return L;
 }
 

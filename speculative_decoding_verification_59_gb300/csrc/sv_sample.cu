@@ -18,107 +18,275 @@
 //   sample_decide_kernel  one CTA per sequence: row statistics from the
 //                         partials, the accept decisions, every output but
 //                         the final token;
-//   sample_zsum_kernel    one CTA per 8192-element chunk of row k: sums of the
-//                         exponentials of the target and draft chunk;
-//   sample_wsum_kernel    one CTA per chunk (rejections only): the ratio of the
-//                         two row normalisers from all chunk sums, then the
-//                         chunk's residual weight total;
-//   sample_search_kernel  one CTA per sequence: prefix over the chunk totals,
-//                         the owning chunk, its weights recomputed and scanned,
-//                         the owning element.
-// The weights are formed from the very exponentials whose sums normalise them,
-// all sums are float-float (about 48 bits), and a chunk's total and the scan
-// that later searches inside it come from the same block-scan code, so the
-// intervals of chunks, threads and elements tile [0, S) exactly.
+//   sample_zsum_kernel    one CTA per 8192-element chunk of row k, one warp
+//                         per 1024-element segment: sums of the exponentials
+//                         of the target and draft segment;
+//   sample_wsum_kernel    the same grid (rejections only): the ratio of the
+//                         two row normalisers from all segment sums, then
+//                         each segment's residual weight total;
+//   sample_search_kernel  one CTA per sequence: prefix over the segment
+//                         totals, the owning segment, its 1024 weights
+//                         recomputed and scanned, the owning element.
+// The weights are formed from the very exponentials whose sums normalise them
+// (the same arithmetic in every kernel), and all sums are float-float (about
+// 48 bits): the CDF each sequence samples from stays within ~1e-9 of the
+// exact one, which matters because the long tail of a 150K-token vocabulary
+// puts CDF boundaries ~1e-7 apart.
 #include "sv_stream.cuh"
 
 namespace sv {
 
-#ifndef SV_FINAL_EXACT_EXP
-#define SV_FINAL_EXACT_EXP 0
-#endif
-
 
 // ---------------------------------------------------------------- pass 2
-constexpr int kCT = kFinalChunkThreads;        // threads per chunk CTA (kFinalPerThread elements each)
-constexpr int kCW = kCT / 32;
+constexpr int kCT = kFinalChunkThreads;        // threads per chunk CTA
+constexpr int kCW = kCT / 32;                  // warps per chunk CTA = segments per chunk
+constexpr int kSeg = kFinalChunk / kCW;        // elements per segment (1024)
+constexpr int kSearchPT = kSeg / kCT;          // elements per thread in the search (4)
+constexpr float kLn2 = 0.6931471805599453f;
 
-// exp((z - m) / T) for the final pass, as 2^x with x = (z - m) log2(e)/T
+// exp((z - m)/T) for the final pass, as 2^x with x = (z - m) log2(e)/T
 // carried in two floats: x_hi into the special-function unit, x_lo through
 // the first-order factor (1 + x_lo ln 2).  Measured against exact values on
 // GB300 the result has a relative error of mean -4.9e-8 and RMS 6.4e-8 over
-// bf16 logits in [-25, 0] -- the mean is a common factor of every weight,
-// which the normalisation cancels, and the rest matches expf's 3.8e-8 RMS at
-// less than half its instruction count.  SV_FINAL_EXACT_EXP=1 selects expf
-// with a two-float argument instead (for accuracy studies).
-constexpr float kLn2 = 0.6931471805599453f;
+// bf16 logits in [-25, 0]; the mean is a common factor of every weight, which
+// the normalisation cancels.  A single rounding of x, which reaches ~100 in
+// magnitude, would cost up to 4e-6 per term.
+//
+// Two versions compute the same quantity.  The fast one works on pairs of
+// logits with packed f32x2 arithmetic; it first raises every logit to a row
+// floor m - 200/T' (T' = 1/s), below which the exponential flushes to zero
+// anyway, so that no argument overflows and masked (-inf) logits need no
+// test.  The guarded scalar one serves rows whose maximum or temperature is
+// too extreme for that floor.
 
+// Row constants of the fast version.
+struct RowExp {
+    f32x2 nm2;         // (-m, -m)
+    f32x2 msh2;        // (ms_hi, ms_hi): m s as float-float (fp32 logits)
+    f32x2 nmsl2;       // (-ms_lo, -ms_lo)
+    float floor;       // logits below this are raised to it
+    uint32_t floor2;   // the floor as a packed bfloat16 pair (rounded down)
+    float m;
+};
+
+// Packed temperature constants.
+struct ExpK {
+    f32x2 s2, ns2, slo2, ln2_2;
+};
+
+__device__ __forceinline__ ExpK exp_consts(const VerifyArgs& a) {
+    return ExpK{f2_pack(a.s, a.s), f2_pack(-a.s, -a.s), f2_pack(a.s_lo, a.s_lo),
+                f2_pack(kLn2, kLn2)};
+}
+
+// Whether a row with maximum m can take the fast version: the floor
+// m - 200/s must be finite and well below m.
+__device__ __forceinline__ bool fast_row(float m, float s) {
+    return fabsf(m) < 1e30f && s > 1e-30f && s < 1e30f && 200.f / s >= fabsf(m) * (1.f / 65536.f);
+}
+
+__device__ __forceinline__ RowExp row_exp(float m, const VerifyArgs& a) {
+    RowExp r;
+    r.m = m;
+    r.nm2 = f2_pack(-m, -m);
+    const float hi = m * a.s;
+    const float lo = fmaf(m, a.s, -hi) + m * a.s_lo;
+    r.msh2 = f2_pack(hi, hi);
+    r.nmsl2 = f2_pack(-lo, -lo);
+    r.floor = m - 200.f / a.s;
+    // bfloat16 rounding toward -inf: truncate positives, round negatives away from zero
+    uint32_t fb = __float_as_uint(r.floor);
+    fb = (fb & 0x80000000u) ? ((fb + 0xffffu) & 0xffff0000u) : (fb & 0xffff0000u);
+    r.floor2 = (fb >> 16) | (fb & 0xffff0000u);
+    return r;
+}
+
+// Fast version for the two bfloat16 logits packed in w.  z - m is exact for
+// bfloat16 values of comparable magnitude, and its product with s splits
+// exactly into x_hi + x_lo through one FMA.
+__device__ __forceinline__ f32x2 exp_pair_bf16(uint32_t w, const RowExp& r, const ExpK& k) {
+    asm("max.bf16x2 %0, %0, %1;" : "+r"(w) : "r"(r.floor2));
+    const f32x2 d = f2_add(f2_pack(bf16_lo(w), bf16_hi(w)), r.nm2);
+    const f32x2 nxh = f2_mul(d, k.ns2);                   // -x_hi
+    const f32x2 xl = f2_fma(d, k.slo2, f2_fma(d, k.s2, nxh));
+    float h0, h1;
+    f2_unpack(nxh, h0, h1);
+    const f32x2 c = f2_pack(ex2_approx(-h0), ex2_approx(-h1));
+    return f2_fma(c, f2_mul(xl, k.ln2_2), c);
+}
+
+// Fast version for two fp32 logits: z s - m s with z s split exactly
+// (TwoProd through an FMA) and m s precomputed as float-float.
+__device__ __forceinline__ f32x2 exp_pair_f32(float z0, float z1, const RowExp& r, const ExpK& k) {
+    const f32x2 z = f2_pack(fmaxf(z0, r.floor), fmaxf(z1, r.floor));
+    const f32x2 np = f2_mul(z, k.ns2);                    // -(z s), rounded
+    const f32x2 pe = f2_fma(z, k.s2, np);                 // z s - p, exact
+    const f32x2 nxh = f2_add(np, r.msh2);                 // -x_hi
+    const f32x2 xl = f2_fma(z, k.slo2, f2_add(pe, r.nmsl2));
+    float h0, h1;
+    f2_unpack(nxh, h0, h1);
+    const f32x2 c = f2_pack(ex2_approx(-h0), ex2_approx(-h1));
+    return f2_fma(c, f2_mul(xl, k.ln2_2), c);
+}
+
+// Guarded scalar version: any finite m and temperature, -inf logits give 0.
 template <int ELT>
-__device__ __forceinline__ float final_exp(float z, float m, const VerifyArgs& a) {
+__device__ __forceinline__ float exp_guarded(float z, float m, const VerifyArgs& a) {
     float d_hi = z - m, d_lo = 0.f;                       // exact for two bf16 values
     if constexpr (ELT == 4) {
         const float bb = d_hi - z;
         d_lo = (z - (d_hi - bb)) + (-m - bb);
     }
-#if SV_FINAL_EXACT_EXP
-    if (d_hi == kNegInf) return 0.f;
-    const float y = d_hi * a.invT;
-    const float rem = fmaf(-y, a.T, d_hi) + d_lo;
-    const float e = expf(y);
-    return fmaf(e, rem * a.invT, e);
-#else
     const float xh = d_hi * a.s;
-    if (xh == kNegInf) return 0.f;                        // masked logit, or far below the max
+    if (!(xh > kNegInf)) return 0.f;                      // masked logit, or far below the max
     const float xl = fmaf(d_hi, a.s, -xh) + fmaf(d_hi, a.s_lo, d_lo * a.s);
     const float c = ex2_approx(xh);
     return fmaf(c, xl * kLn2, c);
-#endif
 }
 
-// Kahan-compensated running sum (four float operations per term).
-struct KSum {
-    float s = 0.f, c = 0.f;
-    __device__ __forceinline__ void add(float x) {
-        const float y = x - c;
-        const float t = s + y;
-        c = (t - s) - y;
+// The exponentials of the first NP pairs of logits in one 16-byte vector,
+// as packed pairs in index order (a vector holds 4 pairs of bfloat16 logits,
+// 2 pairs of fp32 ones).
+template <int ELT, bool FAST, int NP = 8 / ELT>
+__device__ __forceinline__ void vec_exps(const uint4& q, const RowExp& r, const ExpK& k,
+                                         const VerifyArgs& a, f32x2 (&e)[NP]) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        if constexpr (FAST) {
+            if constexpr (ELT == 2) e[i] = exp_pair_bf16(u4_get(q, i), r, k);
+            else e[i] = exp_pair_f32(__uint_as_float(u4_get(q, 2 * i)),
+                                     __uint_as_float(u4_get(q, 2 * i + 1)), r, k);
+        } else {
+            float z0, z1;
+            if constexpr (ELT == 2) {
+                z0 = bf16_lo(u4_get(q, i));
+                z1 = bf16_hi(u4_get(q, i));
+            } else {
+                z0 = __uint_as_float(u4_get(q, 2 * i));
+                z1 = __uint_as_float(u4_get(q, 2 * i + 1));
+            }
+            e[i] = f2_pack(exp_guarded<ELT>(z0, r.m, a), exp_guarded<ELT>(z1, r.m, a));
+        }
+    }
+}
+
+// 16 bytes of logits starting at element j (a multiple of 16/ELT); elements
+// at or past V read as -inf.  VEC: 16-byte aligned rows and V a multiple of
+// 16/ELT, so a vector is either wholly inside the row or wholly outside.
+template <int ELT, bool VEC>
+__device__ __forceinline__ uint4 load_vec(const char* row, int V, int j) {
+    const uint32_t ninf = ELT == 4 ? 0xff800000u : 0xff80ff80u;
+    if constexpr (VEC) {
+        return j < V ? ld_stream16(row + (size_t)j * ELT) : make_uint4(ninf, ninf, ninf, ninf);
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (ELT == 4) {
+                w[i] = j + i < V ? __ldg(reinterpret_cast<const uint32_t*>(row) + j + i) : ninf;
+            } else {
+                const unsigned short* r16 = reinterpret_cast<const unsigned short*>(row);
+                const uint32_t lo = j + 2 * i < V ? __ldg(r16 + j + 2 * i) : 0xff80u;
+                const uint32_t hi = j + 2 * i + 1 < V ? __ldg(r16 + j + 2 * i + 1) : 0xff80u;
+                w[i] = lo | (hi << 16);
+            }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Kahan-compensated running sums of a pair of floats (packed).
+struct KSum2 {
+    f32x2 s = 0ull, c = 0ull;
+    __device__ __forceinline__ void add(f32x2 x) {
+        const f32x2 y = f2_sub(x, c);
+        const f32x2 t = f2_add(s, y);
+        c = f2_sub(f2_sub(t, s), y);
         s = t;
     }
-    __device__ __forceinline__ FF value() const { return ff_norm(FF{s, -c}); }
+    __device__ __forceinline__ FF value() const {
+        float s0, s1, c0, c1;
+        f2_unpack(s, s0, s1);
+        f2_unpack(c, c0, c1);
+        return ff_combine(ff_norm(FF{s0, -c0}), ff_norm(FF{s1, -c1}));
+    }
 };
 
-constexpr int kPT = kFinalPerThread;
+// Residual weights max(0, ea - R eb) of a pair (R = Za / Zb as (Rhi, Rlo)),
+// i.e. max(0, p - q) scaled by Za.
+__device__ __forceinline__ f32x2 resid_pair(f32x2 ea, f32x2 eb, f32x2 nRhi2, f32x2 nRlo2) {
+    float w0, w1;
+    f2_unpack(f2_fma(nRlo2, eb, f2_fma(nRhi2, eb, ea)), w0, w1);
+    return f2_pack(fmaxf(w0, 0.f), fmaxf(w1, 0.f));
+}
 
-// The kPT logits of row `row` at [j0, j0 + kPT); entries at or beyond V are
-// -inf.  All loads are issued before any is used.
-template <int ELT, bool VEC>
-__device__ __forceinline__ void load_seg(const char* row, int V, int j0, float (&z)[kPT]) {
-    if constexpr (VEC) {
-        constexpr int PV = 16 / ELT;                      // V is a multiple of PV
-        uint4 q[kPT / PV];
+// The sequence's final-pass rows: target row k (a) and, after a rejection,
+// draft row k (b).
+struct FinalRows {
+    const char* ra;
+    const char* rb;
+    RowExp xa, xb;
+    bool rej, fast;
+};
+
+template <int ELT>
+__device__ __forceinline__ FinalRows final_rows(const VerifyArgs& a, int b, const SampleDesc& d) {
+    FinalRows f;
+    const size_t rowbytes = (size_t)a.V * ELT;
+    f.rej = d.k < a.gamma;
+    f.ra = a.zt + ((size_t)b * (a.gamma + 1) + d.k) * rowbytes;
+    f.rb = f.rej ? a.zd + ((size_t)b * a.gamma + d.k) * rowbytes : f.ra;
+    f.xa = row_exp(d.mt, a);
+    f.xb = row_exp(f.rej ? d.md : d.mt, a);
+    f.fast = fast_row(d.mt, a.s) && (!f.rej || fast_row(d.md, a.s));
+    return f;
+}
+
+// Segment layout of a chunk CTA: warp w covers the kSeg consecutive elements
+// [c kFinalChunk + w kSeg, + kSeg) -- one "segment" -- with its lanes
+// interleaved over 16-byte vectors (vector h of lane l starts at element
+// (l + 32 h) 16/ELT of the segment), so every load instruction of a warp
+// reads 512 contiguous bytes.  MODE 0: sums of ea and eb; MODE 1: sum of the
+// residual weights.
+template <int ELT, bool VEC, bool FAST, int MODE>
+__device__ __forceinline__ void segment_sums(const VerifyArgs& a, const FinalRows& f, int c,
+                                             FF R, FF* s0, FF* s1) {
+    constexpr int PV = 16 / ELT;
+    constexpr int NV = kSeg / (32 * PV);                  // vectors per lane: 4 (bf16), 8 (fp32)
+    constexpr int NB = FAST ? 4 : 1;                      // vectors per load batch
+    constexpr int NP = 8 / ELT;                           // pairs per vector
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int j0 = c * kFinalChunk + warp * kSeg;
+    const ExpK k = exp_consts(a);
+    const f32x2 nRhi2 = f2_pack(-R.hi, -R.hi), nRlo2 = f2_pack(-R.lo, -R.lo);
+    KSum2 ka, kb;
 #pragma unroll
-        for (int h = 0; h < kPT / PV; ++h) {
-            const int jj = j0 + PV * h;
-            q[h] = jj < V ? ld_stream16(row + (size_t)jj * ELT)
-                          : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    for (int h0 = 0; h0 < NV; h0 += NB) {
+        uint4 qa[NB], qb[NB];
+#pragma unroll
+        for (int h = 0; h < NB; ++h) {
+            const int j = j0 + (lane + 32 * (h0 + h)) * PV;
+            qa[h] = load_vec<ELT, VEC>(f.ra, a.V, j);
+            if (f.rej) qb[h] = load_vec<ELT, VEC>(f.rb, a.V, j);
         }
 #pragma unroll
-        for (int h = 0; h < kPT / PV; ++h)
+        for (int h = 0; h < NB; ++h) {
+            f32x2 ea[NP], eb[NP];
+            vec_exps<ELT, FAST>(qa[h], f.xa, k, a, ea);
+            if (f.rej) vec_exps<ELT, FAST>(qb[h], f.xb, k, a, eb);
 #pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                if constexpr (ELT == 2) {
-                    const uint32_t w = u4_get(q[h], e >> 1);
-                    z[PV * h + e] = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+            for (int i = 0; i < NP; ++i) {
+                if constexpr (MODE == 0) {
+                    ka.add(ea[i]);
+                    if (f.rej) kb.add(eb[i]);
                 } else {
-                    const uint32_t w = u4_get(q[h], e);
-                    // -inf padding for fp32 vectors past V
-                    z[PV * h + e] = (j0 + PV * h < V) ? __uint_as_float(w) : kNegInf;
+                    ka.add(resid_pair(ea[i], eb[i], nRhi2, nRlo2));
                 }
             }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kPT; ++e) z[e] = (j0 + e < V) ? load_logit<ELT>(row, j0 + e) : kNegInf;
+        }
     }
+    *s0 = warp_sum_ff(ka.value());
+    if (MODE == 0) *s1 = f.rej ? warp_sum_ff(kb.value()) : FF{0.f, 0.f};
 }
 
 // Inclusive scan of one float-float value per thread over a kCT-thread block
@@ -149,92 +317,16 @@ __device__ __forceinline__ FF block_excl_from_incl(FF r, const FF* wtot_scanned)
     return warp > 0 ? wtot_scanned[warp - 1] : FF{0.f, 0.f};
 }
 
-// The kPT logits of row `row` this thread holds in chunk c, lane-interleaved
-// 16-byte vectors (coalesced): vector h is number tid + kCT h of the chunk.
-// Entries at or beyond V are -inf.
-template <int ELT, bool VEC>
-__device__ __forceinline__ void load_interleaved(const char* row, int V, int c, float (&z)[kPT]) {
-    constexpr int PV = 16 / ELT;
-    const int j00 = c * kFinalChunk;
-    if constexpr (VEC) {
-        uint4 q[kPT / PV];
-#pragma unroll
-        for (int h = 0; h < kPT / PV; ++h) {
-            const int jj = j00 + ((int)threadIdx.x + kCT * h) * PV;
-            q[h] = jj < V ? ld_stream16(row + (size_t)jj * ELT)
-                          : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-        }
-#pragma unroll
-        for (int h = 0; h < kPT / PV; ++h)
-#pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                if constexpr (ELT == 2) {
-                    const uint32_t w = u4_get(q[h], e >> 1);
-                    z[PV * h + e] = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-                } else {
-                    const int jj = j00 + ((int)threadIdx.x + kCT * h) * PV;
-                    z[PV * h + e] = jj < V ? __uint_as_float(u4_get(q[h], e)) : kNegInf;
-                }
-            }
-    } else {
-#pragma unroll
-        for (int h = 0; h < kPT / PV; ++h)
-#pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                const int j = j00 + ((int)threadIdx.x + kCT * h) * PV + e;
-                z[PV * h + e] = j < V ? load_logit<ELT>(row, j) : kNegInf;
-            }
-    }
-}
-
-// The exponentials of this thread's kPT elements of chunk c of the
-// sequence's target row k (ea) and draft row k (eb, rejections only), in the
-// interleaved layout (CONTIG = false) or as one contiguous run (CONTIG = true,
-// index order, for the search).
-template <int ELT, bool VEC, bool CONTIG>
-__device__ __forceinline__ void chunk_exps(const VerifyArgs& a, int b, const SampleDesc& d, int c,
-                                           float (&ea)[kPT], float (&eb)[kPT]) {
-    const bool rej = d.k < a.gamma;
-    const size_t rowbytes = (size_t)a.V * ELT;
-    const char* rt = a.zt + ((size_t)b * (a.gamma + 1) + d.k) * rowbytes;
-    const char* rd = a.zd + ((size_t)b * a.gamma + d.k) * rowbytes;
-    float zt[kPT], zd[kPT];
-    if constexpr (CONTIG) {
-        const int j0 = c * kFinalChunk + threadIdx.x * kPT;
-        load_seg<ELT, VEC>(rt, a.V, j0, zt);
-        if (rej) load_seg<ELT, VEC>(rd, a.V, j0, zd);
-    } else {
-        load_interleaved<ELT, VEC>(rt, a.V, c, zt);
-        if (rej) load_interleaved<ELT, VEC>(rd, a.V, c, zd);
-    }
-#pragma unroll
-    for (int e = 0; e < kPT; ++e) {
-        ea[e] = final_exp<ELT>(zt[e], d.mt, a);
-        eb[e] = rej ? final_exp<ELT>(zd[e], d.md, a) : 0.f;
-    }
-}
-
-// Residual weight max(0, p_k - q_k) scaled by Za: ea - (Za/Zb) eb, with the
-// ratio as a float-float pair (Rhi, Rlo).
-__device__ __forceinline__ float resid(float ea, float eb, float Rhi, float Rlo) {
-    return fmaxf(fmaf(-Rlo, eb, fmaf(-Rhi, eb, ea)), 0.f);
-}
-
-__device__ __forceinline__ FF sum_seg(const float (&w)[kPT]) {
-    KSum acc;
-#pragma unroll
-    for (int e = 0; e < kPT; ++e) acc.add(w[e]);
-    return acc.value();
-}
-
-// The ratio Za / Zb of the two row normalisers of sequence b, from the chunk
-// sums (block-wide, identical in every CTA that calls it).
+// The ratio Za / Zb of the two row normalisers of sequence b, from the
+// segment sums (block-wide, identical in every CTA that calls it).
 __device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* wtot) {
+    const int ns = a.C * kCW;
+    const float4* zs = a.zsum + (size_t)b * ns;
     FF za{0.f, 0.f}, zb{0.f, 0.f};
-    if ((int)threadIdx.x < a.C) {
-        const float4 q = a.zsum[(size_t)b * a.C + threadIdx.x];
-        za = FF{q.x, q.y};
-        zb = FF{q.z, q.w};
+    for (int s = threadIdx.x; s < ns; s += kCT) {
+        const float4 q = zs[s];
+        za = ff_combine(za, FF{q.x, q.y});
+        zb = ff_combine(zb, FF{q.z, q.w});
     }
     FF Za, Zb;
     block_incl_scan_ff(za, wtot, &Za);
@@ -253,22 +345,25 @@ __global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs 
     write_sample_decision(a, blockIdx.x, threadIdx.x, dsm);
 }
 
+// Per (sequence, chunk): the sums of the exponentials of target row k and
+// (after a rejection) draft row k over each of the chunk's segments.
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT) sample_zsum_kernel(const VerifyArgs a) {
-    __shared__ FF wtot[kCW];
     const int b = blockIdx.x, c = blockIdx.y;
     pdl_trigger();
     pdl_wait();
     const SampleDesc d = a.desc[b];
     if (d.k < 0) return;
-    float ea[kPT], eb[kPT];
-    chunk_exps<ELT, VEC, false>(a, b, d, c, ea, eb);
-    FF Za, Zb;
-    block_incl_scan_ff(sum_seg(ea), wtot, &Za);
-    block_incl_scan_ff(sum_seg(eb), wtot, &Zb);
-    if (threadIdx.x == 0) a.zsum[(size_t)b * a.C + c] = make_float4(Za.hi, Za.lo, Zb.hi, Zb.lo);
+    const FinalRows f = final_rows<ELT>(a, b, d);
+    FF za, zb;
+    if (f.fast) segment_sums<ELT, VEC, true, 0>(a, f, c, FF{0.f, 0.f}, &za, &zb);
+    else segment_sums<ELT, VEC, false, 0>(a, f, c, FF{0.f, 0.f}, &za, &zb);
+    if ((threadIdx.x & 31) == 0)
+        a.zsum[((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5)] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
 }
 
+// Per (sequence, chunk), rejections only: the residual weight totals of the
+// chunk's segments.
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT) sample_wsum_kernel(const VerifyArgs a) {
     __shared__ FF wtot[kCW];
@@ -278,19 +373,60 @@ __global__ void __launch_bounds__(kCT) sample_wsum_kernel(const VerifyArgs a) {
     const SampleDesc d = a.desc[b];
     if (d.k < 0 || d.k >= a.gamma) return;               // bonus rows use the exponential sums
     const FF R = normaliser_ratio(a, b, wtot);
-    float ea[kPT], eb[kPT], w[kPT];
-    chunk_exps<ELT, VEC, false>(a, b, d, c, ea, eb);
-#pragma unroll
-    for (int e = 0; e < kPT; ++e) w[e] = resid(ea[e], eb[e], R.hi, R.lo);
-    FF W;
-    block_incl_scan_ff(sum_seg(w), wtot, &W);
-    if (threadIdx.x == 0) a.wsum[(size_t)b * a.C + c] = make_float2(W.hi, W.lo);
+    const FinalRows f = final_rows<ELT>(a, b, d);
+    FF w, unused;
+    if (f.fast) segment_sums<ELT, VEC, true, 1>(a, f, c, R, &w, &unused);
+    else segment_sums<ELT, VEC, false, 1>(a, f, c, R, &w, &unused);
+    if ((threadIdx.x & 31) == 0)
+        a.wsum[((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5)] = make_float2(w.hi, w.lo);
 }
 
+// The weights of the kSearchPT consecutive elements this thread holds in
+// segment sg: j = sg kSeg + kSearchPT tid + e.
+template <int ELT, bool VEC, bool FAST>
+__device__ __forceinline__ void search_weights(const VerifyArgs& a, const FinalRows& f, int sg,
+                                               FF R, bool rej, float (&w)[kSearchPT]) {
+    static_assert(kSearchPT == 4, "one 8- or 16-byte load per row and thread");
+    const int j = sg * kSeg + kSearchPT * (int)threadIdx.x;
+    uint4 qa, qb;
+    if constexpr (ELT == 4) {
+        qa = load_vec<4, VEC>(f.ra, a.V, j);
+        if (rej) qb = load_vec<4, VEC>(f.rb, a.V, j);
+    } else {
+        // four bfloat16 values: the low half of a 16-byte vector
+        auto ld8 = [&](const char* row) -> uint4 {
+            if constexpr (VEC) {
+                if (j >= a.V) return make_uint4(0xff80ff80u, 0xff80ff80u, 0u, 0u);
+                uint2 v;
+                asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                    : "=r"(v.x), "=r"(v.y) : "l"(row + (size_t)j * 2));
+                return make_uint4(v.x, v.y, 0u, 0u);
+            } else {
+                return load_vec<2, false>(row, a.V, j);   // elements past j + 3 are unused
+            }
+        };
+        qa = ld8(f.ra);
+        if (rej) qb = ld8(f.rb);
+    }
+    const ExpK k = exp_consts(a);
+    const f32x2 nRhi2 = f2_pack(-R.hi, -R.hi), nRlo2 = f2_pack(-R.lo, -R.lo);
+    f32x2 ea[2], eb[2];
+    vec_exps<ELT, FAST, 2>(qa, f.xa, k, a, ea);
+    if (rej) vec_exps<ELT, FAST, 2>(qb, f.xb, k, a, eb);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const f32x2 p = rej ? resid_pair(ea[i], eb[i], nRhi2, nRlo2) : ea[i];
+        f2_unpack(p, w[2 * i], w[2 * i + 1]);
+    }
+}
+
+// One CTA per sequence: the owning segment from the segment totals, then the
+// owning element from that segment's weights, recomputed with the same
+// arithmetic that produced its total.
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) {
     __shared__ FF wtot[kCW];
-    __shared__ int s_sel, s_last;
+    __shared__ int s_sel, s_last, s_seg;
     __shared__ FF s_lo;
     const int b = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
@@ -298,19 +434,25 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     if (d.k < 0) return;
     bool rej = d.k < a.gamma;
     const FF R = rej ? normaliser_ratio(a, b, wtot) : FF{0.f, 0.f};
+    const int ns = a.C * kCW;                             // segments in the row
+    const int G = (ns + kCT - 1) / kCT;                   // consecutive segments per thread
+    auto seg_total = [&](int s) -> FF {
+        if (rej) {
+            const float2 q = a.wsum[(size_t)b * ns + s];
+            return FF{q.x, q.y};
+        }
+        const float4 q = a.zsum[(size_t)b * ns + s];
+        return FF{q.x, q.y};
+    };
 
-    // Chunk totals and their prefix; fall back to p_k if the residual is empty.
+    // Thread totals over its segments and their prefix; fall back to p_k if
+    // the residual is empty.
     FF T{0.f, 0.f}, S{0.f, 0.f}, incl{0.f, 0.f};
     for (int attempt = 0; attempt < 2; ++attempt) {
         T = FF{0.f, 0.f};
-        if (tid < a.C) {
-            if (rej) {
-                const float2 q = a.wsum[(size_t)b * a.C + tid];
-                T = FF{q.x, q.y};
-            } else {
-                const float4 q = a.zsum[(size_t)b * a.C + tid];
-                T = FF{q.x, q.y};
-            }
+        for (int g = 0; g < G; ++g) {
+            const int s = tid * G + g;
+            if (s < ns) T = ff_combine(T, seg_total(s));
         }
         incl = block_incl_scan_ff(T, wtot, &S);
         if (S.hi > 0.f || !rej) break;
@@ -322,28 +464,49 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     if (!ff_lt(target, S))                                // u >= 1 clamps to the last token with mass
         target = ff_norm(FF{S.hi, S.lo - fabsf(S.hi) * 1.4210855e-14f});
 
-    // The owning chunk: the one whose interval [excl, incl) holds the target.
-    // The intervals tile [0, S) exactly, so there is one; the last chunk with
-    // mass stands in should rounding ever leave a gap.
+    // The owning thread: the one whose interval [excl, incl) holds the target
+    // (the intervals tile [0, S) exactly; the last thread with mass stands in
+    // should rounding ever leave a gap), then its owning segment.
     if (tid == 0) { s_sel = -1; s_last = -1; }
     __syncthreads();
-    bool has = tid < a.C && T.hi > 0.f;
-    if (has && !ff_lt(target, excl) && ff_lt(target, incl)) { s_sel = tid; s_lo = excl; }
+    bool has = T.hi > 0.f;
+    if (has && !ff_lt(target, excl) && ff_lt(target, incl)) s_sel = tid;
     if (has) atomicMax(&s_last, tid);
     __syncthreads();
-    if (s_sel < 0 && tid == s_last) { s_sel = tid; s_lo = excl; }
+    if (tid == (s_sel >= 0 ? s_sel : s_last)) {
+        FF run = excl;
+        int pick = -1, last = -1;
+        FF plo = excl, llo = excl;
+        for (int g = 0; g < G; ++g) {
+            const int s = tid * G + g;
+            if (s >= ns) break;
+            const FF t = seg_total(s);
+            const FF nxt = ff_combine(run, t);
+            if (t.hi > 0.f) {
+                last = s;
+                llo = run;
+                if (pick < 0 && ff_lt(target, nxt)) { pick = s; plo = run; }
+            }
+            run = nxt;
+        }
+        if (pick < 0) { pick = last; plo = llo; }
+        s_seg = pick;
+        s_lo = plo;
+    }
     __syncthreads();
-    const int cs = s_sel;
+    const int sg = s_seg;
     const FF P = s_lo;
     __syncthreads();
 
-    // Inside the chunk: the same weights and the same scan that produced its
-    // total, so the thread intervals tile [P, P + T_cs) exactly.
-    float ea[kPT], eb[kPT], w[kPT];
-    chunk_exps<ELT, VEC, true>(a, b, d, cs, ea, eb);
+    // Inside the segment: kSearchPT consecutive elements per thread.
+    const FinalRows f = final_rows<ELT>(a, b, d);
+    float w[kSearchPT];
+    if (f.fast) search_weights<ELT, VEC, true>(a, f, sg, R, rej, w);
+    else search_weights<ELT, VEC, false>(a, f, sg, R, rej, w);
+    FF ts{0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < kPT; ++e) w[e] = rej ? resid(ea[e], eb[e], R.hi, R.lo) : ea[e];
-    const FF ts = sum_seg(w);
+    for (int e = 0; e < kSearchPT; ++e) ff_add(ts, w[e]);
+    ts = ff_norm(ts);
     FF tot;
     const FF ti = block_incl_scan_ff(ts, wtot, &tot);
     const FF te = block_excl_from_incl(ti, wtot);
@@ -361,7 +524,7 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
         FF run{0.f, 0.f};
         int pick = -1, last = -1;
 #pragma unroll
-        for (int e = 0; e < kPT; ++e) {
+        for (int e = 0; e < kSearchPT; ++e) {
             ff_add(run, w[e]);
             if (w[e] > 0.f) {
                 last = e;
@@ -370,7 +533,7 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
         }
         if (pick < 0) pick = last;
         if (pick >= 0)
-            a.out_tok[(size_t)b * (a.gamma + 1) + d.k] = cs * kFinalChunk + tid * kPT + pick;
+            a.out_tok[(size_t)b * (a.gamma + 1) + d.k] = sg * kSeg + tid * kSearchPT + pick;
     }
 }
 

@@ -78,68 +78,134 @@ __device__ __forceinline__ float lane_max(const uint4 (&v)[kVecPerLane]) {
     }
 }
 
-// Row statistics of one warp chunk: its max m and sum_j 2^(z_j s - m s).  m s
-// is rounded once for the whole chunk, a common factor the merge of partials
-// absorbs within ~1e-6.
+// Row statistics of one warp chunk: its max m and sum_j 2^((z_j - m) s).
+// While |m s| < kFmaArgLimit each argument is one FMA, z_j s - fl(m s): the
+// whole chunk then carries the common factor 2^(m s - fl(m s)), which the
+// merge of partials (sv_decide.cuh) divides out exactly.  Beyond that limit
+// (tiny temperatures) the arguments are (z_j - m) s.  The arguments and the
+// running sums go through packed f32x2 FMAs and adds, two logits per
+// instruction.
 template <int ELT>
 __device__ __forceinline__ float2 warp_rowstats(const uint4 (&v)[kVecPerLane], float s) {
     const float m = warp_max(lane_max<ELT>(v));
-    float z = 0.f;
-    if (m != kNegInf) {
-        const float ms = m * s;
-        const bool wide = !(fabsf(ms) < 1e30f);            // extreme temperature: no overflow
+    if (m == kNegInf) return make_float2(m, 0.f);          // warp-uniform
+    const float ms = m * s;
+    float z;
+    if (fabsf(ms) < kFmaArgLimit) {
+        const f32x2 s2 = f2_pack(s, s), nms2 = f2_pack(-ms, -ms);
+        f32x2 acc = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < kVecPerLane; ++t)
+#pragma unroll
+            for (int c = 0; c < 4; c += (ELT == 2 ? 1 : 2)) {
+                f32x2 x;
+                if constexpr (ELT == 2) {
+                    const uint32_t w = u4_get(v[t], c);
+                    x = f2_pack(bf16_lo(w), bf16_hi(w));
+                } else {
+                    x = f2_pack(__uint_as_float(u4_get(v[t], c)), __uint_as_float(u4_get(v[t], c + 1)));
+                }
+                float a, b;
+                f2_unpack(f2_fma(x, s2, nms2), a, b);
+                acc = f2_add(acc, f2_pack(ex2_approx(a), ex2_approx(b)));
+            }
+        float a, b;
+        f2_unpack(acc, a, b);
+        z = a + b;
+    } else {                                               // tiny temperature
+        z = 0.f;
 #pragma unroll
         for (int t = 0; t < kVecPerLane; ++t)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t w = u4_get(v[t], c);
                 if constexpr (ELT == 2) {
-                    const float lo = bf16_lo(w), hi = bf16_hi(w);
-                    z += ex2_approx(wide ? (lo - m) * s : fmaf(lo, s, -ms));
-                    z += ex2_approx(wide ? (hi - m) * s : fmaf(hi, s, -ms));
+                    z += ex2_approx((bf16_lo(w) - m) * s);
+                    z += ex2_approx((bf16_hi(w) - m) * s);
                 } else {
-                    const float x = __uint_as_float(w);
-                    z += ex2_approx(wide ? (x - m) * s : fmaf(x, s, -ms));
+                    z += ex2_approx((__uint_as_float(w) - m) * s);
                 }
             }
-        z = warp_sum(z);
     }
-    return make_float2(m, z);
+    return make_float2(m, warp_sum(z));
+}
+
+// Largest logit of one 16-byte vector, as a packed bf16x2 pair (bfloat16) or
+// a float (fp32).
+template <int ELT>
+__device__ __forceinline__ uint32_t vec_max_bits(const uint4& q) {
+    if constexpr (ELT == 2) {
+        uint32_t a = q.x, b = q.z;
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(q.y));
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(b) : "r"(q.w));
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(b));
+        return a;
+    } else {
+        return __float_as_uint(fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w))));
+    }
+}
+
+template <int ELT>
+__device__ __forceinline__ float vec_max_value(uint32_t bits) {
+    if constexpr (ELT == 2) return fmaxf(bf16_lo(bits), bf16_hi(bits));
+    else return __uint_as_float(bits);
+}
+
+// Position (0..16/ELT-1) of the first element of a vector equal to m, or
+// 16/ELT when there is none.  Float compares: -0.0 == +0.0.
+template <int ELT>
+__device__ __forceinline__ int vec_first_eq(const uint4& q, float m) {
+    constexpr int PV = 16 / ELT;
+    int e = PV;
+#pragma unroll
+    for (int i = PV - 1; i >= 0; --i) {
+        float x;
+        if constexpr (ELT == 4) {
+            x = __uint_as_float(u4_get(q, i));
+        } else {
+            const uint32_t w = u4_get(q, i >> 1);
+            x = (i & 1) ? bf16_hi(w) : bf16_lo(w);
+        }
+        if (x == m) e = i;
+    }
+    return e;
 }
 
 // (value, lowest index) of one warp chunk whose first element is row index
-// base, valid_bytes of it inside the row.  The warp first agrees on the
-// chunk maximum; only lanes holding it search for its first position.
+// base; padding past the row reads as -inf and follows every valid element
+// in index order.  The lane's elements are in vectors t = 0..7 at positions
+// base + (lane + 32 t) * PV, so index order is vector t first, then lane,
+// then position in the vector: after the warp agrees on the maximum m, the
+// first vector t holding m (one ballot per vector) and the lowest lane with it
+// locate the first occurrence, and that lane's vector is searched alone.
 template <int ELT>
-__device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane], int valid_bytes, int base) {
+__device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane], int base) {
     const int lane = threadIdx.x & 31;
     constexpr int PV = 16 / ELT;
-    const float lm = lane_max<ELT>(v);
+    float vm[kVecPerLane];
+    float lm = kNegInf;
+#pragma unroll
+    for (int t = 0; t < kVecPerLane; ++t) {
+        vm[t] = vec_max_value<ELT>(vec_max_bits<ELT>(v[t]));
+        lm = fmaxf(lm, vm[t]);
+    }
     const float m = warp_max(lm);
     int bi = 0x7fffffff;
-    if (lm == m) {                                         // float compare: -0.0 == +0.0
-        for (int t = 0; t < kVecPerLane && bi == 0x7fffffff; ++t) {
-            if ((lane + 32 * t) * 16 >= valid_bytes) break;
 #pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                float x;
-                if constexpr (ELT == 4) {
-                    x = __uint_as_float(u4_get(v[t], e));
-                } else {
-                    const uint32_t w = u4_get(v[t], e >> 1);
-                    x = (e & 1) ? bf16_hi(w) : bf16_lo(w);
-                }
-                if (x == m && bi == 0x7fffffff) bi = base + (lane + 32 * t) * PV + e;
-            }
+    for (int t = 0; t < kVecPerLane; ++t) {
+        const unsigned hit = __ballot_sync(0xffffffffu, vm[t] == m);
+        if (hit && bi == 0x7fffffff) {                       // warp-uniform
+            const int src = __ffs(hit) - 1;
+            const int e = __shfl_sync(0xffffffffu, vec_first_eq<ELT>(v[t], m), src);
+            bi = base + (src + 32 * t) * PV + e;
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bi = min(bi, __shfl_xor_sync(0xffffffffu, bi, o));
     return make_float2(m + 0.0f, __int_as_float(bi));
 }
 
 template <int ELT, int MODE>
-__global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -205,9 +271,16 @@ __global__ void __launch_bounds__(kRingThreads) ring_stream_kernel(const VerifyA
         float2 part;
         if (use) {
             uint4 v[kVecPerLane];
-            lane_words<ELT>(ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes), wb, v);
+            const unsigned char* chunk = ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes);
+            if (wb >= 32 * kLaneBytes) {
+#pragma unroll
+                for (int t = 0; t < kVecPerLane; ++t)
+                    v[t] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * t) * 16);
+            } else {
+                lane_words<ELT>(chunk, wb, v);
+            }
             if constexpr (MODE == kModeSample) part = warp_rowstats<ELT>(v, a.s);
-            else part = warp_argmax_chunk<ELT>(v, wb, (int)(off / ELT) + cw * (32 * kLaneBytes / ELT));
+            else part = warp_argmax_chunk<ELT>(v, (int)(off / ELT) + cw * (32 * kLaneBytes / ELT));
         } else {
             part = MODE == kModeSample ? make_float2(kNegInf, 0.f)
                                        : make_float2(kNegInf, __int_as_float(0x7fffffff));
@@ -247,9 +320,14 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
                 for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i) m = fmaxf(m, ch.val(i));
                 m = warp_max(m);
                 if (m != kNegInf) {
+                    // the same arguments as warp_rowstats
+                    const float ms = m * a.s;
+                    const bool fmapath = fabsf(ms) < kFmaArgLimit;
 #pragma unroll
-                    for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i)
-                        z += ex2_approx((ch.val(i) - m) * a.s);
+                    for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i) {
+                        const float x = ch.val(i);
+                        z += ex2_approx(fmapath ? fmaf(x, a.s, -ms) : (x - m) * a.s);
+                    }
                     z = warp_sum(z);
                 }
             }

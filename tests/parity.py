@@ -16,10 +16,12 @@ LOGPROB_RTOL = 1e-5
 
 
 def compare_sample(gpu_tok, gpu_acc, ref, x, u, gpu_lp=None, check_lp=True):
-    """Returns dict(failures=[...], excused=int, exact=int, rows=int)."""
+    """Returns dict(failures=[...], excused=int, exact=int, rows=int, events=[...]);
+    events lists each excused difference as (kind, sequence, position, margin)."""
     B, g1 = gpu_tok.shape
     g = g1 - 1
     fails, excused, exact = [], 0, 0
+    events = []
     for b in range(B):
         ko, kg = int(ref["accepted"][b]), int(gpu_acc[b])
         if ko < 0 or kg < 0:
@@ -36,6 +38,7 @@ def compare_sample(gpu_tok, gpu_acc, ref, x, u, gpu_lp=None, check_lp=True):
             m = abs(float(u[b, i]) - float(ref["ratio"][b, i]))
             if m < MARGIN:
                 excused += 1
+                events.append(("accept", b, i, m))
             else:
                 fails.append((b, "accept decision", i, float(u[b, i]), float(ref["ratio"][b, i])))
             continue
@@ -50,6 +53,7 @@ def compare_sample(gpu_tok, gpu_acc, ref, x, u, gpu_lp=None, check_lp=True):
         dist = max(0.0, lo - uu, uu - hi)
         if dist < MARGIN:
             excused += 1
+            events.append(("final", b, ko, dist))
         else:
             fails.append((b, "final token", to, tg, uu, lo, hi))
     if gpu_lp is not None and check_lp:
@@ -63,7 +67,8 @@ def compare_sample(gpu_tok, gpu_acc, ref, x, u, gpu_lp=None, check_lp=True):
             bad = (~tiny) & (rel > LOGPROB_RTOL)
             if bad.any():
                 fails.append((int(b), "logprob", float(rel[bad].max())))
-    return {"failures": fails, "excused": excused, "exact": exact, "rows": B * g1}
+    return {"failures": fails, "excused": excused, "exact": exact, "rows": B * g1,
+            "events": events}
 
 
 def compare_exact(name, got, want):

@@ -140,6 +140,25 @@ def test_sample_small(sv, name, B, gamma, V):
     check_sample(sv, W.make_chain(name, B=B, gamma=gamma, V=V))
 
 
+@pytest.mark.parametrize("name,T", [
+    ("chain-b8", 1e-3),     # sharp: most rows put almost all mass on one token
+    ("chain-b8", 1e-12),    # extreme: the row-floor fast path is off, guarded exponentials
+    ("chain-b8", 40.0),     # flat
+    ("chain-b256", 1e-12),
+])
+def test_sample_extreme_temperatures(sv, name, T):
+    check_sample(sv, W.make_chain(name, B=4, gamma=3, V=9000, T=T))
+
+
+def test_sample_huge_logits(sv):
+    # |max logit| >= 1e30 also switches the final pass to the guarded exponentials
+    x = W.make_chain("chain-b256", B=4, gamma=3, V=9000)
+    x.target = (x.target * np.float32(4e30)).astype(np.float32)
+    x.draft = (x.draft * np.float32(4e30)).astype(np.float32)
+    x.T = 3e30
+    check_sample(sv, x)
+
+
 def test_sample_identical_models_accept_all(sv):
     x = W.make_chain("chain-b8", B=4, V=8192)
     x.draft = x.target[:, :x.gamma].copy()

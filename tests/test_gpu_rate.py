@@ -50,23 +50,33 @@ def test_sampling_mismatch_rate(sv, name):
     excused = exact = rows = 0
     failures = []
     accepted = []
-    for _ in range(rounds):
+    events = []
+    lp_err = None
+    for r in range(rounds):
         u = rng.random((x.B, x.gamma + 1), dtype=np.float32)
-        tok, acc = sv.verify_sample(zt, zd, xt, torch.from_numpy(u).cuda(), x.T, workspace=ws)
+        tok, acc, lp = sv.verify_sample(zt, zd, xt, torch.from_numpy(u).cuda(), x.T,
+                                        logprobs=True, workspace=ws)
         tok, acc = tok.cpu().numpy(), acc.cpu().numpy()
         ref = oracle.verify_sample(x.target, x.draft, x.draft_tokens, u, x.T, want_ratio=True,
-                                   want_cdf=True)
+                                   want_cdf=True, want_logprob=(r == 0))
+        if r == 0:
+            # largest relative error of p_i(x_i), q_i(x_i) (the logits are fixed)
+            pg = np.exp(lp.cpu().numpy().astype(np.float64))
+            pr = np.exp(ref["logprob"])
+            lp_err = float(np.max(np.abs(pg - pr) / np.maximum(pr, 1e-300)))
         res = compare_sample(tok, acc, ref, x.draft_tokens, u)
         failures += res["failures"]
         excused += res["excused"]
         exact += res["exact"]
         rows += res["rows"]
+        events += [(k, int(b), int(i), float(m)) for (k, b, i, m) in res["events"]]
         accepted.append(acc.mean())
     rate = excused / rows
     summary = {"workload": name, "rounds": rounds, "rows": rows, "sequences": rounds * x.B,
                "exact_final_tokens": exact, "excused": excused, "hard_failures": len(failures),
                "excused_rate_per_row": rate, "bar": RATE_BAR,
-               "mean_tokens_per_round": float(np.mean(accepted)) + 1.0}
+               "mean_tokens_per_round": float(np.mean(accepted)) + 1.0,
+               "max_prob_rel_err": lp_err, "excused_events": events[:50]}
     print(json.dumps(summary))
     if os.path.isdir(OUT):
         with open(os.path.join(OUT, f"rate_{name}.json"), "w") as f:
