@@ -50,6 +50,8 @@ def _load():
             lib.oracle_verify_greedy.restype = I
             lib.oracle_verify_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, I]
             lib.oracle_verify_tree_greedy.restype = I
+            lib.oracle_topk_exclude.argtypes = [P, P, I, I, I, P, P, I]
+            lib.oracle_topk_exclude.restype = I
             lib.oracle_softmax_row.argtypes = [P, I, ctypes.c_double, P]
             lib.oracle_softmax_row.restype = I
             _lib = lib
@@ -126,6 +128,22 @@ def verify_tree_greedy(target, node_tokens, parents, *, nthreads=0):
     if bad < 0:
         raise ValueError("oracle_verify_tree_greedy: invalid arguments")
     return {"nodes": out_n, "tokens": out_t, "accepted": out_a, "bad": bad}
+
+
+def topk_exclude(logits, K, exclude=None, *, nthreads=0):
+    """Top-K tokens of each row of logits [R, V] (larger logit first, lower
+    index on ties), with exclude[r] removed and -1 padding."""
+    lib = _load()
+    logits = _f32(logits)
+    R, V = logits.shape
+    ex = None if exclude is None else _i32(exclude)
+    out_i = np.empty((R, K), np.int32)
+    out_v = np.empty((R, K), np.float32)
+    rc = lib.oracle_topk_exclude(_ptr(logits), _ptr(ex), R, V, int(K), _ptr(out_i), _ptr(out_v),
+                                 int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_topk_exclude: invalid arguments")
+    return {"idx": out_i, "val": out_v}
 
 
 def softmax_row(z, T):

@@ -309,3 +309,52 @@ int oracle_verify_tree_greedy(const float* target, const int32_t* tokens, const 
     }
     return bad;
 }
+
+/* ---- top-K branch tokens --------------------------------------------------- */
+/* [AdaPLD] 3.3 and Algorithm 1: TopKNextTokens(...) \ {d_main[1]}.  The top K
+ * of a row by (larger logit, then lower index): a scan in index order that
+ * keeps the best K seen so far, sorted; an element enters only when its logit
+ * is strictly larger than the current K-th (so among equal logits the earlier
+ * index stays ahead), then the excluded token is dropped from the list. */
+int oracle_topk_exclude(const float* logits, const int32_t* exclude, int R, int V, int K,
+                        int32_t* out_idx, float* out_val, int nthreads) {
+    if (R < 0 || V <= 0 || K <= 0 || K > 64) return -1;
+    if (R == 0) return 0;
+    if (!logits || !out_idx) return -1;
+    int nt = threads_for(nthreads);
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+        const float* z = logits + (size_t)r * (size_t)V;
+        int32_t* oi = out_idx + (size_t)r * (size_t)K;
+        float* ov = out_val ? out_val + (size_t)r * (size_t)K : NULL;
+        int idx[64];
+        double val[64];
+        int n = 0;                                       /* entries held, <= K */
+        for (int j = 0; j < V; ++j) {
+            const double x = (double)z[j];
+            if (n == K && !(x > val[K - 1])) continue;
+            int pos = n < K ? n : K - 1;                 /* slot it takes before sifting up */
+            if (n < K) ++n;
+            while (pos > 0 && x > val[pos - 1]) {
+                val[pos] = val[pos - 1];
+                idx[pos] = idx[pos - 1];
+                --pos;
+            }
+            val[pos] = x;
+            idx[pos] = j;
+        }
+        const int ex = exclude ? exclude[r] : -1;
+        int o = 0;
+        for (int i = 0; i < n; ++i) {
+            if (idx[i] == ex) continue;
+            oi[o] = idx[i];
+            if (ov) ov[o] = (float)val[i];
+            ++o;
+        }
+        for (; o < K; ++o) {
+            oi[o] = -1;
+            if (ov) ov[o] = -INFINITY;
+        }
+    }
+    return 0;
+}

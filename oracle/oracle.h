@@ -82,6 +82,23 @@ int oracle_verify_tree_greedy(const float* target, const int32_t* tokens, const 
                               int B, int N, int V, int32_t* out_nodes, int32_t* out_tokens,
                               int32_t* out_accepted, int nthreads);
 
+/*
+ * Branch tokens of a draft tree ([AdaPLD] 3.3, "strict hit path", and
+ * Algorithm 1, TopKNextTokens(M, x_{<=p*}, K) \ {d_main[1]}): for each of R
+ * rows of V logits, the K tokens with the largest logits (larger logit first,
+ * lower index first among equal logits, -0.0 equal to +0.0), then the row's
+ * excluded token removed from that list if it is in it.  The list keeps its
+ * order and is padded with -1 at the end (value -inf); it is also padded when
+ * V < K.
+ *   logits   [R, V]
+ *   exclude  [R] (nullable: no exclusion); -1 excludes nothing
+ *   out_idx  [R, K]
+ *   out_val  [R, K] (nullable) the logits of out_idx
+ * K is at most 64.
+ */
+int oracle_topk_exclude(const float* logits, const int32_t* exclude, int R, int V, int K,
+                        int32_t* out_idx, float* out_val, int nthreads);
+
 /* Temperature softmax of one row, p_j = exp(z_j/T - lse), in double. */
 int oracle_softmax_row(const float* z, int V, double T, double* out_p);
 

@@ -529,3 +529,47 @@ def test_zero_mass_tokens_never_chosen_at_cdf_edges():
     for u_last, expect in [(0.0, 2), (1.0, 4)]:
         out = oracle.verify_sample(zt, zd, x, np.array([[0.9, u_last]], np.float32), 1.0)
         assert out["accepted"][0] == 0 and out["tokens"][0, 0] == expect, (u_last, out)
+
+
+# ------------------------------------------------------------- top-K branches
+def _topk_brute(z, K, ex):
+    """AdaPLD, Algorithm 1: TopKNextTokens(...) minus the excluded token, by
+    sorting the whole row on (larger logit, lower index)."""
+    order = sorted(range(len(z)), key=lambda j: (-float(z[j]), j))[:K]
+    kept = [j for j in order if j != ex]
+    return kept + [-1] * (K - len(kept))
+
+
+@pytest.mark.parametrize("V,K", [(1, 1), (3, 4), (7, 2), (50, 4), (50, 8), (1000, 4), (300, 64)])
+def test_topk_matches_sorted_definition(V, K):
+    rng = np.random.default_rng(V * 131 + K)
+    R = 40
+    z = rng.integers(-4, 4, size=(R, V)).astype(np.float32)   # many equal logits
+    ex = rng.integers(-1, V, size=R).astype(np.int32)
+    ex[::3] = -1
+    # half of the exclusions hit a token of the row's top K
+    for r in range(0, R, 2):
+        ex[r] = _topk_brute(z[r], K, -1)[min(K - 1, r % K)]
+    got = oracle.topk_exclude(z, K, ex)
+    for r in range(R):
+        want = _topk_brute(z[r], K, int(ex[r]))
+        assert got["idx"][r].tolist() == want, (r, want, got["idx"][r])
+        for j, v in zip(want, got["val"][r]):
+            assert (j < 0 and v == -np.inf) or v == z[r, j]
+
+
+def test_topk_without_exclusion_k1_is_first_argmax():
+    rng = np.random.default_rng(7)
+    z = rng.integers(-2, 2, size=(30, 97)).astype(np.float32)
+    got = oracle.topk_exclude(z, 1)["idx"][:, 0]
+    assert (got == np.argmax(z, axis=1)).all()
+
+
+def test_topk_signed_zero_and_masked_rows():
+    z = np.array([[-0.0, 0.0, -np.inf, -np.inf],
+                  [-np.inf, -np.inf, -np.inf, -np.inf],
+                  [1.0, -np.inf, 1.0, 0.5]], np.float32)
+    got = oracle.topk_exclude(z, 3, np.array([-1, 1, 0], np.int32))["idx"]
+    assert got[0].tolist() == [0, 1, 2]        # -0.0 == +0.0: lower index first
+    assert got[1].tolist() == [0, 2, -1]       # all masked: index order, 1 excluded
+    assert got[2].tolist() == [2, 3, -1]       # 0 excluded from [0, 2, 3]
