@@ -334,6 +334,9 @@ def run_own(args):
     f1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+    # ---- next-step paths, timed on their own (not part of the step above)
+    extra = {"topk_k4": time_topk(sv, torch, copies, x, stream, sh, max(50, min(K, 500)),
+                                  max_over_ranks, world, dev)}
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
@@ -395,10 +398,53 @@ def run_own(args):
             "gpu_launches": 9 * K,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "extra_paths": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_topk(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, dev):
+    """Top-4 branch tokens (AdaPLD's TopKNextTokens minus the main path's first
+    token) over every target row of the batch, each row excluding the draft
+    token drafted at its position (the bonus row excludes nothing); one call
+    per step on rotating input copies, CUDA events on the launching stream."""
+    B, g, V = x.B, x.gamma, x.V
+    rows = B * (g + 1)
+    dcode = sv.SPEC_DTYPE_BF16 if x.dtype == "bf16" else sv.SPEC_DTYPE_F32
+    ex = np.concatenate([x.draft_tokens, np.full((B, 1), -1, np.int32)], axis=1)
+    exd = torch.from_numpy(np.ascontiguousarray(ex)).to(dev)
+    idx = torch.empty((rows, 4), dtype=torch.int32, device=dev)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get_bytes(sv.spec_topk_workspace_size(rows, V, 4))
+
+    def call(c):
+        st = sv.spec_topk_exclude(c["zt"].data_ptr(), dcode, rows, V, 4, exd.data_ptr(),
+                                  idx.data_ptr(), None, wp, wb, sh)
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, "topk")
+
+    for s in range(5):
+        call(copies[s % len(copies)])
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        call(copies[s % len(copies)])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+    elt = 2 if x.dtype == "bf16" else 4
+    nbytes = rows * V * elt
+    peak, src = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"what": "top-4 of every target row, excluding the row's draft token",
+            "rows": rows, "V": V, "calls": steps, "ms_per_call": ms,
+            "rows_per_s": world * rows / (ms * 1e-3),
+            "hbm": {"achieved_gbs": gbs, "peak_gbs": peak, "peak_source": src,
+                    "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes},
+            "gpu_launches_per_call": 2}
 
 
 def oracle_slice(x, n, ttok, tpar, nthreads):

@@ -176,6 +176,28 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
                                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Branch tokens of a draft tree ([AdaPLD] 3.3 "strict hit path" and
+ * Algorithm 1: TopKNextTokens(M, x_{<=p*}, K) \ {d_main[1]}): for each of
+ * `rows` rows of V logits, the K tokens with the largest logits (larger logit
+ * first, lower index first among equal logits, -0.0 equal to +0.0), then the
+ * row's excluded token removed from that list when it is in it.  The list
+ * keeps its order and is padded with -1 (value -inf), also when V < K.
+ *   logits   [rows, V], row-major, 16-byte aligned, bf16 or fp32; -inf
+ *            (masked) logits are ordinary values, NaN is undefined
+ *   exclude  [rows] int32 (NULL: no exclusion); -1, or any value outside
+ *            [0, V), excludes nothing
+ *   out_idx  [rows, K] int32
+ *   out_val  [rows, K] float (NULL: not written): the logits of out_idx
+ * 1 <= K <= 8.  Workspace: spec_topk_workspace_size(rows, V, K) bytes,
+ * 256-byte aligned, its first 256 bytes zero-filled once (the error word, as
+ * for the verification calls); nothing else is carried between calls.
+ */
+size_t spec_topk_workspace_size(int rows, int V, int K);
+spec_status_t spec_topk_exclude(const void* logits, spec_dtype_t dtype, int rows, int V, int K,
+                                const int32_t* exclude, int32_t* out_idx, float* out_val,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.
  *
  * The source pages have no counterpart to this call; it exists for callers

@@ -56,6 +56,8 @@ SIGNATURES = {
                                     _P], _I),
     "spec_verify_greedy": ([_P, _I, _P, _I, _I, _I, _P, _P, _P, _S, _P], _I),
     "spec_verify_tree_greedy": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
+    "spec_topk_workspace_size": ([_I, _I, _I], _S),
+    "spec_topk_exclude": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
     "spec_verify_read_error": ([_P, _P, _P], _I),
     "spec_verify_status_string": ([_I], ctypes.c_char_p),
 }
@@ -90,6 +92,16 @@ def load_library():
 # ---- raw C-ABI calls (pointers are ints, stream is an int handle or 0) ------
 def spec_verify_workspace_size(B: int, gamma_or_nodes: int, V: int) -> int:
     return load_library().spec_verify_workspace_size(B, gamma_or_nodes, V)
+
+
+def spec_topk_workspace_size(rows: int, V: int, K: int) -> int:
+    return load_library().spec_topk_workspace_size(rows, V, K)
+
+
+def spec_topk_exclude(logits, dtype, rows, V, K, exclude, out_idx, out_val, ws, ws_bytes,
+                      stream) -> int:
+    return load_library().spec_topk_exclude(logits, dtype, rows, V, K, exclude, out_idx, out_val,
+                                            ws, ws_bytes, stream)
 
 
 def spec_verify_workspace_init(ws: int, nbytes: int, stream: int = 0) -> int:
@@ -193,8 +205,10 @@ class Workspace:
         self.buf = None
 
     def get(self, B: int, g: int, V: int, stream=None):
+        return self.get_bytes(spec_verify_workspace_size(B, g, V), stream)
+
+    def get_bytes(self, need: int, stream=None):
         torch = _torch()
-        need = spec_verify_workspace_size(B, g, V)
         if self.buf is None or self.buf.numel() < need:
             self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
             _check(spec_verify_workspace_init(self.buf.data_ptr(), self.buf.numel(), _stream(stream)),
@@ -243,6 +257,28 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, 
                             _stream(stream))
     _check(st, "spec_verify_sample")
     return (tok, acc, lp) if logprobs else (tok, acc)
+
+
+def topk_exclude(logits, K: int, exclude=None, *, values=False,
+                 workspace: Optional[Workspace] = None, out=None, stream=None):
+    """Top-K branch tokens (see spec_topk_exclude).  logits [..., V] contiguous
+    CUDA tensor (bf16 or fp32), exclude int32 with one entry per row or None.
+    Returns idx [..., K] int32 (and, with values=True, the logits [..., K])."""
+    torch = _torch()
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    if out is None:
+        idx = torch.empty((*logits.shape[:-1], K), dtype=torch.int32, device=dev)
+        val = torch.empty((*logits.shape[:-1], K), dtype=torch.float32, device=dev) if values else None
+    else:
+        idx, val = out
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get_bytes(spec_topk_workspace_size(rows, V, K), stream)
+    st = spec_topk_exclude(_ptr(logits), _dtype_code(logits), rows, V, K, _ptr(exclude), _ptr(idx),
+                           _ptr(val), wp, wb, _stream(stream))
+    _check(st, "spec_topk_exclude")
+    return (idx, val) if values else idx
 
 
 def verify_greedy(target, draft_tokens, *, workspace: Optional[Workspace] = None, out=None,

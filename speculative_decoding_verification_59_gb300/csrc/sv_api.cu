@@ -149,6 +149,26 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
                                  out_path_nodes, out_tokens, out_num_accepted, workspace, stream));
 }
 
+size_t spec_topk_workspace_size(int rows, int V, int K) {
+    if (rows < 0 || V <= 0 || K < 1 || K > 8) return 0;
+    return topk_workspace_size(rows, V, K);
+}
+
+spec_status_t spec_topk_exclude(const void* logits, spec_dtype_t dtype, int rows, int V, int K,
+                                const int32_t* exclude, int32_t* out_idx, float* out_val,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || V <= 0 || K < 1 || K > 8) return SPEC_ERR_INVALID_ARG;
+    if ((long long)rows * nseg(V, elt_size(dtype)) >= (1LL << 31)) return SPEC_ERR_INVALID_ARG;
+    if (rows == 0) return SPEC_OK;
+    if (!logits || !out_idx || !workspace) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(logits, 16)) return SPEC_ERR_MISALIGNED;
+    if (!aligned(workspace, 256)) return SPEC_ERR_MISALIGNED;
+    if (workspace_bytes < topk_workspace_size(rows, V, K)) return SPEC_ERR_WORKSPACE_TOO_SMALL;
+    return to_status(launch_topk(logits, dtype, rows, V, K, exclude, out_idx, out_val, workspace,
+                                 stream));
+}
+
 spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32_t* code) {
     if (!workspace || !code) return SPEC_ERR_INVALID_ARG;
     int32_t v = 0;

@@ -22,7 +22,13 @@ constexpr int kGroup = kThreads;                 // 256
 constexpr int kMaxGamma = 256;                   // sampling: rows per sequence <= 513
 constexpr int kMaxNodes = 1024;                  // greedy chains and trees: rows <= 1024
 
-enum : int { kModeSample = 0, kModeGreedy = 1, kModeTree = 2 };
+enum : int { kModeSample = 0, kModeGreedy = 1, kModeTree = 2,
+             kModeTopK2 = 3, kModeTopK4 = 4, kModeTopK8 = 5 };
+
+// List length of a top-K streaming mode (0 for the other modes).
+__host__ __device__ constexpr int topk_of(int mode) {
+    return mode == kModeTopK2 ? 2 : mode == kModeTopK4 ? 4 : mode == kModeTopK8 ? 8 : 0;
+}
 
 // Row-statistics partials take their exponent arguments as z s - fl(m s)
 // while |fl(m s)| < kFmaArgLimit (2^24: the rounding residual of m s is then

@@ -97,4 +97,11 @@ cudaError_t launch_tree(const void* zt, spec_dtype_t dt, const int32_t* tok, con
                         int B, int N, int V, int32_t* out_nodes, int32_t* out_tok,
                         int32_t* out_acc, void* ws, cudaStream_t st);
 
+// Top-K branch tokens (K <= 8) of rows x V logits, one token per row excluded.
+cudaError_t launch_topk(const void* logits, spec_dtype_t dt, int rows, int V, int K,
+                        const int32_t* exclude, int32_t* out_idx, float* out_val, void* ws,
+                        cudaStream_t st);
+size_t topk_workspace_size(int rows, int V, int K);
+int topk_list_len(int K);
+
 }  // namespace sv

@@ -181,7 +181,6 @@ __device__ __forceinline__ int vec_first_eq(const uint4& q, float m) {
 // locate the first occurrence, and that lane's vector is searched alone.
 template <int ELT>
 __device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane], int base) {
-    const int lane = threadIdx.x & 31;
     constexpr int PV = 16 / ELT;
     float vm[kVecPerLane];
     float lm = kNegInf;
@@ -204,11 +203,165 @@ __device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane
     return make_float2(m + 0.0f, __int_as_float(bi));
 }
 
+// ---- top-K lists (branch tokens of a draft tree) -----------------------------
+// The K best (value, index) pairs seen by a lane, best first: larger value
+// first, lower index first among equal values (am_better).  Empty slots hold
+// (-inf, INT_MAX), which every real element beats.
+template <int K>
+struct TopList {
+    float v[K];
+    int i[K];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int k = 0; k < K; ++k) { v[k] = kNegInf; i[k] = 0x7fffffff; }
+    }
+    __device__ __forceinline__ void insert(float x, int j) {
+        if (!am_better(x, j, v[K - 1], i[K - 1])) return;
+        v[K - 1] = x;
+        i[K - 1] = j;
+#pragma unroll
+        for (int k = K - 1; k > 0; --k)
+            if (am_better(v[k], i[k], v[k - 1], i[k - 1])) {
+                const float tv = v[k]; v[k] = v[k - 1]; v[k - 1] = tv;
+                const int ti = i[k]; i[k] = i[k - 1]; i[k - 1] = ti;
+            }
+    }
+};
+
+// The warp's K best entries over all lanes' lists, best first, in every
+// lane: K rounds of a warp argmax over the list heads, the winning lane
+// popping its head (indices are distinct across lanes).
+template <int K>
+__device__ __forceinline__ void warp_merge_topk(TopList<K>& L, float (&ov)[K], int (&oi)[K]) {
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+        float hv = L.v[0];
+        int hi = L.i[0];
+        warp_argmax(hv, hi);
+        ov[r] = hv;
+        oi[r] = hi;
+        if (L.i[0] == hi && hi != 0x7fffffff) {
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k) { L.v[k] = L.v[k + 1]; L.i[k] = L.i[k + 1]; }
+            L.v[K - 1] = kNegInf;
+            L.i[K - 1] = 0x7fffffff;
+        }
+    }
+}
+
+// Entries a warp chunk leaves for a top-K merge: up to 2K candidates in any
+// order, the rest (-inf, INT_MAX).
+__host__ __device__ constexpr int topk_slots(int K) { return 2 * K; }
+
+// Top-K candidates of one warp chunk whose first element is row index base,
+// of which valid_bytes lie inside the row; v holds the lane's vectors, chunk
+// the same bytes in shared memory.  Every element of the chunk's top K is at
+// least thr, the K-th largest of the 32 lane maxima (those are K distinct
+// elements), so only vectors whose maximum reaches thr are opened: each lane
+// marks its elements >= thr in a 64-bit mask (bit 8 t + e for element e of
+// vector t).  When the warp marks at most 2K elements (nearly always: a few
+// more than K) they are written as they are, unsorted, into the chunk's 2K
+// slots -- the merge orders them.  Otherwise the lanes insert their marked
+// elements into sorted lists and the warp merges the lists into the chunk's
+// exact top K.  Marked elements are read back from shared memory in one loop,
+// which keeps the kernel's instruction footprint small.
+template <int ELT, int K>
+__device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
+                                                const unsigned char* chunk, int valid_bytes,
+                                                int base, float2* out) {
+    const int lane = threadIdx.x & 31;
+    constexpr int PV = 16 / ELT;
+    constexpr int KS = topk_slots(K);
+    float vm[kVecPerLane];
+    float lm = kNegInf;
+#pragma unroll
+    for (int t = 0; t < kVecPerLane; ++t) {
+        vm[t] = vec_max_value<ELT>(vec_max_bits<ELT>(v[t]));
+        lm = fmaxf(lm, vm[t]);
+    }
+    float x = lm, thr = kNegInf;
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+        thr = warp_max(x);
+        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
+        if (lane == __ffs(own) - 1) x = kNegInf;
+    }
+    unsigned long long mask = 0ull;
+#pragma unroll
+    for (int t = 0; t < kVecPerLane; ++t) {
+        if ((lane + 32 * t) * 16 < valid_bytes && vm[t] >= thr) {
+            unsigned bits = 0u;
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                float y;
+                if constexpr (ELT == 4) {
+                    y = __uint_as_float(u4_get(v[t], e));
+                } else {
+                    const uint32_t w = u4_get(v[t], e >> 1);
+                    y = (e & 1) ? bf16_hi(w) : bf16_lo(w);
+                }
+                bits |= (y >= thr ? 1u : 0u) << e;
+            }
+            mask |= (unsigned long long)bits << (8 * t);
+        }
+    }
+    auto element = [&](int bit, float* y, int* j) {
+        const int t = bit >> 3, e = bit & 7;
+        const int off = (lane + 32 * t) * 16 + e * ELT;
+        if constexpr (ELT == 4) *y = *reinterpret_cast<const float*>(chunk + off);
+        else *y = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(chunk + off) << 16);
+        *y += 0.0f;                                        // -0.0 counts as +0.0
+        *j = base + (lane + 32 * t) * PV + e;
+    };
+    // exclusive prefix of the lanes' counts
+    const int n = __popcll(mask);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total <= KS) {                                     // warp-uniform
+        int slot = incl - n;
+#pragma unroll 1
+        while (mask) {
+            const int bit = __ffsll((long long)mask) - 1;
+            mask &= mask - 1ull;
+            float y;
+            int j;
+            element(bit, &y, &j);
+            out[slot++] = make_float2(y, __int_as_float(j));
+        }
+        if (lane >= total && lane < KS) out[lane] = make_float2(kNegInf, __int_as_float(0x7fffffff));
+        return;
+    }
+    TopList<K> L;
+    L.init();
+#pragma unroll 1
+    while (mask) {
+        const int bit = __ffsll((long long)mask) - 1;
+        mask &= mask - 1ull;
+        float y;
+        int j;
+        element(bit, &y, &j);
+        L.insert(y, j);
+    }
+    float ov[K];
+    int oi[K];
+    warp_merge_topk<K>(L, ov, oi);
+    if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < K; ++r) out[r] = make_float2(ov[r], __int_as_float(oi[r]));
+    if (lane >= K && lane < KS) out[lane] = make_float2(kNegInf, __int_as_float(0x7fffffff));
+}
+
 template <int ELT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int KT = topk_of(MODE);
     const size_t rowbytes = (size_t)a.V * ELT;
     const int P = a.nseg * kWarps;
     const unsigned total = (unsigned)a.total_chunks;
@@ -268,7 +421,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
         const int wb = bytes - cw * (32 * kLaneBytes);            // valid bytes of this warp chunk
         const bool use = __all_sync(0xffffffffu, ok) && wb > 0;
-        float2 part;
+        float2 part = make_float2(0.f, 0.f);
         if (use) {
             uint4 v[kVecPerLane];
             const unsigned char* chunk = ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes);
@@ -279,16 +432,23 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
             } else {
                 lane_words<ELT>(chunk, wb, v);
             }
+            const int base = (int)(off / ELT) + cw * (32 * kLaneBytes / ELT);
             if constexpr (MODE == kModeSample) part = warp_rowstats<ELT>(v, a.s);
-            else part = warp_argmax_chunk<ELT>(v, (int)(off / ELT) + cw * (32 * kLaneBytes / ELT));
+            else if constexpr (KT > 0)
+                warp_topk_chunk<ELT, KT>(v, chunk, wb, base,
+                                         a.parts + ((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT));
+            else part = warp_argmax_chunk<ELT>(v, base);
         } else {
             part = MODE == kModeSample ? make_float2(kNegInf, 0.f)
                                        : make_float2(kNegInf, __int_as_float(0x7fffffff));
+            if constexpr (KT > 0)
+                if (lane < topk_slots(KT))
+                    a.parts[((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT) + lane] = part;
         }
         __syncwarp();
         if (lane == 0) {
             if (ok) mbar_arrive(&empty[st]);
-            a.parts[(size_t)rr * P + seg * kWarps + cw] = part;
+            if constexpr (KT == 0) a.parts[(size_t)rr * P + seg * kWarps + cw] = part;
         }
     }
     if (!ok && lane == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
@@ -310,8 +470,51 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
         const int seg = (int)(c - rr * (unsigned)a.nseg);
         const char* row = stream_row<MODE>(a, rr, rowbytes);
         const int base = (seg * kWarps + warp) * WE;
-        float2 part;
-        if constexpr (MODE == kModeSample) {
+        float2 part = make_float2(0.f, 0.f);
+        if constexpr (topk_of(MODE) > 0) {
+            // as warp_topk_chunk: threshold from the K-th largest lane
+            // maximum, a mask of the lane's elements that reach it, one
+            // insertion loop (the marked logits are re-read from the row)
+            constexpr int KT = topk_of(MODE);
+            static_assert(LaneChunk<ELT, VEC>::EPL <= 64, "one mask bit per lane element");
+            unsigned long long mask = 0ull;
+            if (base < a.V) {                                  // warp-uniform
+                LaneChunk<ELT, VEC> ch;
+                ch.load(row, a.V, base, lane);
+                float x = kNegInf;
+#pragma unroll
+                for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i) x = fmaxf(x, ch.val(i));
+                float thr = kNegInf;
+#pragma unroll
+                for (int r = 0; r < KT; ++r) {
+                    thr = warp_max(x);
+                    const unsigned own = __ballot_sync(0xffffffffu, x == thr);
+                    if (lane == __ffs(own) - 1) x = kNegInf;
+                }
+#pragma unroll
+                for (int i = 0; i < LaneChunk<ELT, VEC>::EPL; ++i)
+                    if (ch.idx(base, lane, i) < a.V && ch.val(i) >= thr) mask |= 1ull << i;
+            }
+            TopList<KT> L;
+            L.init();
+#pragma unroll 1
+            while (mask) {
+                const int i = __ffsll((long long)mask) - 1;
+                mask &= mask - 1ull;
+                const int j = base + lane + 32 * i;
+                L.insert(load_logit<ELT>(row, j) + 0.0f, j);
+            }
+            float ov[KT];
+            int oi[KT];
+            warp_merge_topk<KT>(L, ov, oi);
+            float2* out = a.parts + ((size_t)rr * P + seg * kWarps + warp) * topk_slots(KT);
+            if (lane == 0)
+#pragma unroll
+                for (int r = 0; r < KT; ++r) out[r] = make_float2(ov[r], __int_as_float(oi[r]));
+            if (lane >= KT && lane < topk_slots(KT))
+                out[lane] = make_float2(kNegInf, __int_as_float(0x7fffffff));
+            continue;
+        } else if constexpr (MODE == kModeSample) {
             float m = kNegInf, z = 0.f;
             if (base < a.V) {
                 LaneChunk<ELT, VEC> ch;

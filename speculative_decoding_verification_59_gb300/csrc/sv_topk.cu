@@ -1,0 +1,143 @@
+// Branch tokens of a draft tree: the top K tokens of each logit row with one
+// token excluded.
+//
+// Source: "AdaPLD: adaptive retrieval and reuse for efficient model-free
+// speculative decoding", section 3.3 (strict hit path: the branches are the
+// target model's top K next tokens, without the token the copied main path
+// already starts with) and Algorithm 1 (TopKNextTokens(M, x_{<=p*}, K) \
+// {d_main[1]}; without the exclusion on the semantic hit path).
+//
+// The top K of a row is taken by (larger logit, lower index): temperature does
+// not change it.  The excluded token is removed from that list afterwards,
+// which leaves K-1 tokens when it was among them; the list is padded with -1.
+//
+// One streaming pass (sv_stream.cuh, top-K mode) turns every 4 KB warp chunk
+// of every row into at most 2 KC candidates that include the chunk's top KC
+// (KC = 2, 4 or 8, the smallest that is at least K); one warp per row then
+// merges the row's candidates into its top KC and applies the exclusion,
+// chained behind the stream with programmatic dependent launch.
+#include "sv_stream.cuh"
+
+namespace sv {
+
+constexpr int kTopkRowsPerCta = kThreads / 32;
+
+template <int KC>
+__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a, int K,
+                                                              const int32_t* exclude,
+                                                              float* out_val) {
+    constexpr int KS = topk_slots(KC);
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kTopkRowsPerCta + (threadIdx.x >> 5);
+    if (r >= a.B) return;                                 // warp-uniform
+    // The row's candidates are one contiguous array of n entries.  Pass 1:
+    // each lane's largest; the row's top KC are all at least thr, the KC-th
+    // largest of those 32 maxima.  Pass 2 inserts only entries >= thr.
+    const int n = a.nseg * kWarps * KS;
+    const float2* pr = a.parts + (size_t)r * n;
+    constexpr int kBatch = 8;                             // loads in flight per lane
+    float x = kNegInf;
+    for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
+        float2 e[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int i = q0 + 32 * q;
+            e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) x = fmaxf(x, e[q].x);
+    }
+    float thr = kNegInf;
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+        thr = warp_max(x);
+        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
+        if (lane == __ffs(own) - 1) x = kNegInf;
+    }
+    TopList<KC> L;
+    L.init();
+    for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
+        float2 e[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int i = q0 + 32 * q;
+            e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            if (e[q].x >= thr) L.insert(e[q].x, __float_as_int(e[q].y));
+    }
+    float ov[KC];
+    int oi[KC];
+    warp_merge_topk<KC>(L, ov, oi);
+    if (lane == 0) {
+        const int ex = exclude ? exclude[r] : -1;
+        int o = 0;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            const bool keep = k < K && oi[k] >= 0 && oi[k] < a.V && oi[k] != ex;
+            if (keep) {
+                a.out_tok[(size_t)r * K + o] = oi[k];
+                if (out_val) out_val[(size_t)r * K + o] = ov[k];
+                ++o;
+            }
+        }
+        for (; o < K; ++o) {
+            a.out_tok[(size_t)r * K + o] = -1;
+            if (out_val) out_val[(size_t)r * K + o] = kNegInf;
+        }
+    }
+}
+
+int topk_list_len(int K) { return K <= 2 ? 2 : K <= 4 ? 4 : 8; }
+
+template <int KC>
+static cudaError_t launch_topk_t(const VerifyArgs& a, int elt, int K, const int32_t* exclude,
+                                 float* out_val, const DeviceInfo& di, cudaStream_t st) {
+    constexpr int MODE = KC == 2 ? kModeTopK2 : KC == 4 ? kModeTopK4 : kModeTopK8;
+    cudaError_t e = elt == 2 ? launch_stream<2, MODE>(a, di, st) : launch_stream<4, MODE>(a, di, st);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.B + kTopkRowsPerCta - 1) / kTopkRowsPerCta, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_merge_kernel<KC>, a, K, exclude, out_val);
+}
+
+cudaError_t launch_topk(const void* logits, spec_dtype_t dt, int rows, int V, int K,
+                        const int32_t* exclude, int32_t* out_idx, float* out_val, void* ws,
+                        cudaStream_t st) {
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int elt = elt_size(dt);
+    char* w = static_cast<char*>(ws);
+    VerifyArgs a = {};
+    a.zt = static_cast<const char*>(logits);
+    a.rows_per_seq = 1;
+    a.V = V;
+    a.nseg = nseg(V, elt);
+    a.total_chunks = (long long)rows * a.nseg;
+    a.B = rows;
+    a.parts = reinterpret_cast<float2*>(w + 256);
+    a.err = reinterpret_cast<int*>(w);
+    a.out_tok = out_idx;
+    const int KC = topk_list_len(K);
+    if (KC == 2) return launch_topk_t<2>(a, elt, K, exclude, out_val, di, st);
+    if (KC == 4) return launch_topk_t<4>(a, elt, K, exclude, out_val, di, st);
+    return launch_topk_t<8>(a, elt, K, exclude, out_val, di, st);
+}
+
+size_t topk_workspace_size(int rows, int V, int K) {
+    // error word, then 2 KC candidate entries per warp chunk (fp32 has the most chunks)
+    return 256 + align256(sizeof(float2) * (size_t)rows * (size_t)nseg(V, 4) * kWarps *
+                          (size_t)topk_slots(topk_list_len(K)));
+}
+
+}  // namespace sv

@@ -92,6 +92,26 @@ def test_sample_argument_checks(lib):
     assert call_sample(ws_bytes=need - 1) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_topk_argument_checks(lib):
+    k = sv.spec_topk_exclude
+    need = sv.spec_topk_workspace_size(3, 100, 4)
+    assert need > 256
+    assert sv.spec_topk_workspace_size(3, 100, 9) == 0            # K outside 1..8
+    assert sv.spec_topk_workspace_size(3, 100, 8) >= sv.spec_topk_workspace_size(3, 100, 4)
+    assert k(FAKE, 9, 3, 100, 4, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_UNSUPPORTED_DTYPE
+    assert k(FAKE, 0, 3, 100, 0, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE, 0, 3, 100, 9, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE, 0, -1, 100, 4, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE, 0, 3, 0, 4, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE, 0, 0, 100, 4, None, FAKE, None, WS, need, None) == sv.SPEC_OK
+    assert k(None, 0, 3, 100, 4, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE, 0, 3, 100, 4, None, None, None, WS, need, None) == sv.SPEC_ERR_INVALID_ARG
+    assert k(FAKE + 4, 0, 3, 100, 4, None, FAKE, None, WS, need, None) == sv.SPEC_ERR_MISALIGNED
+    assert k(FAKE, 0, 3, 100, 4, None, FAKE, None, WS + 64, need, None) == sv.SPEC_ERR_MISALIGNED
+    assert k(FAKE, 0, 3, 100, 4, None, FAKE, None, WS, need - 1, None) == \
+        sv.SPEC_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_greedy_and_tree_argument_checks(lib):
     g = sv.spec_verify_greedy
     assert g(FAKE, 5, FAKE, 1, 1, 10, FAKE, FAKE, WS, 1 << 20, None) == sv.SPEC_ERR_UNSUPPORTED_DTYPE
