@@ -335,8 +335,10 @@ def run_own(args):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     # ---- next-step paths, timed on their own (not part of the step above)
-    extra = {"topk_k4": time_topk(sv, torch, copies, x, stream, sh, max(50, min(K, 500)),
-                                  max_over_ranks, world, dev)}
+    nx = max(50, min(K, 500))
+    extra = {"topk_k4": time_topk(sv, torch, copies, x, stream, sh, nx, max_over_ranks, world, dev),
+             "lazy_sample": time_lazy(sv, torch, copies, x, stream, sh, nx, max_over_ranks, world,
+                                      dev, acct)}
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
@@ -445,6 +447,47 @@ def time_topk(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, de
             "hbm": {"achieved_gbs": gbs, "peak_gbs": peak, "peak_source": src,
                     "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes},
             "gpu_launches_per_call": 2}
+
+
+def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, dev, acct):
+    """spec_verify_sample_lazy on the step's inputs: the same tokens as the
+    full sampling pass, reading only the rows of positions up to the first
+    rejection.  Reports the call time and the bytes actually read."""
+    B, g, V = x.B, x.gamma, x.V
+    dcode = sv.SPEC_DTYPE_BF16 if x.dtype == "bf16" else sv.SPEC_DTYPE_F32
+    tok = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get(B, g, V)
+
+    def call(c):
+        st = sv.spec_verify_sample_lazy(c["zt"].data_ptr(), c["zd"].data_ptr(), dcode,
+                                        c["x"].data_ptr(), c["u"].data_ptr(), x.T, B, g, V,
+                                        tok.data_ptr(), acc.data_ptr(), None, wp, wb, sh)
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, "lazy")
+
+    for s in range(5):
+        call(copies[s % len(copies)])
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        call(copies[s % len(copies)])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+    k = acc.cpu().numpy().astype(np.int64)
+    elt = 2 if x.dtype == "bf16" else 4
+    rows_read = int(np.where(k >= g, 2 * g + 1, 2 * (k + 1)).sum())
+    bytes_read = rows_read * V * elt
+    return {"what": "lazy stochastic verification (rows after the first rejection not read) "
+                    "+ final sample, same inputs as the step",
+            "ms_per_call": ms, "calls": steps,
+            "rows_per_s": world * B * (g + 1) / (ms * 1e-3),
+            "pass1_rows_read": rows_read, "pass1_rows_full": B * (2 * g + 1),
+            "pass1_bytes_read": bytes_read, "pass1_bytes_full": acct["bytes_stats"],
+            "gpu_launches_per_call": 4}
 
 
 def oracle_slice(x, n, ttok, tpar, nthreads):

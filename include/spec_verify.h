@@ -121,6 +121,27 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
                                  cudaStream_t stream);
 
 /*
+ * Lazy (early-exit) stochastic verification ([SD] "What happens in one
+ * round", step 3: the first rejection discards every later draft, so a
+ * position's rows are only needed while every earlier draft was accepted).
+ * Same arguments, workspace and outputs as spec_verify_sample, with the same
+ * tokens and accept counts; only the rows of positions 0..k are read (and
+ * target row gamma when every draft is accepted): 2 (k + 1) rows instead of
+ * 2 gamma + 1 after a rejection at k.  out_logprobs (nullable) holds the
+ * log-probabilities of positions 0..min(k, gamma - 1); later positions, and
+ * every position of a bad sequence, are NaN.  One thread-block cluster per
+ * sequence.  Rows whose byte length is not a multiple of 16 take the full
+ * pass (every row read) with the same outputs.  Device-side bad-input
+ * detection covers the rows it reads.
+ */
+spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* draft_logits,
+                                      spec_dtype_t dtype, const int32_t* draft_tokens,
+                                      const float* uniforms, float temperature, int B, int gamma,
+                                      int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                      float* out_logprobs, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
+/*
  * The two halves of spec_verify_sample, for callers that want to overlap or
  * time them separately; spec_verify_sample is exactly _stats then _finish on
  * the same stream with the same arguments and workspace.

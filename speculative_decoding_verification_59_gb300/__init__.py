@@ -49,6 +49,8 @@ SIGNATURES = {
     "spec_verify_workspace_init": ([_P, _S, _P], _I),
     "spec_verify_sample": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _S,
                             _P], _I),
+    "spec_verify_sample_lazy": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _S,
+                                 _P], _I),
     "spec_verify_sample_stats": ([_P, _P, _I, ctypes.c_float, _I, _I, _I, _P, _S, _P], _I),
     "spec_verify_sample_finish": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P,
                                    _S, _P], _I),
@@ -113,6 +115,15 @@ def spec_verify_sample(target, draft, dtype, draft_tokens, uniforms, temperature
     return load_library().spec_verify_sample(target, draft, dtype, draft_tokens, uniforms,
                                              temperature, B, gamma, V, out_tokens,
                                              out_num_accepted, out_logprobs, ws, ws_bytes, stream)
+
+
+def spec_verify_sample_lazy(target, draft, dtype, draft_tokens, uniforms, temperature, B, gamma,
+                            V, out_tokens, out_num_accepted, out_logprobs, ws, ws_bytes,
+                            stream) -> int:
+    return load_library().spec_verify_sample_lazy(target, draft, dtype, draft_tokens, uniforms,
+                                                  temperature, B, gamma, V, out_tokens,
+                                                  out_num_accepted, out_logprobs, ws, ws_bytes,
+                                                  stream)
 
 
 def spec_verify_sample_stats(target, draft, dtype, temperature, B, gamma, V, ws, ws_bytes,
@@ -234,11 +245,13 @@ def _ws(workspace, device):
 
 
 def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, logprobs=False,
-                  workspace: Optional[Workspace] = None, out=None, stream=None):
+                  workspace: Optional[Workspace] = None, out=None, stream=None, lazy=False):
     """Stochastic verification (see spec_verify_sample).  target [B, g+1, V],
     draft [B, g, V] (same dtype), draft_tokens [B, g] int32, uniforms
     [B, g+1] float32, all contiguous CUDA tensors.  Returns (tokens [B, g+1],
-    num_accepted [B]) or, with logprobs=True, also [B, g, 2] log-probabilities."""
+    num_accepted [B]) or, with logprobs=True, also [B, g, 2] log-probabilities.
+    lazy=True: spec_verify_sample_lazy (same outputs, rows after the first
+    rejection not read, their log-probabilities NaN)."""
     torch = _torch()
     B, g1, V = target.shape
     g = g1 - 1
@@ -251,11 +264,11 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, 
         tok, acc, lp = out
     ws = _ws(workspace, dev)
     wp, wb = ws.get(B, g, V, stream)
-    st = spec_verify_sample(_ptr(target), _ptr(draft) if g > 0 else None, _dtype_code(target),
-                            _ptr(draft_tokens) if g > 0 else None, _ptr(uniforms),
-                            float(temperature), B, g, V, _ptr(tok), _ptr(acc), _ptr(lp), wp, wb,
-                            _stream(stream))
-    _check(st, "spec_verify_sample")
+    fn = spec_verify_sample_lazy if lazy else spec_verify_sample
+    st = fn(_ptr(target), _ptr(draft) if g > 0 else None, _dtype_code(target),
+            _ptr(draft_tokens) if g > 0 else None, _ptr(uniforms), float(temperature), B, g, V,
+            _ptr(tok), _ptr(acc), _ptr(lp), wp, wb, _stream(stream))
+    _check(st, "spec_verify_sample_lazy" if lazy else "spec_verify_sample")
     return (tok, acc, lp) if logprobs else (tok, acc)
 
 

@@ -69,14 +69,14 @@ static spec_status_t sample_common(const void* target_logits, const void* draft_
     if (!(temperature >= kMinTemperature) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
     if (B == 0) return SPEC_OK;
     if (!target_logits || (gamma > 0 && !draft_logits)) return SPEC_ERR_INVALID_ARG;
-    if ((parts & kSampleFinish) &&
-        (!uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)))
+    const bool finish = (parts & (kSampleFinish | kSampleLazy)) != 0;
+    if (finish && (!uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)))
         return SPEC_ERR_INVALID_ARG;
     if (!aligned(target_logits, 16) || (gamma > 0 && !aligned(draft_logits, 16)))
         return SPEC_ERR_MISALIGNED;
     spec_status_t s = check_ws(workspace, workspace_bytes, B, gamma, V);
     if (s != SPEC_OK) return s;
-    if ((parts & kSampleFinish) && !sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
+    if (finish && !sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
     return to_status(launch_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                                    temperature, B, gamma, V, out_tokens, out_num_accepted,
                                    out_logprobs, workspace, stream, parts));
@@ -91,6 +91,17 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
     return sample_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
                          B, gamma, V, out_tokens, out_num_accepted, out_logprobs, workspace,
                          workspace_bytes, stream, kSampleStats | kSampleFinish);
+}
+
+spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* draft_logits,
+                                      spec_dtype_t dtype, const int32_t* draft_tokens,
+                                      const float* uniforms, float temperature, int B, int gamma,
+                                      int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                      float* out_logprobs, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+    return sample_common(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                         B, gamma, V, out_tokens, out_num_accepted, out_logprobs, workspace,
+                         workspace_bytes, stream, kSampleLazy);
 }
 
 spec_status_t spec_verify_sample_stats(const void* target_logits, const void* draft_logits,

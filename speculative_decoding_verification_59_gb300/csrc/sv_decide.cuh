@@ -83,6 +83,58 @@ struct SampleDecideSmem {
     int bad, k;
 };
 
+// Row r of sequence b from its warp partials (one warp, every lane gets the
+// result): M = max m_p and lnZ = ln sum_p Z_p 2^((m_p - M) s - r_p), with
+// r_p = partial_residual(m_p) (float-float sum, each lane holding up to
+// kHeld partials in registers).  lnZ is 0 for a row without a finite logit.
+__device__ __forceinline__ void merge_row_stats(const VerifyArgs& a, int b, int r, int lane,
+                                                float* Mout, float* lnZout) {
+    constexpr int kHeld = 8;
+    const int P = a.nseg * kWarps;
+    const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
+    float2 q[kHeld];
+#pragma unroll
+    for (int h = 0; h < kHeld; ++h) {
+        const int p = lane + 32 * h;
+        q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
+    }
+    float m = kNegInf;
+#pragma unroll
+    for (int h = 0; h < kHeld; ++h) m = fmaxf(m, q[h].x);
+    for (int p = lane + 32 * kHeld; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
+    m = warp_max(m);
+    FF z{0.f, 0.f};
+    if (m != kNegInf) {
+#pragma unroll
+        for (int h = 0; h < kHeld; ++h)
+            if (q[h].x != kNegInf)
+                ff_add(z, q[h].y * ex2_approx(fmaf(q[h].x - m, a.s, -partial_residual(q[h].x, a.s))));
+        for (int p = lane + 32 * kHeld; p < P; p += 32) {
+            const float2 t = __ldcg(&pr[p]);
+            if (t.x != kNegInf)
+                ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
+        }
+    }
+    z = ff_norm(warp_sum_ff(z));
+    *Mout = m;
+    *lnZout = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
+}
+
+// ln p(x) = (z_x - M)/T - lnZ for a row with max M and normaliser lnZ.
+__device__ __forceinline__ float row_log_prob(float zx, float M, float lnZ, const VerifyArgs& a) {
+    return (zx - M) / a.T - lnZ;
+}
+
+// The accept test u < p(x)/q(x) from the two log-probabilities (p = 0
+// rejects, q = 0 with p > 0 accepts).
+__device__ __forceinline__ bool accept_draft(float lp, float lq, float u) {
+    float r;
+    if (lp == kNegInf) r = 0.f;
+    else if (lq == kNegInf) r = CUDART_INF_F;
+    else r = expf(lp - lq);
+    return u < r;
+}
+
 // Row statistics from the partials (M = max m_p, Z = sum Z_p 2^((m_p - M) s),
 // float-float) and the accept decisions u_i < p_i(x_i)/q_i(x_i) in single
 // precision (GB300's double-precision rate is a small fraction of its float
@@ -92,7 +144,6 @@ struct SampleDecideSmem {
 template <int ELT>
 __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
     const int lane = gt & 31, gw = gt >> 5;
-    const int P = a.nseg * kWarps;
     const size_t rowbytes = (size_t)a.V * ELT;
     // Issue the gathers of z[x_i] first: their latency overlaps the merges.
     int xi = -1;
@@ -106,39 +157,12 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
     }
     if (gt == 0) sm.bad = 0;
     group_sync();
-    // Row r: M = max m_p, Z = sum Z_p 2^((m_p - M) s - r_p) over its warp
-    // partials, r_p = partial_residual(m_p), each lane holding up to kHeld of
-    // them in registers (float-float sum).
-    constexpr int kHeld = 8;
     for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
-        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
-        float2 q[kHeld];
-#pragma unroll
-        for (int h = 0; h < kHeld; ++h) {
-            const int p = lane + 32 * h;
-            q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
-        }
-        float m = kNegInf;
-#pragma unroll
-        for (int h = 0; h < kHeld; ++h) m = fmaxf(m, q[h].x);
-        for (int p = lane + 32 * kHeld; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
-        m = warp_max(m);
-        FF z{0.f, 0.f};
-        if (m != kNegInf) {
-#pragma unroll
-            for (int h = 0; h < kHeld; ++h)
-                if (q[h].x != kNegInf)
-                    ff_add(z, q[h].y * ex2_approx(fmaf(q[h].x - m, a.s, -partial_residual(q[h].x, a.s))));
-            for (int p = lane + 32 * kHeld; p < P; p += 32) {
-                const float2 t = __ldcg(&pr[p]);
-                if (t.x != kNegInf)
-                    ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
-            }
-        }
-        z = ff_norm(warp_sum_ff(z));
+        float M, lnZ;
+        merge_row_stats(a, b, r, lane, &M, &lnZ);
         if (lane == 0) {
-            sm.M[r] = m;
-            sm.lnZ[r] = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
+            sm.M[r] = M;
+            sm.lnZ[r] = lnZ;
         }
     }
     group_sync();
@@ -154,8 +178,8 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
             sm.lp[i] = sm.lq[i] = 0.f;
         } else {
-            sm.lp[i] = (ztx - sm.M[i]) / a.T - sm.lnZ[i];
-            sm.lq[i] = (zdx - sm.M[a.gamma + 1 + i]) / a.T - sm.lnZ[a.gamma + 1 + i];
+            sm.lp[i] = row_log_prob(ztx, sm.M[i], sm.lnZ[i], a);
+            sm.lq[i] = row_log_prob(zdx, sm.M[a.gamma + 1 + i], sm.lnZ[a.gamma + 1 + i], a);
         }
     }
     for (int r = gt; r < a.rows_per_seq; r += kGroup)
@@ -165,14 +189,8 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
         int k = -1;
         if (!sm.bad) {
             k = a.gamma;                                   // left to right; first rejection wins
-            for (int i = 0; i < a.gamma; ++i) {
-                const float lp = sm.lp[i], lq = sm.lq[i];
-                float r;
-                if (lp == kNegInf) r = 0.f;
-                else if (lq == kNegInf) r = CUDART_INF_F;
-                else r = expf(lp - lq);
-                if (!(a.u[(size_t)b * (a.gamma + 1) + i] < r)) { k = i; break; }
-            }
+            for (int i = 0; i < a.gamma; ++i)
+                if (!accept_draft(sm.lp[i], sm.lq[i], a.u[(size_t)b * (a.gamma + 1) + i])) { k = i; break; }
         }
         sm.k = k;
     }

@@ -80,9 +80,10 @@ cudaError_t device_info(DeviceInfo* out);
 
 // ---- launchers (return the first CUDA error) ------------------------------
 // parts: kSampleStats (streaming row statistics), kSampleFinish (the accept
-// decisions and the final residual/bonus token), or both.
+// decisions and the final residual/bonus token), both, or kSampleLazy.
 constexpr int kSampleStats = 1;
 constexpr int kSampleFinish = 2;
+constexpr int kSampleLazy = 4;     // early-exit pass instead of stats + decisions, then the final sample
 cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
                           const float* u, float T, int B, int gamma, int V, int32_t* out_tok,
                           int32_t* out_acc, float* out_lp, void* ws, cudaStream_t st, int parts);

@@ -537,6 +537,230 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     }
 }
 
+// ------------------------------------------------ lazy (early-exit) pass 1
+// Source: "Speculative decoding: guess a few tokens first - why the answer
+// stays the same", section "What happens in one round", step 3: drafts are
+// checked left to right and the first rejection discards every later draft.
+// The lazy pass therefore reads position i's two rows only when drafts
+// 0..i-1 were all accepted: one thread-block cluster per sequence streams the
+// rows of one position at a time (target row i and draft row i, target row
+// gamma last), each of its kLazyCluster CTAs taking a fixed share of the block
+// chunks of a row through the same bulk-copy ring and warp_rowstats as the
+// full pass, so the per-warp partials -- and every decision taken from them --
+// are bit-identical to the full pass.  After each position a cluster barrier
+// makes the partials visible; every CTA then merges the two rows and takes
+// the accept decision (the same arithmetic in each CTA, so all agree), and
+// the cluster stops at the first rejection.  Bytes read per sequence:
+// 2 (k + 1) rows after a rejection at k, 2 gamma + 1 when all are accepted.
+// The final sample runs the usual zsum / wsum / search kernels.
+constexpr int kLazyCluster = 4;
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int ELT>
+__global__ void __launch_bounds__(kRingThreads, 2) lazy_sample_kernel(const VerifyArgs a) {
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ float sM[2], slnZ[2];
+    __shared__ float s_lp[kMaxGamma], s_lq[kMaxGamma];
+    __shared__ float s_zt[kMaxGamma], s_zd[kMaxGamma];   // z^t_i[x_i], z^d_i[x_i], gathered up front
+    __shared__ int s_stop, s_k, s_bad, s_ok;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned rank = cluster_ctarank();
+    const int b = blockIdx.x / kLazyCluster;
+    const size_t rowbytes = (size_t)a.V * ELT;
+    const int P = a.nseg * kWarps;
+    unsigned sg0, sg1;
+    cta_range((unsigned)a.nseg, rank, kLazyCluster, &sg0, &sg1);
+    const unsigned nmine = sg1 - sg0;                     // this CTA's block chunks of a row
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kWarps);
+        }
+        mbar_init_fence();
+        int bad = 0;
+        for (int i = 0; i < a.gamma; ++i) {
+            const int xi = a.x[(size_t)b * a.gamma + i];
+            if (xi < 0 || xi >= a.V) bad = SPEC_DEVERR_TOKEN_RANGE;
+        }
+        s_bad = bad;
+        s_stop = 0;
+        s_ok = 1;
+    }
+    for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
+        const int xi = a.x[(size_t)b * a.gamma + i];
+        const bool in = xi >= 0 && xi < a.V;
+        s_zt[i] = in ? load_logit<ELT>(sample_row(a, b, i, rowbytes), xi) : 0.f;
+        s_zd[i] = in ? load_logit<ELT>(sample_row(a, b, a.gamma + 1 + i, rowbytes), xi) : 0.f;
+    }
+    __syncthreads();
+    pdl_trigger();
+    int k = -1;
+    unsigned issued = 0, it = 0;                          // ring counters, kept across positions
+    bool ok = true;
+    if (!s_bad) {
+        for (int i = 0; i <= a.gamma; ++i) {
+            const unsigned nchunks = (i < a.gamma ? 2u : 1u) * nmine;
+            // rows of position i: j = 0 target row i, j = 1 draft row i
+            auto row_of = [&](unsigned cc) { return cc < nmine ? i : a.gamma + 1 + i; };
+            if (warp == 0) {
+                if (lane == 0) {
+                    for (unsigned cc = 0; cc < nchunks && ok; ++cc, ++issued) {
+                        const int st = (int)(issued % kStages);
+                        const unsigned use = issued / kStages;
+                        if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) { ok = false; break; }
+                        const int seg = (int)(sg0 + cc % nmine);
+                        const size_t off = (size_t)seg * kStageBytes;
+                        const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
+                        mbar_arrive_expect_tx(&full[st], bytes);
+                        bulk_g2s(ring + (size_t)st * kStageBytes,
+                                 sample_row(a, b, row_of(cc), rowbytes) + off, bytes, &full[st]);
+                    }
+                    if (!ok) s_ok = 0;
+                }
+            } else {
+                const int cw = warp - 1;
+                for (unsigned cc = 0; cc < nchunks; ++cc, ++it) {
+                    const int st = (int)(it % kStages);
+                    if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
+                    const int seg = (int)(sg0 + cc % nmine);
+                    const size_t off = (size_t)seg * kStageBytes;
+                    const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
+                    const int wb = bytes - cw * (32 * kLaneBytes);
+                    const bool use = __all_sync(0xffffffffu, ok) && wb > 0;
+                    float2 part = make_float2(kNegInf, 0.f);
+                    if (use) {
+                        uint4 v[kVecPerLane];
+                        const unsigned char* chunk = ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes);
+                        if (wb >= 32 * kLaneBytes) {
+#pragma unroll
+                            for (int t = 0; t < kVecPerLane; ++t)
+                                v[t] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * t) * 16);
+                        } else {
+                            lane_words<ELT>(chunk, wb, v);
+                        }
+                        part = warp_rowstats<ELT>(v, a.s);
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (ok) mbar_arrive(&empty[st]);
+                        a.parts[((size_t)b * a.rows_per_seq + row_of(cc)) * P + seg * kWarps + cw] = part;
+                    }
+                }
+                if (!ok && lane == 0) s_ok = 0;
+            }
+            __syncthreads();
+            cluster_sync_all();                           // every CTA's partials of position i are visible
+            if (warp == 1 || (warp == 2 && i < a.gamma)) {
+                const int j = warp - 1;
+                float M, lnZ;
+                merge_row_stats(a, b, j == 0 ? i : a.gamma + 1 + i, lane, &M, &lnZ);
+                if (lane == 0) { sM[j] = M; slnZ[j] = lnZ; }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                if (!s_ok) {
+                    atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+                    s_stop = 1;
+                    s_k = -1;
+                } else if (sM[0] == kNegInf || (i < a.gamma && sM[1] == kNegInf)) {
+                    s_bad = SPEC_DEVERR_EMPTY_ROW;
+                    s_stop = 1;
+                    s_k = -1;
+                } else if (i == a.gamma) {
+                    s_stop = 1;                           // every draft accepted
+                    s_k = a.gamma;
+                } else {
+                    const float lp = row_log_prob(s_zt[i], sM[0], slnZ[0], a);
+                    const float lq = row_log_prob(s_zd[i], sM[1], slnZ[1], a);
+                    s_lp[i] = lp;
+                    s_lq[i] = lq;
+                    if (!accept_draft(lp, lq, a.u[(size_t)b * (a.gamma + 1) + i])) {
+                        s_stop = 1;
+                        s_k = i;
+                    }
+                }
+            }
+            __syncthreads();
+            if (s_stop) break;                            // block-uniform, and the same in every CTA
+        }
+        k = s_k;
+    }
+    if (rank != 0) return;
+    // outputs of the sequence (CTA 0 of the cluster); slot k belongs to the search
+    if (s_bad) {
+        k = -1;
+        if (threadIdx.x == 0) atomicOr(a.err, s_bad);
+    }
+    if (threadIdx.x == 0) {
+        a.out_acc[b] = k;
+        SampleDesc d;
+        d.k = k;
+        d.mt = k >= 0 ? sM[0] : 0.f;
+        d.md = (k >= 0 && k < a.gamma) ? sM[1] : 0.f;
+        d.pad = 0;
+        a.desc[b] = d;
+    }
+    for (int i = threadIdx.x; i <= a.gamma; i += blockDim.x)
+        if (k < 0 || i != k)
+            a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
+    if (a.out_lp)
+        for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
+            float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
+            const bool have = k >= 0 && i <= k;           // positions that were read
+            o[0] = have ? s_lp[i] : CUDART_NAN_F;
+            o[1] = have ? s_lq[i] : CUDART_NAN_F;
+        }
+}
+
+// Rows that are not a multiple of 16 bytes take the full pass in lazy mode;
+// this clears the log-probabilities of the positions a lazy pass does not read.
+__global__ void lazy_mask_logprobs_kernel(const VerifyArgs a) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= a.B) return;
+    const int k = a.out_acc[b];
+    for (int i = 0; i < a.gamma; ++i)
+        if (k < 0 || i > k) {
+            a.out_lp[((size_t)b * a.gamma + i) * 2] = CUDART_NAN_F;
+            a.out_lp[((size_t)b * a.gamma + i) * 2 + 1] = CUDART_NAN_F;
+        }
+}
+
+template <int ELT>
+static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
+    auto kfn = lazy_sample_kernel<ELT>;
+    const int smem = kStages * kStageBytes;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.B * kLazyCluster, 1, 1);
+    cfg.blockDim = dim3(kRingThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kLazyCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, a);
+}
+
 // ---------------------------------------------------------------- launch
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor drains and waits (griddepcontrol.wait) for its results.
@@ -556,9 +780,12 @@ static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const VerifyArgs& a
 }
 
 template <int ELT, bool VEC>
-static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st) {
-    cudaError_t e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, a, st);
-    if (e != cudaSuccess) return e;
+static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool decide = true) {
+    cudaError_t e = cudaSuccess;
+    if (decide) {
+        e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, a, st);
+        if (e != cudaSuccess) return e;
+    }
     e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
     if (e != cudaSuccess) return e;
     e = launch_pdl(sample_wsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
@@ -603,6 +830,16 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     a.out_acc = out_acc;
     a.out_lp = out_lp;
 
+    bool mask_lp = false;
+    if (parts & kSampleLazy) {
+        if (vec) {
+            e = elt == 2 ? launch_lazy<2>(a, st) : launch_lazy<4>(a, st);
+            if (e != cudaSuccess) return e;
+            return elt == 2 ? launch_final_t<2, true>(a, st, false) : launch_final_t<4, true>(a, st, false);
+        }
+        parts = kSampleStats | kSampleFinish;             // full pass, then unread positions cleared
+        mask_lp = out_lp != nullptr;
+    }
     if (parts & kSampleStats) {
         e = elt == 2 ? launch_stream<2, kModeSample>(a, di, st) : launch_stream<4, kModeSample>(a, di, st);
         if (e != cudaSuccess) return e;
@@ -610,6 +847,11 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     if (parts & kSampleFinish) {
         if (elt == 2) e = vec ? launch_final_t<2, true>(a, st) : launch_final_t<2, false>(a, st);
         else e = vec ? launch_final_t<4, true>(a, st) : launch_final_t<4, false>(a, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (mask_lp) {
+        lazy_mask_logprobs_kernel<<<(B + 127) / 128, 128, 0, st>>>(a);
+        e = cudaGetLastError();
     }
     return e;
 }

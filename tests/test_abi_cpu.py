@@ -92,6 +92,25 @@ def test_sample_argument_checks(lib):
     assert call_sample(ws_bytes=need - 1) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_lazy_sample_shares_the_argument_checks(lib):
+    f = sv.spec_verify_sample_lazy
+    ok = dict(t=FAKE, d=FAKE, dt=sv.SPEC_DTYPE_BF16, x=FAKE, u=FAKE, T=1.0, B=2, g=3, V=100,
+              tok=FAKE, acc=FAKE, lp=None, ws=WS, wb=1 << 24)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["t"], a["d"], a["dt"], a["x"], a["u"], a["T"], a["B"], a["g"], a["V"], a["tok"],
+                 a["acc"], a["lp"], a["ws"], a["wb"], None)
+    assert call(dt=3) == sv.SPEC_ERR_UNSUPPORTED_DTYPE
+    assert call(g=300) == sv.SPEC_ERR_INVALID_ARG
+    assert call(T=0.0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(u=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(x=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(t=FAKE + 2) == sv.SPEC_ERR_MISALIGNED
+    assert call(wb=16) == sv.SPEC_ERR_WORKSPACE_TOO_SMALL
+    assert call(B=0) == sv.SPEC_OK
+
+
 def test_topk_argument_checks(lib):
     k = sv.spec_topk_exclude
     need = sv.spec_topk_workspace_size(3, 100, 4)
