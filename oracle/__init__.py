@@ -52,6 +52,8 @@ def _load():
             lib.oracle_verify_tree_greedy.restype = I
             lib.oracle_topk_exclude.argtypes = [P, P, I, I, I, P, P, I]
             lib.oracle_topk_exclude.restype = I
+            lib.oracle_ngram_retrieve.argtypes = [P, P, I, I, I, I, I, P, P, P, I]
+            lib.oracle_ngram_retrieve.restype = I
             lib.oracle_softmax_row.argtypes = [P, I, ctypes.c_double, P]
             lib.oracle_softmax_row.restype = I
             _lib = lib
@@ -144,6 +146,24 @@ def topk_exclude(logits, K, exclude=None, *, nthreads=0):
     if rc < 0:
         raise ValueError("oracle_topk_exclude: invalid arguments")
     return {"idx": out_i, "val": out_v}
+
+
+def ngram_retrieve(tokens, lengths, w, L, max_matches, *, nthreads=0):
+    """Lexical retrieval per sequence: match count, the first max_matches match
+    positions (ascending, -1 padded) and the draft after the last match."""
+    lib = _load()
+    tokens = _i32(tokens)
+    B, n_max = tokens.shape
+    lengths = _i32(lengths)
+    cnt = np.empty((B,), np.int32)
+    mat = np.empty((B, max_matches), np.int32)
+    dr = np.empty((B, L), np.int32)
+    bad = lib.oracle_ngram_retrieve(_ptr(tokens), _ptr(lengths), B, n_max, int(w), int(L),
+                                    int(max_matches), _ptr(cnt), _ptr(mat), _ptr(dr),
+                                    int(nthreads))
+    if bad < 0:
+        raise ValueError("oracle_ngram_retrieve: invalid arguments")
+    return {"count": cnt, "matches": mat, "draft": dr, "bad": bad}
 
 
 def softmax_row(z, T):

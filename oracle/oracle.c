@@ -358,3 +358,49 @@ int oracle_topk_exclude(const float* logits, const int32_t* exclude, int R, int 
     }
     return 0;
 }
+
+/* ---- lexical (n-gram) retrieval -------------------------------------------- */
+/* [AdaPLD] 3.2: the candidates are every earlier position where the most
+ * recent token occurs with the preceding tokens matching too (a window of w
+ * tokens equal to the query); 3.3: the main draft copies the span after the
+ * chosen position.  Plain loops over positions and window offsets. */
+int oracle_ngram_retrieve(const int32_t* tokens, const int32_t* lengths, int B, int n_max, int w,
+                          int L, int max_matches, int32_t* out_count, int32_t* out_matches,
+                          int32_t* out_draft, int nthreads) {
+    if (B < 0 || n_max <= 0 || w < 1 || w > 8 || L < 0 || max_matches < 0) return -1;
+    if (B == 0) return 0;
+    if (!tokens || !lengths || !out_count) return -1;
+    int bad = 0;
+    int nt = threads_for(nthreads);
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1) reduction(+ : bad)
+    for (int b = 0; b < B; ++b) {
+        const int32_t* t = tokens + (size_t)b * (size_t)n_max;
+        const int n = lengths[b];
+        int32_t* om = out_matches ? out_matches + (size_t)b * (size_t)max_matches : NULL;
+        int32_t* od = out_draft ? out_draft + (size_t)b * (size_t)L : NULL;
+        for (int k = 0; k < max_matches && om; ++k) om[k] = -1;
+        for (int k = 0; k < L && od; ++k) od[k] = -1;
+        if (n < 1 || n > n_max) {
+            out_count[b] = -1;
+            bad += 1;
+            continue;
+        }
+        int count = 0, last = -1;
+        if (n >= w) {
+            const int32_t* q = t + (n - w);               /* the query: the last w tokens */
+            for (int p = w - 1; p <= n - 2; ++p) {
+                int eq = 1;
+                for (int o = 0; o < w; ++o)
+                    if (t[p - w + 1 + o] != q[o]) { eq = 0; break; }
+                if (!eq) continue;
+                if (om && count < max_matches) om[count] = p;
+                ++count;
+                last = p;
+            }
+        }
+        out_count[b] = count;
+        if (od && last >= 0)
+            for (int k = 0; k < L && last + 1 + k <= n - 1; ++k) od[k] = t[last + 1 + k];
+    }
+    return bad;
+}

@@ -99,6 +99,26 @@ int oracle_verify_tree_greedy(const float* target, const int32_t* tokens, const 
 int oracle_topk_exclude(const float* logits, const int32_t* exclude, int R, int V, int K,
                         int32_t* out_idx, float* out_val, int nthreads);
 
+/*
+ * Lexical retrieval of a reuse position ([AdaPLD] 3.2 "lexical retrieval
+ * stage", 3.3 "strict hit path", Algorithm 1 LexicalRetrieval and d_main).
+ * Sequence b's context is tokens[b, 0..len[b]-1]; its query is its last w
+ * tokens.  A match is a position p <= len[b]-2 whose window
+ * tokens[p-w+1..p] equals the query (p >= w-1).
+ *   tokens      [B, n_max] int32 context streams (entries past len[b] ignored)
+ *   lengths     [B] context lengths, 1..n_max
+ *   out_count   [B] number of matches
+ *   out_matches [B, max_matches] the first max_matches match positions in
+ *               ascending order, then -1
+ *   out_draft   [B, L] the continuation after the most recent match p*:
+ *               tokens[p*+1 .. min(p*+L, len[b]-1)], then -1 (all -1 when
+ *               there is no match)
+ * 1 <= w <= 8.
+ */
+int oracle_ngram_retrieve(const int32_t* tokens, const int32_t* lengths, int B, int n_max, int w,
+                          int L, int max_matches, int32_t* out_count, int32_t* out_matches,
+                          int32_t* out_draft, int nthreads);
+
 /* Temperature softmax of one row, p_j = exp(z_j/T - lse), in double. */
 int oracle_softmax_row(const float* z, int V, double T, double* out_p);
 

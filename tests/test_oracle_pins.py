@@ -573,3 +573,44 @@ def test_topk_signed_zero_and_masked_rows():
     assert got[0].tolist() == [0, 1, 2]        # -0.0 == +0.0: lower index first
     assert got[1].tolist() == [0, 2, -1]       # all masked: index order, 1 excluded
     assert got[2].tolist() == [2, 3, -1]       # 0 excluded from [0, 2, 3]
+
+
+# ----------------------------------------------------- lexical (n-gram) retrieval
+def test_ngram_hand_worked():
+    # a b c a b c a b (a=1, b=2, c=3); query = last 2 tokens (a, b)
+    t = np.array([[1, 2, 3, 1, 2, 3, 1, 2]], np.int32)
+    r = oracle.ngram_retrieve(t, [8], w=2, L=3, max_matches=4)
+    assert r["count"][0] == 2
+    assert r["matches"][0].tolist() == [1, 4, -1, -1]     # windows (0,1) and (3,4); (6,7) is the query
+    assert r["draft"][0].tolist() == [3, 1, 2]            # after p* = 4
+    r = oracle.ngram_retrieve(t, [8], w=3, L=5, max_matches=1)
+    assert r["count"][0] == 1 and r["matches"][0].tolist() == [4]   # (c, a, b) ends at 4 only
+    assert r["draft"][0].tolist() == [3, 1, 2, -1, -1]   # clipped at the end of the context
+    r = oracle.ngram_retrieve(t, [5], w=2, L=2, max_matches=2)      # context a b c a b
+    assert r["count"][0] == 1 and r["draft"][0].tolist() == [3, 1]
+
+
+def _ngram_brute(t, n, w, L, cap):
+    q = list(t[n - w:n]) if n >= w else None
+    ms = [p for p in range(w - 1, n - 1) if q is not None and list(t[p - w + 1:p + 1]) == q]
+    draft = [-1] * L
+    if ms:
+        p = ms[-1]
+        cont = list(t[p + 1:min(p + L, n - 1) + 1])
+        draft = cont + [-1] * (L - len(cont))
+    return len(ms), (ms[:cap] + [-1] * cap)[:cap], draft
+
+
+@pytest.mark.parametrize("w", [1, 2, 3, 5, 8])
+def test_ngram_matches_brute_force(w):
+    rng = np.random.default_rng(w)
+    B, n_max = 30, 300
+    t = rng.integers(0, 4, size=(B, n_max)).astype(np.int32)   # 4-token alphabet: many matches
+    lengths = rng.integers(1, n_max + 1, size=B).astype(np.int32)
+    lengths[0], lengths[1] = 1, w                                # no room for a match
+    r = oracle.ngram_retrieve(t, lengths, w=w, L=6, max_matches=7)
+    for b in range(B):
+        cnt, ms, dr = _ngram_brute(t[b], int(lengths[b]), w, 6, 7)
+        assert r["count"][b] == cnt
+        assert r["matches"][b].tolist() == ms
+        assert r["draft"][b].tolist() == dr
