@@ -219,6 +219,34 @@ spec_status_t spec_topk_exclude(const void* logits, spec_dtype_t dtype, int rows
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Lexical retrieval of a reuse position ([AdaPLD] 3.2 "lexical retrieval
+ * stage", 3.3 "strict hit path", Algorithm 1 LexicalRetrieval and d_main):
+ * sequence b's context is tokens[b, 0 .. lengths[b]-1] and its query its last
+ * w tokens.  A match is a position p with w-1 <= p <= lengths[b]-2 whose
+ * window tokens[b, p-w+1 .. p] equals the query.  The pages choose among the
+ * matches by hidden-state similarity; here the most recent match p* is the
+ * reuse position.
+ *   tokens      [B, n_max] int32, 16-byte aligned, n_max a multiple of 4;
+ *               entries at or past lengths[b] are ignored
+ *   lengths     [B] int32 in 1..n_max (device); another value marks the
+ *               sequence bad: out_count -1, every output -1, error bit
+ *               SPEC_DEVERR_TOKEN_RANGE
+ *   out_count   [B]: number of matches
+ *   out_matches [B, max_matches]: the first max_matches match positions in
+ *               ascending order, then -1
+ *   out_draft   [B, L] (NULL: not written): tokens[b, p*+1 .. min(p*+L,
+ *               lengths[b]-1)], then -1; all -1 without a match
+ * 1 <= w <= 8, 0 <= L <= 1024, 1 <= max_matches <= 4096.  Workspace:
+ * spec_ngram_workspace_size(B, n_max, max_matches) bytes, 256-byte aligned,
+ * first 256 bytes zero-filled once (the error word).
+ */
+size_t spec_ngram_workspace_size(int B, int n_max, int max_matches);
+spec_status_t spec_ngram_retrieve(const int32_t* tokens, const int32_t* lengths, int B, int n_max,
+                                  int w, int L, int max_matches, int32_t* out_count,
+                                  int32_t* out_matches, int32_t* out_draft, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.
  *
  * The source pages have no counterpart to this call; it exists for callers

@@ -60,6 +60,8 @@ SIGNATURES = {
     "spec_verify_tree_greedy": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
     "spec_topk_workspace_size": ([_I, _I, _I], _S),
     "spec_topk_exclude": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
+    "spec_ngram_workspace_size": ([_I, _I, _I], _S),
+    "spec_ngram_retrieve": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
     "spec_verify_read_error": ([_P, _P, _P], _I),
     "spec_verify_status_string": ([_I], ctypes.c_char_p),
 }
@@ -104,6 +106,17 @@ def spec_topk_exclude(logits, dtype, rows, V, K, exclude, out_idx, out_val, ws, 
                       stream) -> int:
     return load_library().spec_topk_exclude(logits, dtype, rows, V, K, exclude, out_idx, out_val,
                                             ws, ws_bytes, stream)
+
+
+def spec_ngram_workspace_size(B: int, n_max: int, max_matches: int) -> int:
+    return load_library().spec_ngram_workspace_size(B, n_max, max_matches)
+
+
+def spec_ngram_retrieve(tokens, lengths, B, n_max, w, L, max_matches, out_count, out_matches,
+                        out_draft, ws, ws_bytes, stream) -> int:
+    return load_library().spec_ngram_retrieve(tokens, lengths, B, n_max, w, L, max_matches,
+                                              out_count, out_matches, out_draft, ws, ws_bytes,
+                                              stream)
 
 
 def spec_verify_workspace_init(ws: int, nbytes: int, stream: int = 0) -> int:
@@ -292,6 +305,25 @@ def topk_exclude(logits, K: int, exclude=None, *, values=False,
                            _ptr(val), wp, wb, _stream(stream))
     _check(st, "spec_topk_exclude")
     return (idx, val) if values else idx
+
+
+def ngram_retrieve(tokens, lengths, w: int, L: int, max_matches: int, *,
+                   workspace: Optional[Workspace] = None, stream=None):
+    """Lexical retrieval (see spec_ngram_retrieve).  tokens [B, n_max] int32
+    (n_max a multiple of 4), lengths [B] int32, CUDA tensors.  Returns
+    (count [B], matches [B, max_matches], draft [B, L])."""
+    torch = _torch()
+    B, n_max = tokens.shape
+    dev = tokens.device
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    mat = torch.empty((B, max_matches), dtype=torch.int32, device=dev)
+    dr = torch.empty((B, max(L, 1)), dtype=torch.int32, device=dev)
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get_bytes(spec_ngram_workspace_size(B, n_max, max_matches), stream)
+    st = spec_ngram_retrieve(_ptr(tokens), _ptr(lengths), B, n_max, w, L, max_matches, _ptr(cnt),
+                             _ptr(mat), _ptr(dr), wp, wb, _stream(stream))
+    _check(st, "spec_ngram_retrieve")
+    return cnt, mat, dr[:, :L]
 
 
 def verify_greedy(target, draft_tokens, *, workspace: Optional[Workspace] = None, out=None,

@@ -180,6 +180,29 @@ spec_status_t spec_topk_exclude(const void* logits, spec_dtype_t dtype, int rows
                                  stream));
 }
 
+size_t spec_ngram_workspace_size(int B, int n_max, int max_matches) {
+    if (B < 0 || n_max < 4 || n_max % 4 != 0 || max_matches < 1 || max_matches > 4096) return 0;
+    return ngram_workspace_size(B, n_max, max_matches);
+}
+
+spec_status_t spec_ngram_retrieve(const int32_t* tokens, const int32_t* lengths, int B, int n_max,
+                                  int w, int L, int max_matches, int32_t* out_count,
+                                  int32_t* out_matches, int32_t* out_draft, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    if (B < 0 || n_max < 4 || w < 1 || w > 8 || L < 0 || L > 1024 || max_matches < 1 ||
+        max_matches > 4096)
+        return SPEC_ERR_INVALID_ARG;
+    if (n_max % 4 != 0) return SPEC_ERR_MISALIGNED;
+    if (B == 0) return SPEC_OK;
+    if (!tokens || !lengths || !out_count || !out_matches || !workspace) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(tokens, 16)) return SPEC_ERR_MISALIGNED;
+    if (!aligned(workspace, 256)) return SPEC_ERR_MISALIGNED;
+    if (workspace_bytes < ngram_workspace_size(B, n_max, max_matches))
+        return SPEC_ERR_WORKSPACE_TOO_SMALL;
+    return to_status(launch_ngram(tokens, lengths, B, n_max, w, L, max_matches, out_count,
+                                  out_matches, out_draft, workspace, stream));
+}
+
 spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32_t* code) {
     if (!workspace || !code) return SPEC_ERR_INVALID_ARG;
     int32_t v = 0;

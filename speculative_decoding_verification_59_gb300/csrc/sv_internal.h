@@ -105,4 +105,10 @@ cudaError_t launch_topk(const void* logits, spec_dtype_t dt, int rows, int V, in
 size_t topk_workspace_size(int rows, int V, int K);
 int topk_list_len(int K);
 
+// Lexical (n-gram) retrieval of reuse positions over B token streams.
+cudaError_t launch_ngram(const int32_t* tokens, const int32_t* lengths, int B, int n_max, int w,
+                         int L, int max_matches, int32_t* out_count, int32_t* out_matches,
+                         int32_t* out_draft, void* ws, cudaStream_t st);
+size_t ngram_workspace_size(int B, int n_max, int max_matches);
+
 }  // namespace sv

@@ -25,6 +25,12 @@ Workloads (B sequences, gamma drafts, V vocabulary, T temperature):
                                                of depths 1..7, node token = argmax of the parent's
                                                row with probability 0.7, seed 4
 
+  ngram-b64     B=64  token streams of 32768..65536 tokens (n_max 65536), V=151936: Zipf-like
+                tokens with repeated spans (a block copies an earlier span with
+                probability 0.35), the last 32 tokens copied from earlier in the
+                stream for 70% of the sequences (a lexical hit), query w=3,
+                draft L=7, up to 64 matches kept, seed 5
+
 The vocabulary 151936 is Qwen3's and gamma=7 matches the K=7 of the DLite
 reading notes (section "Experimental setup").  Every workload can be shrunk
 (B, gamma, V overrides) with the same recipe for parity tests.
@@ -37,7 +43,8 @@ from typing import Optional
 import numpy as np
 
 __all__ = [
-    "WORKLOADS", "ChainInputs", "TreeInputs", "make_chain", "make_tree",
+    "WORKLOADS", "ChainInputs", "TreeInputs", "NgramInputs", "make_chain", "make_tree",
+    "make_ngram",
     "tree_topology", "to_bf16_exact", "gumbel_argmax",
 ]
 
@@ -69,6 +76,21 @@ class TreeWorkload:
     match_prob: float
 
 
+@dataclasses.dataclass(frozen=True)
+class NgramWorkload:
+    name: str
+    B: int
+    n_max: int
+    n_min: int
+    V: int
+    w: int
+    L: int
+    max_matches: int
+    seed: int
+    copy_prob: float     # a block repeats an earlier span
+    hit_prob: float      # the stream ends with a copied span
+
+
 WORKLOADS = {
     "chain-small": ChainWorkload("chain-small", 1, 4, 1000, "f32", 1.0, 0, "gauss", 2.0, (0.5,)),
     "chain-b8": ChainWorkload("chain-b8", 8, 7, 151936, "bf16", 1.0, 1, "boosted", 3.0, (1.0,)),
@@ -76,7 +98,59 @@ WORKLOADS = {
                                (0.25, 1.0, 4.0)),
     "chain-b256": ChainWorkload("chain-b256", 256, 4, 128256, "f32", 1.0, 3, "mixed", 2.5, (2.5,)),
     "tree-b32": TreeWorkload("tree-b32", 32, 36, 151936, "bf16", 4, 7, 4, 0.7),
+    "ngram-b64": NgramWorkload("ngram-b64", 64, 65536, 32768, 151936, 3, 7, 64, 5, 0.35, 0.7),
 }
+
+
+@dataclasses.dataclass
+class NgramInputs:
+    tokens: np.ndarray     # [B, n_max] int32 (zero past each length)
+    lengths: np.ndarray    # [B] int32
+    w: int
+    L: int
+    max_matches: int
+    name: str
+
+
+def make_ngram(name: str = "ngram-b64", *, B: Optional[int] = None, n_max: Optional[int] = None,
+               n_min: Optional[int] = None, seed: Optional[int] = None) -> NgramInputs:
+    """Token streams for lexical retrieval: Zipf-like tokens (80% from 2000
+    frequent ids, 20% uniform over V) in blocks of 64..512 tokens, each block
+    copying an earlier span of the same stream with probability copy_prob;
+    with probability hit_prob the stream ends with a 32-token copy of an
+    earlier span, so its last w tokens occur earlier."""
+    wl = WORKLOADS[name]
+    assert isinstance(wl, NgramWorkload), name
+    B = wl.B if B is None else B
+    n_max = wl.n_max if n_max is None else n_max
+    n_min = min(wl.n_min, n_max) if n_min is None else n_min
+    seed = wl.seed if seed is None else seed
+    ss = np.random.SeedSequence(seed).spawn(3)
+    r_len, r_tok, r_blk = (np.random.default_rng(x) for x in ss)
+    lengths = r_len.integers(n_min, n_max + 1, size=B).astype(np.int32)
+    freq = (r_tok.permutation(wl.V)[:2000]).astype(np.int32)
+    ranks = 1.0 / np.arange(1, 2001) ** 1.1
+    ranks /= ranks.sum()
+    tokens = np.zeros((B, n_max), np.int32)
+    for b in range(B):
+        n = int(lengths[b])
+        out = np.empty(n, np.int32)
+        pos = 0
+        while pos < n:
+            blk = min(int(r_blk.integers(64, 513)), n - pos)
+            if pos > blk and r_blk.random() < wl.copy_prob:
+                src = int(r_blk.integers(0, pos - blk + 1))
+                out[pos:pos + blk] = out[src:src + blk]
+            else:
+                fr = r_tok.random(blk) < 0.8
+                out[pos:pos + blk] = np.where(fr, freq[r_tok.choice(2000, blk, p=ranks)],
+                                              r_tok.integers(0, wl.V, blk)).astype(np.int32)
+            pos += blk
+        if n > 128 and r_blk.random() < wl.hit_prob:
+            src = int(r_blk.integers(0, n - 64))
+            out[n - 32:] = out[src:src + 32]
+        tokens[b, :n] = out
+    return NgramInputs(tokens, lengths, wl.w, wl.L, wl.max_matches, name)
 
 BOOSTED_PER_ROW = 20
 BOOST = 8.0

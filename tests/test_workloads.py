@@ -78,3 +78,14 @@ def test_tree_match_rate():
                       for b in range(t.B)])
     assert abs(match.mean() - 0.7) < 0.06
     assert (t.node_tokens[:, 0] == -1).all()
+
+
+def test_ngram_streams_shape_determinism_and_hits():
+    g1 = W.make_ngram("ngram-b64", B=16, n_max=8192, n_min=2048)
+    g2 = W.make_ngram("ngram-b64", B=16, n_max=8192, n_min=2048)
+    assert g1.tokens.shape == (16, 8192) and g1.tokens.dtype == np.int32
+    assert np.array_equal(g1.tokens, g2.tokens) and np.array_equal(g1.lengths, g2.lengths)
+    assert ((g1.lengths >= 2048) & (g1.lengths <= 8192)).all()
+    for b in range(16):
+        assert (g1.tokens[b, g1.lengths[b]:] == 0).all()
+        assert ((g1.tokens[b] >= 0) & (g1.tokens[b] < 151936)).all()
