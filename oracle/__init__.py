@@ -166,6 +166,38 @@ def ngram_retrieve(tokens, lengths, w, L, max_matches, *, nthreads=0):
     return {"count": cnt, "matches": mat, "draft": dr, "bad": bad}
 
 
+def cosine_topk(hidden, query, delta, positions=None):
+    """Semantic fallback of AdaPLD (section 3.2, "semantic fallback stage";
+    Algorithm 1, SemanticFallback): score(j) = h_current . h_j /
+    (|h_current| |h_j|) over the window rows h_j of each sequence, in fp64
+    (0 when either norm is 0), then the delta largest scores, larger first,
+    lower window index first among equal scores.  hidden [B, W, d], query
+    [B, d] (float32 arrays holding the exact input values); positions [B, W]
+    maps window rows to context positions (None: the window index itself).
+    Returns idx [B, delta] (window rows), pos [B, delta], score [B, delta]
+    and all scores [B, W]."""
+    H = np.asarray(hidden, dtype=np.float64)
+    q = np.asarray(query, dtype=np.float64)
+    B, W, d = H.shape
+    dots = np.einsum("bwd,bd->bw", H, q)
+    nh = np.sqrt(np.einsum("bwd,bwd->bw", H, H))
+    nq = np.sqrt(np.einsum("bd,bd->b", q, q))
+    den = nh * nq[:, None]
+    scores = np.where(den > 0, dots / np.where(den > 0, den, 1.0), 0.0)
+    idx = np.full((B, delta), -1, np.int32)
+    sc = np.full((B, delta), -np.inf)
+    for b in range(B):
+        order = np.lexsort((np.arange(W), -scores[b]))[:delta]
+        idx[b, :len(order)] = order
+        sc[b, :len(order)] = scores[b, order]
+    if positions is None:
+        pos = idx.copy()
+    else:
+        P = np.asarray(positions, dtype=np.int32)
+        pos = np.where(idx >= 0, np.take_along_axis(P, np.maximum(idx, 0), axis=1), -1)
+    return {"idx": idx, "pos": pos.astype(np.int32), "score": sc, "scores": scores}
+
+
 def softmax_row(z, T):
     lib = _load()
     z = _f32(z)

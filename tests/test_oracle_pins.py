@@ -614,3 +614,34 @@ def test_ngram_matches_brute_force(w):
         assert r["count"][b] == cnt
         assert r["matches"][b].tolist() == ms
         assert r["draft"][b].tolist() == dr
+
+
+# ------------------------------------------------ semantic fallback (cosine)
+def test_cosine_special_vectors():
+    q = np.array([[1.0, 2.0, -2.0, 0.5]], np.float32)
+    H = np.stack([q[0], -q[0], 3 * q[0], np.array([2.0, -1.0, 0.0, 0.0], np.float32),
+                  np.zeros(4, np.float32)])[None]
+    r = oracle.cosine_topk(H, q, 5)
+    s = r["scores"][0]
+    assert s[0] == pytest.approx(1.0, abs=1e-15)      # identical
+    assert s[1] == pytest.approx(-1.0, abs=1e-15)     # opposite
+    assert s[2] == pytest.approx(1.0, abs=1e-15)      # scale does not matter
+    assert s[3] == pytest.approx(0.0, abs=1e-15)      # orthogonal
+    assert s[4] == 0.0                                # zero row scores 0
+    assert r["idx"][0].tolist() == [0, 2, 3, 4, 1]    # ties: lower index first
+
+
+def test_cosine_matches_scipy_distance():
+    from scipy.spatial.distance import cdist
+    rng = np.random.default_rng(3)
+    B, W, d = 5, 37, 64
+    H = rng.standard_normal((B, W, d)).astype(np.float32)
+    q = rng.standard_normal((B, d)).astype(np.float32)
+    pos = rng.integers(0, 10**6, size=(B, W)).astype(np.int32)
+    r = oracle.cosine_topk(H, q, 6, positions=pos)
+    for b in range(B):
+        want = 1.0 - cdist(q[b:b + 1].astype(np.float64), H[b].astype(np.float64), "cosine")[0]
+        assert np.allclose(r["scores"][b], want, rtol=0, atol=1e-12)
+        top = sorted(range(W), key=lambda j: (-want[j], j))[:6]
+        assert r["idx"][b].tolist() == top
+        assert r["pos"][b].tolist() == [int(pos[b, j]) for j in top]
