@@ -340,7 +340,9 @@ def run_own(args):
              "lazy_sample": time_lazy(sv, torch, copies, x, stream, sh, nx, max_over_ranks, world,
                                       dev, acct),
              "ngram_b64": time_ngram(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev,
-                                     rank)}
+                                     rank),
+             "cosine_b64": time_cosine(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev,
+                                       rank)}
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
@@ -491,6 +493,47 @@ def time_ngram(sv, torch, W, stream, sh, steps, max_over_ranks, world, dev, rank
             "tokens_per_s": world * ntok / (ms * 1e-3),
             "bytes_per_call": 4 * ntok, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak,
             "l2": "8 rotating input copies, 134 MB in all (> L2)", "gpu_launches_per_call": 2}
+
+
+def time_cosine(sv, torch, W, stream, sh, steps, max_over_ranks, world, dev, rank):
+    """Semantic fallback over the cosine-b64 windows (64 sequences x 240
+    hidden states x 4096, bf16, delta 4): every window row is read once.
+    Two input copies of 126 MB rotate (252 MB, more than the 129 MB L2)."""
+    c = W.make_cosine("cosine-b64", seed=W.WORKLOADS["cosine-b64"].seed + 1000 * rank)
+    B, Wn, d = c.hidden.shape
+    hs = [torch.from_numpy(c.hidden).to(dev).to(torch.bfloat16) for _ in range(2)]
+    qs = torch.from_numpy(c.query).to(dev).to(torch.bfloat16)
+    pos = torch.from_numpy(c.positions).to(dev)
+    idx = torch.empty((B, c.delta), dtype=torch.int32, device=dev)
+    out_pos = torch.empty((B, c.delta), dtype=torch.int32, device=dev)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get_bytes(sv.spec_cosine_workspace_size(B, Wn))
+
+    def call(h):
+        st = sv.spec_cosine_topk(h.data_ptr(), qs.data_ptr(), sv.SPEC_DTYPE_BF16, B, Wn, d, c.delta,
+                                 pos.data_ptr(), idx.data_ptr(), out_pos.data_ptr(), None, wp, wb, sh)
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, "cosine")
+
+    for s in range(5):
+        call(hs[s % 2])
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        call(hs[s % 2])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+    nbytes = B * Wn * d * 2 + B * d * 2
+    peak, src = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del hs
+    return {"what": "cosine top-4 over 64 windows of 240 x 4096 bf16 hidden states",
+            "ms_per_call": ms, "calls": steps, "rows_per_s": world * B * Wn / (ms * 1e-3),
+            "bytes_per_call": nbytes, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+            "peak_source": src, "l2": "2 rotating input copies, 252 MB in all (> L2)",
+            "gpu_launches_per_call": 2}
 
 
 def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, dev, acct):

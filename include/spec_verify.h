@@ -247,6 +247,30 @@ spec_status_t spec_ngram_retrieve(const int32_t* tokens, const int32_t* lengths,
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Semantic fallback of the reuse-position search ([AdaPLD] 3.2 "semantic
+ * fallback stage", Algorithm 1 SemanticFallback): for each sequence b,
+ * score(j) = h . H_j / (|h| |H_j|) over its window of W hidden states (the
+ * states of the most recent forward steps), then the delta largest scores,
+ * larger first, lower window index first among equal scores.  A zero norm
+ * gives score 0.  Scores are accumulated in fp32 (|error| ~1e-6).
+ *   hidden     [B, W, d] bf16 or fp32, 16-byte aligned, d a multiple of 8
+ *              (bf16) or 4 (fp32)
+ *   query      [B, d] same dtype, 16-byte aligned
+ *   positions  [B, W] int32 (NULL: the window index): the context position of
+ *              each window row
+ *   out_idx    [B, delta] window rows, -1 padded when W < delta
+ *   out_pos    [B, delta] (NULL: not written) their positions, -1 padded
+ *   out_score  [B, delta] (NULL: not written) their scores, -inf padded
+ * 1 <= delta <= 8, W >= 1.  Workspace: spec_cosine_workspace_size(B, W)
+ * bytes, 256-byte aligned.
+ */
+size_t spec_cosine_workspace_size(int B, int W);
+spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype_t dtype, int B,
+                               int W, int d, int delta, const int32_t* positions,
+                               int32_t* out_idx, int32_t* out_pos, float* out_score,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.
  *
  * The source pages have no counterpart to this call; it exists for callers

@@ -62,6 +62,8 @@ SIGNATURES = {
     "spec_topk_exclude": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
     "spec_ngram_workspace_size": ([_I, _I, _I], _S),
     "spec_ngram_retrieve": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P], _I),
+    "spec_cosine_workspace_size": ([_I, _I], _S),
+    "spec_cosine_topk": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P], _I),
     "spec_verify_read_error": ([_P, _P, _P], _I),
     "spec_verify_status_string": ([_I], ctypes.c_char_p),
 }
@@ -117,6 +119,16 @@ def spec_ngram_retrieve(tokens, lengths, B, n_max, w, L, max_matches, out_count,
     return load_library().spec_ngram_retrieve(tokens, lengths, B, n_max, w, L, max_matches,
                                               out_count, out_matches, out_draft, ws, ws_bytes,
                                               stream)
+
+
+def spec_cosine_workspace_size(B: int, W: int) -> int:
+    return load_library().spec_cosine_workspace_size(B, W)
+
+
+def spec_cosine_topk(hidden, query, dtype, B, W, d, delta, positions, out_idx, out_pos, out_score,
+                     ws, ws_bytes, stream) -> int:
+    return load_library().spec_cosine_topk(hidden, query, dtype, B, W, d, delta, positions,
+                                           out_idx, out_pos, out_score, ws, ws_bytes, stream)
 
 
 def spec_verify_workspace_init(ws: int, nbytes: int, stream: int = 0) -> int:
@@ -324,6 +336,25 @@ def ngram_retrieve(tokens, lengths, w: int, L: int, max_matches: int, *,
                              _ptr(mat), _ptr(dr), wp, wb, _stream(stream))
     _check(st, "spec_ngram_retrieve")
     return cnt, mat, dr[:, :L]
+
+
+def cosine_topk(hidden, query, delta: int, positions=None, *,
+                workspace: Optional[Workspace] = None, stream=None):
+    """Semantic fallback (see spec_cosine_topk).  hidden [B, W, d], query
+    [B, d] (same dtype, bf16 or fp32), positions [B, W] int32 or None, CUDA
+    tensors.  Returns (idx [B, delta], pos [B, delta], score [B, delta])."""
+    torch = _torch()
+    B, W, d = hidden.shape
+    dev = hidden.device
+    idx = torch.empty((B, delta), dtype=torch.int32, device=dev)
+    pos = torch.empty((B, delta), dtype=torch.int32, device=dev)
+    sc = torch.empty((B, delta), dtype=torch.float32, device=dev)
+    ws = _ws(workspace, dev)
+    wp, wb = ws.get_bytes(spec_cosine_workspace_size(B, W), stream)
+    st = spec_cosine_topk(_ptr(hidden), _ptr(query), _dtype_code(hidden), B, W, d, delta,
+                          _ptr(positions), _ptr(idx), _ptr(pos), _ptr(sc), wp, wb, _stream(stream))
+    _check(st, "spec_cosine_topk")
+    return idx, pos, sc
 
 
 def verify_greedy(target, draft_tokens, *, workspace: Optional[Workspace] = None, out=None,

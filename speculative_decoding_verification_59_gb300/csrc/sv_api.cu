@@ -203,6 +203,27 @@ spec_status_t spec_ngram_retrieve(const int32_t* tokens, const int32_t* lengths,
                                   out_matches, out_draft, workspace, stream));
 }
 
+size_t spec_cosine_workspace_size(int B, int W) {
+    if (B < 0 || W < 1) return 0;
+    return cosine_workspace_size(B, W);
+}
+
+spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype_t dtype, int B,
+                               int W, int d, int delta, const int32_t* positions,
+                               int32_t* out_idx, int32_t* out_pos, float* out_score,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || W < 1 || d < 1 || delta < 1 || delta > 8) return SPEC_ERR_INVALID_ARG;
+    if ((d * elt_size(dtype)) % 16 != 0) return SPEC_ERR_MISALIGNED;
+    if (B == 0) return SPEC_OK;
+    if (!hidden || !query || !out_idx || !workspace) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(query, 16) || !aligned(workspace, 256))
+        return SPEC_ERR_MISALIGNED;
+    if (workspace_bytes < cosine_workspace_size(B, W)) return SPEC_ERR_WORKSPACE_TOO_SMALL;
+    return to_status(launch_cosine(hidden, query, dtype, B, W, d, delta, positions, out_idx,
+                                   out_pos, out_score, workspace, stream));
+}
+
 spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32_t* code) {
     if (!workspace || !code) return SPEC_ERR_INVALID_ARG;
     int32_t v = 0;

@@ -1,0 +1,154 @@
+// Semantic fallback of the reuse-position search: the window rows whose
+// hidden states are most similar (cosine) to the current one.
+//
+// Source: "AdaPLD: adaptive retrieval and reuse for efficient model-free
+// speculative decoding", section 3.2 (semantic fallback stage: when the
+// lexical stage finds nothing, score(j) = h_current . h_j / (|h_current|
+// |h_j|) over the hidden states of a sliding window of the most recent 30
+// forward steps, and the most similar positions are retrieved) and
+// Algorithm 1 (SemanticFallback: top-delta positions).
+//
+// Each window row is read once: one warp per row accumulates h.q, h.h and
+// q.q in fp32 with packed f32x2 FMAs over 16-byte vectors (the query vector
+// comes through L1, shared by the CTA's warps).  A row with a zero norm, or
+// a zero query, scores 0.  One warp per sequence then keeps the delta best
+// scores (larger first, lower window index first among equal scores) and
+// maps them to context positions.  The pass is a batched matrix-vector
+// product, bound by HBM; it has no dense contraction for tensor cores.
+#include "sv_stream.cuh"
+
+namespace sv {
+
+constexpr int kCosThreads = 256;
+constexpr int kCosRowsPerCta = 32;               // 4 rows per warp
+constexpr int kCosBatch = 4;                     // 16-byte vectors in flight per lane
+
+struct CosArgs {
+    const char* H;            // [B, W, d]
+    const char* q;            // [B, d]
+    const int32_t* positions; // [B, W] or null
+    int B, W, d, delta;
+    float* scores;            // [B, W] (workspace)
+    int32_t* out_idx;         // [B, delta]
+    int32_t* out_pos;         // [B, delta] or null
+    float* out_score;         // [B, delta] or null
+};
+
+// Pair i of the values in a 16-byte vector (bfloat16: word i; fp32: words
+// 2i and 2i + 1).
+template <int ELT>
+__device__ __forceinline__ f32x2 vec_pair(const uint4& v, int i) {
+    if constexpr (ELT == 2) {
+        const uint32_t w = u4_get(v, i);
+        return f2_pack(bf16_lo(w), bf16_hi(w));
+    } else {
+        return f2_pack(__uint_as_float(u4_get(v, 2 * i)), __uint_as_float(u4_get(v, 2 * i + 1)));
+    }
+}
+
+template <int ELT>
+__global__ void __launch_bounds__(kCosThreads) cosine_scores_kernel(const CosArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    const int r0 = blockIdx.y * kCosRowsPerCta;
+    const int nvec = a.d * ELT / 16;
+    constexpr int NP = 8 / ELT;                           // pairs per vector
+    const char* qrow = a.q + (size_t)b * a.d * ELT;
+    for (int r = r0 + warp; r < min(r0 + kCosRowsPerCta, a.W); r += kCosThreads / 32) {
+        const char* hrow = a.H + ((size_t)b * a.W + r) * a.d * ELT;
+        f32x2 dot = f2_pack(0.f, 0.f), nh = dot, nq = dot;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * kCosBatch) {
+            uint4 hv[kCosBatch], qv[kCosBatch];
+#pragma unroll
+            for (int u = 0; u < kCosBatch; ++u) {
+                const int v = v0 + 32 * u;
+                hv[u] = v < nvec ? ld_stream16(hrow + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                qv[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(qrow) + v)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kCosBatch; ++u)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const f32x2 h2 = vec_pair<ELT>(hv[u], i), q2 = vec_pair<ELT>(qv[u], i);
+                    dot = f2_fma(h2, q2, dot);
+                    nh = f2_fma(h2, h2, nh);
+                    nq = f2_fma(q2, q2, nq);
+                }
+        }
+        float d0, d1, h0, h1, q0, q1;
+        f2_unpack(dot, d0, d1);
+        f2_unpack(nh, h0, h1);
+        f2_unpack(nq, q0, q1);
+        const float sd = warp_sum(d0 + d1), sh = warp_sum(h0 + h1), sq = warp_sum(q0 + q1);
+        if (lane == 0)
+            a.scores[(size_t)b * a.W + r] = (sh > 0.f && sq > 0.f) ? sd / sqrtf(sh) / sqrtf(sq) : 0.f;
+    }
+}
+
+constexpr int kCosTopWarps = 8;
+
+template <int KC>
+__global__ void __launch_bounds__(kCosTopWarps * 32) cosine_top_kernel(const CosArgs a) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kCosTopWarps + (threadIdx.x >> 5);
+    if (b >= a.B) return;                                 // warp-uniform
+    TopList<KC> L;
+    L.init();
+    for (int j = lane; j < a.W; j += 32) L.insert(__ldcg(a.scores + (size_t)b * a.W + j), j);
+    float ov[KC];
+    int oi[KC];
+    warp_merge_topk<KC>(L, ov, oi);
+    if (lane == 0)
+        for (int k = 0; k < a.delta; ++k) {
+            const bool have = k < KC && oi[k] >= 0 && oi[k] < a.W;
+            const int j = have ? oi[k] : -1;
+            a.out_idx[(size_t)b * a.delta + k] = j;
+            if (a.out_pos)
+                a.out_pos[(size_t)b * a.delta + k] =
+                    have ? (a.positions ? a.positions[(size_t)b * a.W + j] : j) : -1;
+            if (a.out_score) a.out_score[(size_t)b * a.delta + k] = have ? ov[k] : kNegInf;
+        }
+}
+
+size_t cosine_workspace_size(int B, int W) {
+    return 256 + align256(sizeof(float) * (size_t)B * (size_t)W);
+}
+
+cudaError_t launch_cosine(const void* hidden, const void* query, spec_dtype_t dt, int B, int W,
+                          int d, int delta, const int32_t* positions, int32_t* out_idx,
+                          int32_t* out_pos, float* out_score, void* ws, cudaStream_t st) {
+    CosArgs a;
+    a.H = static_cast<const char*>(hidden);
+    a.q = static_cast<const char*>(query);
+    a.positions = positions;
+    a.B = B;
+    a.W = W;
+    a.d = d;
+    a.delta = delta;
+    a.scores = reinterpret_cast<float*>(static_cast<char*>(ws) + 256);
+    a.out_idx = out_idx;
+    a.out_pos = out_pos;
+    a.out_score = out_score;
+    const dim3 grid((unsigned)B, (unsigned)((W + kCosRowsPerCta - 1) / kCosRowsPerCta), 1);
+    if (dt == SPEC_DTYPE_BF16) cosine_scores_kernel<2><<<grid, kCosThreads, 0, st>>>(a);
+    else cosine_scores_kernel<4><<<grid, kCosThreads, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((B + kCosTopWarps - 1) / kCosTopWarps, 1, 1);
+    cfg.blockDim = dim3(kCosTopWarps * 32, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int KC = topk_list_len(delta);
+    if (KC == 2) return cudaLaunchKernelEx(&cfg, cosine_top_kernel<2>, a);
+    if (KC == 4) return cudaLaunchKernelEx(&cfg, cosine_top_kernel<4>, a);
+    return cudaLaunchKernelEx(&cfg, cosine_top_kernel<8>, a);
+}
+
+}  // namespace sv

@@ -111,4 +111,10 @@ cudaError_t launch_ngram(const int32_t* tokens, const int32_t* lengths, int B, i
                          int32_t* out_draft, void* ws, cudaStream_t st);
 size_t ngram_workspace_size(int B, int n_max, int max_matches);
 
+// Cosine top-delta over windows of hidden states (semantic fallback).
+cudaError_t launch_cosine(const void* hidden, const void* query, spec_dtype_t dt, int B, int W,
+                          int d, int delta, const int32_t* positions, int32_t* out_idx,
+                          int32_t* out_pos, float* out_score, void* ws, cudaStream_t st);
+size_t cosine_workspace_size(int B, int W);
+
 }  // namespace sv

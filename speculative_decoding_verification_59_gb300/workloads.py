@@ -31,6 +31,11 @@ Workloads (B sequences, gamma drafts, V vocabulary, T temperature):
                 stream for 70% of the sequences (a lexical hit), query w=3,
                 draft L=7, up to 64 matches kept, seed 5
 
+  cosine-b64    B=64  windows of W=240 hidden states (30 forward steps of 8 positions),
+                d=4096 (Qwen3-8B's hidden size), bf16: N(0,1) rows and query; half
+                the sequences hold 3 near copies of the query (noise sigma 0.2,
+                0.5, 1.0); delta=4, seed 6
+
 The vocabulary 151936 is Qwen3's and gamma=7 matches the K=7 of the DLite
 reading notes (section "Experimental setup").  Every workload can be shrunk
 (B, gamma, V overrides) with the same recipe for parity tests.
@@ -43,8 +48,8 @@ from typing import Optional
 import numpy as np
 
 __all__ = [
-    "WORKLOADS", "ChainInputs", "TreeInputs", "NgramInputs", "make_chain", "make_tree",
-    "make_ngram",
+    "WORKLOADS", "ChainInputs", "TreeInputs", "NgramInputs", "CosineInputs", "make_chain",
+    "make_tree", "make_ngram", "make_cosine",
     "tree_topology", "to_bf16_exact", "gumbel_argmax",
 ]
 
@@ -91,6 +96,17 @@ class NgramWorkload:
     hit_prob: float      # the stream ends with a copied span
 
 
+@dataclasses.dataclass(frozen=True)
+class CosineWorkload:
+    name: str
+    B: int
+    W: int
+    d: int
+    dtype: str
+    delta: int
+    seed: int
+
+
 WORKLOADS = {
     "chain-small": ChainWorkload("chain-small", 1, 4, 1000, "f32", 1.0, 0, "gauss", 2.0, (0.5,)),
     "chain-b8": ChainWorkload("chain-b8", 8, 7, 151936, "bf16", 1.0, 1, "boosted", 3.0, (1.0,)),
@@ -99,7 +115,44 @@ WORKLOADS = {
     "chain-b256": ChainWorkload("chain-b256", 256, 4, 128256, "f32", 1.0, 3, "mixed", 2.5, (2.5,)),
     "tree-b32": TreeWorkload("tree-b32", 32, 36, 151936, "bf16", 4, 7, 4, 0.7),
     "ngram-b64": NgramWorkload("ngram-b64", 64, 65536, 32768, 151936, 3, 7, 64, 5, 0.35, 0.7),
+    "cosine-b64": CosineWorkload("cosine-b64", 64, 240, 4096, "bf16", 4, 6),
 }
+
+
+@dataclasses.dataclass
+class CosineInputs:
+    hidden: np.ndarray     # [B, W, d] float32 (bf16-exact for dtype "bf16")
+    query: np.ndarray      # [B, d]
+    positions: np.ndarray  # [B, W] int32 context positions of the window rows
+    delta: int
+    dtype: str
+    name: str
+
+
+def make_cosine(name: str = "cosine-b64", *, B: Optional[int] = None, W: Optional[int] = None,
+                d: Optional[int] = None, seed: Optional[int] = None) -> CosineInputs:
+    """Windows of hidden states for the semantic fallback: N(0,1) rows and
+    query; every even sequence plants 3 near copies of its query (noise sigma
+    0.2, 0.5, 1.0) at random window rows.  Row j of a window is context
+    position len_b - W + j for a context length len_b in [W, 65536]."""
+    wl = WORKLOADS[name]
+    assert isinstance(wl, CosineWorkload), name
+    B = wl.B if B is None else B
+    W = wl.W if W is None else W
+    d = wl.d if d is None else d
+    seed = wl.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    H = rng.standard_normal((B, W, d), dtype=np.float32)
+    q = rng.standard_normal((B, d), dtype=np.float32)
+    for b in range(0, B, 2):
+        rows = rng.choice(W, size=min(3, W), replace=False)
+        for r, sig in zip(rows, (0.2, 0.5, 1.0)):
+            H[b, r] = q[b] + np.float32(sig) * rng.standard_normal(d, dtype=np.float32)
+    H = _round(H, wl.dtype)
+    q = _round(q, wl.dtype)
+    lens = rng.integers(W, 65537, size=B)
+    pos = (lens[:, None] - W + np.arange(W)[None, :]).astype(np.int32)
+    return CosineInputs(H, q, pos, wl.delta, wl.dtype, name)
 
 
 @dataclasses.dataclass
