@@ -62,8 +62,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Row constants of the fast version.
 struct RowExp {
     f32x2 nm2;         // (-m, -m)
-    f32x2 msh2;        // (ms_hi, ms_hi): m s as float-float (fp32 logits)
-    f32x2 nmsl2;       // (-ms_lo, -ms_lo)
+    f32x2 nmsh2;       // (-ms_hi, -ms_hi): m s as float-float (fp32 logits)
+    f32x2 mslo2;       // (ms_lo, ms_lo)
     float floor;       // logits below this are raised to it
     uint32_t floor2;   // the floor as a packed bfloat16 pair (rounded down)
     float m;
@@ -71,12 +71,12 @@ struct RowExp {
 
 // Packed temperature constants.
 struct ExpK {
-    f32x2 s2, ns2, slo2, ln2_2;
+    f32x2 s2, ns2, slo2, nslo2, ln2_2, nln2_2;
 };
 
 __device__ __forceinline__ ExpK exp_consts(const VerifyArgs& a) {
     return ExpK{f2_pack(a.s, a.s), f2_pack(-a.s, -a.s), f2_pack(a.s_lo, a.s_lo),
-                f2_pack(kLn2, kLn2)};
+                f2_pack(-a.s_lo, -a.s_lo), f2_pack(kLn2, kLn2), f2_pack(-kLn2, -kLn2)};
 }
 
 // Whether a row with maximum m can take the fast version: the floor
@@ -91,8 +91,8 @@ __device__ __forceinline__ RowExp row_exp(float m, const VerifyArgs& a) {
     r.nm2 = f2_pack(-m, -m);
     const float hi = m * a.s;
     const float lo = fmaf(m, a.s, -hi) + m * a.s_lo;
-    r.msh2 = f2_pack(hi, hi);
-    r.nmsl2 = f2_pack(-lo, -lo);
+    r.nmsh2 = f2_pack(-hi, -hi);
+    r.mslo2 = f2_pack(lo, lo);
     r.floor = m - 200.f / a.s;
     // bfloat16 rounding toward -inf: truncate positives, round negatives away from zero
     uint32_t fb = __float_as_uint(r.floor);
@@ -103,30 +103,32 @@ __device__ __forceinline__ RowExp row_exp(float m, const VerifyArgs& a) {
 
 // Fast version for the two bfloat16 logits packed in w.  z - m is exact for
 // bfloat16 values of comparable magnitude, and its product with s splits
-// exactly into x_hi + x_lo through one FMA.
+// exactly into x_hi + x_lo through one FMA: x_hi = d s rounded, then
+// -x_lo = (x_hi - d s) - d s_lo, scaled by -ln 2 into the factor (1 + x_lo ln 2)
+// -- an arrangement without negated operands.
 __device__ __forceinline__ f32x2 exp_pair_bf16(uint32_t w, const RowExp& r, const ExpK& k) {
     asm("max.bf16x2 %0, %0, %1;" : "+r"(w) : "r"(r.floor2));
     const f32x2 d = f2_add(f2_pack(bf16_lo(w), bf16_hi(w)), r.nm2);
-    const f32x2 nxh = f2_mul(d, k.ns2);                   // -x_hi
-    const f32x2 xl = f2_fma(d, k.slo2, f2_fma(d, k.s2, nxh));
+    const f32x2 xh = f2_mul(d, k.s2);
+    const f32x2 nxl = f2_fma(d, k.nslo2, f2_fma(d, k.ns2, xh));   // -x_lo
     float h0, h1;
-    f2_unpack(nxh, h0, h1);
-    const f32x2 c = f2_pack(ex2_approx(-h0), ex2_approx(-h1));
-    return f2_fma(c, f2_mul(xl, k.ln2_2), c);
+    f2_unpack(xh, h0, h1);
+    const f32x2 c = f2_pack(ex2_approx(h0), ex2_approx(h1));
+    return f2_fma(c, f2_mul(nxl, k.nln2_2), c);
 }
 
 // Fast version for two fp32 logits: z s - m s with z s split exactly
 // (TwoProd through an FMA) and m s precomputed as float-float.
 __device__ __forceinline__ f32x2 exp_pair_f32(float z0, float z1, const RowExp& r, const ExpK& k) {
     const f32x2 z = f2_pack(fmaxf(z0, r.floor), fmaxf(z1, r.floor));
-    const f32x2 np = f2_mul(z, k.ns2);                    // -(z s), rounded
-    const f32x2 pe = f2_fma(z, k.s2, np);                 // z s - p, exact
-    const f32x2 nxh = f2_add(np, r.msh2);                 // -x_hi
-    const f32x2 xl = f2_fma(z, k.slo2, f2_add(pe, r.nmsl2));
+    const f32x2 p = f2_mul(z, k.s2);                      // z s, rounded
+    const f32x2 npe = f2_fma(z, k.ns2, p);                // p - z s, exact
+    const f32x2 xh = f2_add(p, r.nmsh2);                  // x_hi = p - (m s)_hi
+    const f32x2 nxl = f2_fma(z, k.nslo2, f2_add(npe, r.mslo2));   // -x_lo
     float h0, h1;
-    f2_unpack(nxh, h0, h1);
-    const f32x2 c = f2_pack(ex2_approx(-h0), ex2_approx(-h1));
-    return f2_fma(c, f2_mul(xl, k.ln2_2), c);
+    f2_unpack(xh, h0, h1);
+    const f32x2 c = f2_pack(ex2_approx(h0), ex2_approx(h1));
+    return f2_fma(c, f2_mul(nxl, k.nln2_2), c);
 }
 
 // Guarded scalar version: any finite m and temperature, -inf logits give 0.
@@ -814,6 +816,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     const double sd = 1.4426950408889634 / (double)T;
     a.s = (float)sd;
     a.s_lo = (float)(sd - (double)a.s);
+
     a.gamma = gamma;
     a.rows_per_seq = 2 * gamma + 1;
     a.V = V;
