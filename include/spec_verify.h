@@ -125,9 +125,10 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
  * round", step 3: the first rejection discards every later draft, so a
  * position's rows are only needed while every earlier draft was accepted).
  * Same arguments, workspace and outputs as spec_verify_sample, with the same
- * tokens and accept counts; only the rows of positions 0..k are read (and
- * target row gamma when every draft is accepted): 2 (k + 1) rows instead of
- * 2 gamma + 1 after a rejection at k.  out_logprobs (nullable) holds the
+ * tokens and accept counts; only the rows of positions 0..min(k + 1, gamma)
+ * are read after a rejection at k (one position of look-ahead: position k+1
+ * streams while position k is decided), all 2 gamma + 1 rows when every
+ * draft is accepted.  out_logprobs (nullable) holds the
  * log-probabilities of positions 0..min(k, gamma - 1); later positions, and
  * every position of a bad sequence, are NaN.  One thread-block cluster per
  * sequence.  Rows whose byte length is not a multiple of 16 take the full

@@ -543,38 +543,69 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
 // Source: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", section "What happens in one round", step 3: drafts are
 // checked left to right and the first rejection discards every later draft.
-// The lazy pass therefore reads position i's two rows only when drafts
-// 0..i-1 were all accepted: one thread-block cluster per sequence streams the
-// rows of one position at a time (target row i and draft row i, target row
-// gamma last), each of its kLazyCluster CTAs taking a fixed share of the block
-// chunks of a row through the same bulk-copy ring and warp_rowstats as the
-// full pass, so the per-warp partials -- and every decision taken from them --
-// are bit-identical to the full pass.  After each position a cluster barrier
-// makes the partials visible; every CTA then merges the two rows and takes
-// the accept decision (the same arithmetic in each CTA, so all agree), and
-// the cluster stops at the first rejection.  Bytes read per sequence:
-// 2 (k + 1) rows after a rejection at k, 2 gamma + 1 when all are accepted.
-// The final sample runs the usual zsum / wsum / search kernels.
+// The lazy pass therefore reads a position's two rows only while the drafts
+// before it are accepted, give or take one position of look-ahead.
+//
+// One thread-block cluster of kLazyCluster CTAs per sequence; each CTA takes
+// a fixed share of the block chunks of every row.  Per CTA:
+//   producer warp   lane 0 copies the CTA's chunks of position p (target row
+//                   p and draft row p; target row gamma last) into the same
+//                   kind of bulk-copy ring as the full pass, but only for
+//                   p <= (last position decided "accept") + 2;
+//   8 consumer warps turn the copied chunks into the full pass's per-warp
+//                   partials (warp_rowstats), position by position, exactly
+//                   the positions the producer issued;
+//   2 decision warps wait until every CTA of the cluster has the partials of
+//                   position j, merge its two rows (merge_row_stats) and take
+//                   the accept decision (accept_draft) -- the same arithmetic
+//                   as the full pass, in every CTA alike, so every decision
+//                   is bit-identical to it and all CTAs agree.
+// The cluster barrier is used split: each role arrives at phase p when its
+// part of position p is done and waits for phase p-1 only before arriving at
+// p, so the streaming of position j+1 overlaps the decision on position j.
+// Rows read per sequence: those of positions 0..min(k+1, gamma) after a
+// rejection at k (2 gamma + 1 when all drafts are accepted).  The final
+// sample runs the usual zsum / wsum / search kernels.
 constexpr int kLazyCluster = 4;
+constexpr int kLazyDecWarps = 2;
+constexpr int kLazyThreads = kRingThreads + 32 * kLazyDecWarps;
+constexpr int kSmemSpinLimit = 1 << 22;
 
 __device__ __forceinline__ unsigned cluster_ctarank() {
     unsigned r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
+__device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The two decision warps only.
+__device__ __forceinline__ void decision_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kLazyDecWarps) : "memory");
+}
+
+// Bounded wait on a condition over shared memory.
+template <typename Pred>
+__device__ __forceinline__ bool smem_wait(Pred pred) {
+    for (int i = 0; i < kSmemSpinLimit; ++i) {
+        if (pred()) return true;
+        __nanosleep(32);
+    }
+    return false;
 }
 
 template <int ELT>
-__global__ void __launch_bounds__(kRingThreads, 2) lazy_sample_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ float sM[2], slnZ[2];
+    __shared__ float sM[2], slnZ[2], s_Mt, s_Md;
     __shared__ float s_lp[kMaxGamma], s_lq[kMaxGamma];
     __shared__ float s_zt[kMaxGamma], s_zd[kMaxGamma];   // z^t_i[x_i], z^d_i[x_i], gathered up front
-    __shared__ int s_stop, s_k, s_bad, s_ok;
+    __shared__ int s_bad, s_ok, s_k;
+    __shared__ volatile int s_limit, s_stop, s_issued, s_pdone;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned rank = cluster_ctarank();
     const int b = blockIdx.x / kLazyCluster;
@@ -596,8 +627,13 @@ __global__ void __launch_bounds__(kRingThreads, 2) lazy_sample_kernel(const Veri
             if (xi < 0 || xi >= a.V) bad = SPEC_DEVERR_TOKEN_RANGE;
         }
         s_bad = bad;
-        s_stop = 0;
         s_ok = 1;
+        s_k = -1;
+        s_Mt = s_Md = 0.f;
+        s_limit = 1;
+        s_stop = 0;
+        s_issued = -1;
+        s_pdone = 0;
     }
     for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
         const int xi = a.x[(size_t)b * a.gamma + i];
@@ -607,31 +643,69 @@ __global__ void __launch_bounds__(kRingThreads, 2) lazy_sample_kernel(const Veri
     }
     __syncthreads();
     pdl_trigger();
-    int k = -1;
-    unsigned issued = 0, it = 0;                          // ring counters, kept across positions
-    bool ok = true;
+    // rows of position p: chunk cc < nmine of target row p, else of draft row p
+    auto row_of = [&](unsigned cc, int p) { return cc < nmine ? p : a.gamma + 1 + p; };
+
     if (!s_bad) {
-        for (int i = 0; i <= a.gamma; ++i) {
-            const unsigned nchunks = (i < a.gamma ? 2u : 1u) * nmine;
-            // rows of position i: j = 0 target row i, j = 1 draft row i
-            auto row_of = [&](unsigned cc) { return cc < nmine ? i : a.gamma + 1 + i; };
-            if (warp == 0) {
+        if (warp == 0) {
+            // ---- producer
+            unsigned issued = 0;
+            bool ok = true;
+            for (int p = 0; p <= a.gamma; ++p) {
+                int go = 0;
                 if (lane == 0) {
-                    for (unsigned cc = 0; cc < nchunks && ok; ++cc, ++issued) {
+                    if (!smem_wait([&] { return s_stop != 0 || p <= s_limit; })) ok = false;
+                    go = ok && !s_stop;
+                    if (go) s_issued = p;
+                    else s_pdone = 1;
+                    __threadfence_block();
+                    const unsigned nchunks = (p < a.gamma ? 2u : 1u) * nmine;
+                    for (unsigned cc = 0; go && cc < nchunks; ++cc, ++issued) {
                         const int st = (int)(issued % kStages);
                         const unsigned use = issued / kStages;
-                        if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) { ok = false; break; }
+                        if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) {
+                            ok = false;
+                            break;
+                        }
                         const int seg = (int)(sg0 + cc % nmine);
                         const size_t off = (size_t)seg * kStageBytes;
                         const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
                         mbar_arrive_expect_tx(&full[st], bytes);
                         bulk_g2s(ring + (size_t)st * kStageBytes,
-                                 sample_row(a, b, row_of(cc), rowbytes) + off, bytes, &full[st]);
+                                 sample_row(a, b, row_of(cc, p), rowbytes) + off, bytes, &full[st]);
                     }
                     if (!ok) s_ok = 0;
                 }
-            } else {
-                const int cw = warp - 1;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) break;
+                if (p > 0) cluster_wait();
+                cluster_arrive();
+            }
+            if (lane == 0) {
+                s_pdone = 1;
+                // copies still in flight must land before the CTA may exit
+                const unsigned first = issued > kStages ? issued - kStages : 0;
+                for (unsigned i = first; i < issued; ++i)
+                    if (!wait_bounded(&full[i % kStages], (i / kStages) & 1u)) {
+                        atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+                        break;
+                    }
+            }
+        } else if (warp <= kWarps) {
+            // ---- consumers: the positions the producer issued, in order
+            const int cw = warp - 1;
+            unsigned it = 0;
+            bool ok = true;
+            for (int p = 0;; ++p) {
+                int have = 0;
+                if (lane == 0) {
+                    const bool w = smem_wait([&] { return s_issued >= p || s_pdone != 0; });
+                    have = w && s_issued >= p;
+                    if (!w) s_ok = 0;
+                }
+                have = __shfl_sync(0xffffffffu, have, 0);
+                if (!have) break;
+                const unsigned nchunks = (p < a.gamma ? 2u : 1u) * nmine;
                 for (unsigned cc = 0; cc < nchunks; ++cc, ++it) {
                     const int st = (int)(it % kStages);
                     if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
@@ -656,70 +730,84 @@ __global__ void __launch_bounds__(kRingThreads, 2) lazy_sample_kernel(const Veri
                     __syncwarp();
                     if (lane == 0) {
                         if (ok) mbar_arrive(&empty[st]);
-                        a.parts[((size_t)b * a.rows_per_seq + row_of(cc)) * P + seg * kWarps + cw] = part;
+                        a.parts[((size_t)b * a.rows_per_seq + row_of(cc, p)) * P + seg * kWarps + cw] = part;
                     }
                 }
                 if (!ok && lane == 0) s_ok = 0;
+                if (p > 0) cluster_wait();
+                cluster_arrive();                         // this CTA's partials of position p are written
             }
-            __syncthreads();
-            cluster_sync_all();                           // every CTA's partials of position i are visible
-            if (warp == 1 || (warp == 2 && i < a.gamma)) {
-                const int j = warp - 1;
-                float M, lnZ;
-                merge_row_stats(a, b, j == 0 ? i : a.gamma + 1 + i, lane, &M, &lnZ);
-                if (lane == 0) { sM[j] = M; slnZ[j] = lnZ; }
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                if (!s_ok) {
-                    atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
-                    s_stop = 1;
-                    s_k = -1;
-                } else if (sM[0] == kNegInf || (i < a.gamma && sM[1] == kNegInf)) {
-                    s_bad = SPEC_DEVERR_EMPTY_ROW;
-                    s_stop = 1;
-                    s_k = -1;
-                } else if (i == a.gamma) {
-                    s_stop = 1;                           // every draft accepted
-                    s_k = a.gamma;
-                } else {
-                    const float lp = row_log_prob(s_zt[i], sM[0], slnZ[0], a);
-                    const float lq = row_log_prob(s_zd[i], sM[1], slnZ[1], a);
-                    s_lp[i] = lp;
-                    s_lq[i] = lq;
-                    if (!accept_draft(lp, lq, a.u[(size_t)b * (a.gamma + 1) + i])) {
-                        s_stop = 1;
-                        s_k = i;
-                    }
+        } else {
+            // ---- decision warps
+            const int dw = warp - (kWarps + 1);
+            for (int j = 0; j <= a.gamma; ++j) {
+                cluster_arrive();
+                cluster_wait();                           // every CTA's partials of position j are visible
+                if (dw == 0 || j < a.gamma) {
+                    float M, lnZ;
+                    merge_row_stats(a, b, dw == 0 ? j : a.gamma + 1 + j, lane, &M, &lnZ);
+                    if (lane == 0) { sM[dw] = M; slnZ[dw] = lnZ; }
                 }
+                decision_sync();
+                if (dw == 0 && lane == 0) {
+                    bool stop = true;
+                    if (!s_ok) {
+                        atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+                        s_k = -1;
+                    } else if (sM[0] == kNegInf || (j < a.gamma && sM[1] == kNegInf)) {
+                        s_bad = SPEC_DEVERR_EMPTY_ROW;
+                        s_k = -1;
+                    } else if (j == a.gamma) {
+                        s_k = a.gamma;                    // every draft accepted
+                    } else {
+                        const float lp = row_log_prob(s_zt[j], sM[0], slnZ[0], a);
+                        const float lq = row_log_prob(s_zd[j], sM[1], slnZ[1], a);
+                        s_lp[j] = lp;
+                        s_lq[j] = lq;
+                        if (accept_draft(lp, lq, a.u[(size_t)b * (a.gamma + 1) + j])) {
+                            stop = false;
+                            s_limit = j + 2;
+                        } else {
+                            s_k = j;
+                        }
+                    }
+                    if (stop) {
+                        s_Mt = sM[0];
+                        s_Md = j < a.gamma ? sM[1] : 0.f;
+                        s_stop = 1;
+                    }
+                    __threadfence_block();
+                }
+                decision_sync();
+                if (s_stop) break;                        // the same in both warps and every CTA
             }
-            __syncthreads();
-            if (s_stop) break;                            // block-uniform, and the same in every CTA
         }
-        k = s_k;
     }
-    if (rank != 0) return;
-    // outputs of the sequence (CTA 0 of the cluster); slot k belongs to the search
+    // ---- outputs of the sequence: the decision warps of CTA 0
+    if (rank != 0 || warp <= kWarps) return;
+    const int t = threadIdx.x - (kWarps + 1) * 32;
+    const int T = 32 * kLazyDecWarps;
+    int k = s_k;
     if (s_bad) {
         k = -1;
-        if (threadIdx.x == 0) atomicOr(a.err, s_bad);
+        if (t == 0) atomicOr(a.err, s_bad);
     }
-    if (threadIdx.x == 0) {
+    if (t == 0) {
         a.out_acc[b] = k;
         SampleDesc d;
         d.k = k;
-        d.mt = k >= 0 ? sM[0] : 0.f;
-        d.md = (k >= 0 && k < a.gamma) ? sM[1] : 0.f;
+        d.mt = k >= 0 ? s_Mt : 0.f;
+        d.md = (k >= 0 && k < a.gamma) ? s_Md : 0.f;
         d.pad = 0;
         a.desc[b] = d;
     }
-    for (int i = threadIdx.x; i <= a.gamma; i += blockDim.x)
+    for (int i = t; i <= a.gamma; i += T)
         if (k < 0 || i != k)
             a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
     if (a.out_lp)
-        for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
+        for (int i = t; i < a.gamma; i += T) {
             float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
-            const bool have = k >= 0 && i <= k;           // positions that were read
+            const bool have = k >= 0 && i <= k;           // positions decided
             o[0] = have ? s_lp[i] : CUDART_NAN_F;
             o[1] = have ? s_lq[i] : CUDART_NAN_F;
         }
@@ -750,7 +838,7 @@ static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.B * kLazyCluster, 1, 1);
-    cfg.blockDim = dim3(kRingThreads, 1, 1);
+    cfg.blockDim = dim3(kLazyThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
