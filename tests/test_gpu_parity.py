@@ -280,3 +280,38 @@ def test_no_device_error_on_valid_inputs(sv):
     check_greedy(sv, a.target, a.dtype, a.draft_tokens, ws=ws)
     check_tree(sv, t, ws=ws)
     assert ws.read_error() == 0
+
+
+# ------------------------------------------------------- largest and empty sizes
+def test_sample_largest_gamma(sv):
+    # gamma = 256 is the most a sampling call takes (2 * 256 + 1 rows per sequence)
+    x = W.make_chain("chain-b8", B=2, gamma=256, V=4096)
+    res = check_sample(sv, x)
+    assert res["rows"] == 2 * 257
+
+
+def test_greedy_longest_chain(sv):
+    # gamma + 1 = 1024 rows, drafts equal to the target argmax for long runs
+    x = W.make_chain("chain-b8", B=2, gamma=1023, V=2048)
+    am = np.argmax(x.target[:, :x.gamma], axis=2).astype(np.int32)
+    tokens = am.copy()
+    tokens[0, 700] = (tokens[0, 700] + 1) % x.V          # sequence 0 stops at 700, 1 accepts all
+    ref = check_greedy(sv, x.target, x.dtype, tokens)
+    assert ref["accepted"].tolist() == [700, 1023]
+
+
+def test_tree_largest(sv):
+    # 1 + 31 + 31 * 32 = 1024 nodes, the most a tree call takes
+    t = W.make_tree(B=2, V=2048, depth=31, branches=32, match_prob=0.9)
+    assert t.node_tokens.shape[1] == 1024
+    check_tree(sv, t)
+
+
+def test_empty_batch(sv):
+    x = W.make_chain("chain-small", B=1)
+    zt = dev_logits(x.target[:0], x.dtype)
+    zd = dev_logits(x.draft[:0], x.dtype)
+    tok, acc = sv.verify_sample(zt, zd, dev(x.draft_tokens[:0]), dev(x.uniforms[:0]), x.T)
+    assert tok.shape == (0, x.gamma + 1) and acc.shape == (0,)
+    tok, acc = sv.verify_greedy(zt, dev(x.draft_tokens[:0]))
+    assert tok.shape == (0, x.gamma + 1)
