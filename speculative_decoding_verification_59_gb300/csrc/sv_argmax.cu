@@ -20,12 +20,14 @@ namespace sv {
 // until the stream's partials are visible).
 __global__ void __launch_bounds__(kGroup) greedy_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
+    prefetch_tokens(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
     pdl_wait();
     decide_greedy(a, blockIdx.x, threadIdx.x, sm);
 }
 
 __global__ void __launch_bounds__(kGroup) tree_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
+    prefetch_tokens(a, blockIdx.x, threadIdx.x, true, sm);
     pdl_wait();
     decide_tree(a, blockIdx.x, threadIdx.x, sm);
 }

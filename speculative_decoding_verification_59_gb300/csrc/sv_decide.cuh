@@ -80,6 +80,7 @@ struct SampleDecideSmem {
     float M[2 * kMaxGamma + 1];       // row max
     float lnZ[2 * kMaxGamma + 1];     // ln sum exp((z - M)/T)
     float lp[kMaxGamma], lq[kMaxGamma];
+    float u[kMaxGamma];               // accept uniforms
     int bad, k;
 };
 
@@ -155,7 +156,11 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             zdx = load_logit<ELT>(sample_row(a, b, a.gamma + 1 + gt, rowbytes), xi);
         }
     }
+    if (gt < a.gamma) sm.u[gt] = a.u[(size_t)b * (a.gamma + 1) + gt];
     if (gt == 0) sm.bad = 0;
+    // Everything above reads inputs only; the partials below come from the
+    // stream, which may still be finishing.
+    pdl_wait();
     group_sync();
     for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
         float M, lnZ;
@@ -190,7 +195,7 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
         if (!sm.bad) {
             k = a.gamma;                                   // left to right; first rejection wins
             for (int i = 0; i < a.gamma; ++i)
-                if (!accept_draft(sm.lp[i], sm.lq[i], a.u[(size_t)b * (a.gamma + 1) + i])) { k = i; break; }
+                if (!accept_draft(sm.lp[i], sm.lq[i], sm.u[i])) { k = i; break; }
         }
         sm.k = k;
     }
@@ -228,8 +233,22 @@ struct ArgmaxDecideSmem {
     int g[kMaxNodes];                 // row argmax
     int depth[kMaxNodes];             // trees: longest accepted continuation
     int best[kMaxNodes];              // trees: child that continues it
+    int x[kMaxNodes];                 // draft tokens (chains) / node tokens (trees)
+    int par[kMaxNodes];               // trees: parents
     int k, len, bad;
 };
+
+// The sequence's tokens (and parents) into shared memory.  They are inputs,
+// so a decide kernel loads them before waiting for the stream's partials;
+// the merge that follows ends with a group barrier that publishes them.
+__device__ __forceinline__ void prefetch_tokens(const VerifyArgs& a, int b, int gt, bool tree,
+                                                ArgmaxDecideSmem& sm) {
+    const int n = tree ? a.rows_per_seq : a.gamma;
+    for (int i = gt; i < n; i += kGroup) {
+        sm.x[i] = a.x[(size_t)b * n + i];
+        if (tree) sm.par[i] = a.par[(size_t)b * n + i];
+    }
+}
 
 // Argmax of every row of sequence b from the (value, index) partials.
 __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, int gt, int* g) {
@@ -239,10 +258,19 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
         const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
         float bv = kNegInf;
         int bi = 0x7fffffff;
-        for (int p = lane; p < P; p += 32) {
-            const float2 q = __ldcg(&pr[p]);
-            const int qi = __float_as_int(q.y);
-            if (am_better(q.x, qi, bv, bi)) { bv = q.x; bi = qi; }
+        constexpr int kHeld = 4;                           // loads in flight per lane
+        for (int p0 = lane; p0 < P; p0 += 32 * kHeld) {
+            float2 q[kHeld];
+#pragma unroll
+            for (int h = 0; h < kHeld; ++h) {
+                const int p = p0 + 32 * h;
+                q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+            }
+#pragma unroll
+            for (int h = 0; h < kHeld; ++h) {
+                const int qi = __float_as_int(q[h].y);
+                if (am_better(q[h].x, qi, bv, bi)) { bv = q[h].x; bi = qi; }
+            }
         }
         warp_argmax(bv, bi);
         if (lane == 0) g[r] = bi;
@@ -258,7 +286,7 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
     if (gt == 0) {
         int bad = 0;
         for (int i = 0; i < G; ++i) {
-            const int xi = a.x[(size_t)b * G + i];
+            const int xi = sm.x[i];
             if (xi < 0 || xi >= a.V) bad = 1;
         }
         int k = G;
@@ -267,7 +295,7 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
             k = -1;
         } else {
             for (int i = 0; i < G; ++i)
-                if (a.x[(size_t)b * G + i] != sm.g[i]) { k = i; break; }
+                if (sm.x[i] != sm.g[i]) { k = i; break; }
         }
         sm.k = k;
         a.out_acc[b] = k;
@@ -276,7 +304,7 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
     const int k = sm.k;
     for (int i = gt; i <= G; i += kGroup) {
         int v = -1;
-        if (k >= 0) v = i < k ? a.x[(size_t)b * G + i] : (i == k ? sm.g[k] : -1);
+        if (k >= 0) v = i < k ? sm.x[i] : (i == k ? sm.g[k] : -1);
         a.out_tok[(size_t)b * (G + 1) + i] = v;
     }
 }
@@ -286,8 +314,8 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
 // lowest node ids) and the argmax of the path's last node.
 static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
     const int N = a.rows_per_seq;
-    const int32_t* tok = a.x + (size_t)b * N;
-    const int32_t* par = a.par + (size_t)b * N;
+    const int* tok = sm.x;                                 // prefetched
+    const int* par = sm.par;
     if (gt == 0) sm.bad = 0;
     merge_argmax_rows(a, b, gt, sm.g);                     // ends with group_sync
     for (int n = gt; n < N; n += kGroup) {

@@ -342,8 +342,7 @@ template <int ELT>
 __global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs a) {
     __shared__ SampleDecideSmem dsm;
     pdl_trigger();
-    pdl_wait();                                           // the stream's partials are visible
-    decide_sample<ELT>(a, blockIdx.x, threadIdx.x, dsm);
+    decide_sample<ELT>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
     write_sample_decision(a, blockIdx.x, threadIdx.x, dsm);
 }
 
