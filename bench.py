@@ -420,7 +420,7 @@ def run_own(args):
                 "pipelining": "double-buffered: step i+1's host-to-device copy runs on a copy "
                               "stream while step i's kernels run",
             },
-            "gpu_launches": 9 * K,
+            "gpu_launches": 8 * K,
             "clocks": clk,
             "cpu_baseline": cpu,
             "extra_paths": extra,
@@ -596,7 +596,7 @@ def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, de
             "rows_per_s": world * B * (g + 1) / (ms * 1e-3),
             "pass1_rows_read_at_most": rows_read, "pass1_rows_full": B * (2 * g + 1),
             "pass1_bytes_read_at_most": bytes_read, "pass1_bytes_full": acct["bytes_stats"],
-            "gpu_launches_per_call": 4}
+            "gpu_launches_per_call": 3}
 
 
 def oracle_slice(x, n, ttok, tpar, nthreads):

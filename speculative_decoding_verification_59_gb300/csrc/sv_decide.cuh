@@ -58,7 +58,8 @@ struct VerifyArgs {
     float2* parts;             // per-warp-chunk partials
     SampleDesc* desc;          // sampling: rejection index and row maxima
     float4* zsum;              // sampling: [B, C, 8] (Za.hi, Za.lo, Zb.hi, Zb.lo) per segment
-    float2* wsum;              // sampling: [B, C, 8] residual weight total per segment
+    float4* wsum;              // sampling: [B, C, 8] (W.hi, W.lo, D, 0) per segment, rejections:
+                               // residual sum at the desc's ratio rt and its slope
     int* err;
     int32_t* out_tok;
     int32_t* out_acc;
@@ -213,7 +214,7 @@ static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt,
         d.k = k;
         d.mt = k >= 0 ? sm.M[k] : 0.f;
         d.md = (k >= 0 && k < a.gamma) ? sm.M[a.gamma + 1 + k] : 0.f;
-        d.pad = 0;
+        d.rt = (k >= 0 && k < a.gamma) ? expf(sm.lnZ[k] - sm.lnZ[a.gamma + 1 + k]) : 0.f;
         a.desc[b] = d;
     }
     // accepted drafts and padding; slot k belongs to the search kernel

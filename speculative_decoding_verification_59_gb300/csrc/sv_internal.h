@@ -40,11 +40,12 @@ struct SampleDesc {
     int k;        // rejection index (< gamma), gamma when all drafts were accepted, -1: bad input
     float mt;     // max logit of target row k
     float md;     // max logit of draft row k (rejection only)
-    int pad;
+    float rt;     // rejection: Z_t / Z_d of row k from the row statistics (~1e-6 accurate)
 };
 
 // Workspace: [error word (256 bytes reserved) | per-warp row partials |
-// SampleDesc[B] | per-segment normaliser sums | per-segment residual sums].
+// SampleDesc[B] | per-segment normaliser sums | per-segment residual sums
+// and slopes].
 // Every region after the error word is rewritten by the kernels of a call
 // before another kernel of that call reads it, so a workspace carries nothing
 // from one call to the next except the error word, which only accumulates
@@ -67,7 +68,7 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     const size_t segs = (size_t)B * (size_t)final_chunks(V) * kFinalSegs;
     L.zsum_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
     L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * segs);
-    L.total = L.wsum_off + align256(2 * sizeof(float) * segs);
+    L.total = L.wsum_off + align256(4 * sizeof(float) * segs);
     return L;
 }
 

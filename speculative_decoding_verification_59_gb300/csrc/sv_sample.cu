@@ -13,20 +13,22 @@
 // of every sequence from the single row pair it comes from -- target and
 // draft row k after a rejection at k (weights max(0, p_k - q_k)), target row
 // gamma when every draft was accepted (weights p_gamma) -- by inverse CDF in
-// index order.  Four kernels, chained with programmatic dependent launch,
+// index order.  Three kernels, chained with programmatic dependent launch,
 // keep every sequence in flight at once:
 //   sample_decide_kernel  one CTA per sequence: row statistics from the
 //                         partials, the accept decisions, every output but
-//                         the final token;
+//                         the final token, and the approximate normaliser
+//                         ratio rt = Z_t/Z_d of row k from those statistics;
 //   sample_zsum_kernel    one CTA per 8192-element chunk of row k, one warp
 //                         per 1024-element segment: sums of the exponentials
-//                         of the target and draft segment;
-//   sample_wsum_kernel    the same grid (rejections only): the ratio of the
-//                         two row normalisers from all segment sums, then
-//                         each segment's residual weight total;
-//   sample_search_kernel  one CTA per sequence: prefix over the segment
-//                         totals, the owning segment, its 1024 weights
-//                         recomputed and scanned, the owning element.
+//                         of the target and draft segment and, after a
+//                         rejection, the residual sum at ratio rt with its
+//                         slope;
+//   sample_search_kernel  one CTA per sequence: the exact ratio R from the
+//                         exponential sums, the segment residual sums moved
+//                         from rt to R to first order, prefix over them, the
+//                         owning segment, its 1024 weights recomputed at R and
+//                         scanned, the owning element.
 // The weights are formed from the very exponentials whose sums normalise them
 // (the same arithmetic in every kernel), and all sums are float-float (about
 // 48 bits): the CDF each sequence samples from stays within ~1e-9 of the
@@ -248,11 +250,16 @@ __device__ __forceinline__ FinalRows final_rows(const VerifyArgs& a, int b, cons
 // [c kFinalChunk + w kSeg, + kSeg) -- one "segment" -- with its lanes
 // interleaved over 16-byte vectors (vector h of lane l starts at element
 // (l + 32 h) 16/ELT of the segment), so every load instruction of a warp
-// reads 512 contiguous bytes.  MODE 0: sums of ea and eb; MODE 1: sum of the
-// residual weights.
-template <int ELT, bool VEC, bool FAST, int MODE>
+// reads 512 contiguous bytes.  Per segment: za = sum ea, and after a
+// rejection zb = sum eb, w = sum max(0, ea - rt eb) at the approximate
+// normaliser ratio rt, and dd = sum of eb over the elements with
+// ea > rt eb -- minus the slope of w in the ratio.  The search turns w into
+// the residual sum at the exact ratio R to first order, w - (R - rt) dd: the
+// only elements the correction misses are those whose ea/eb lies between rt
+// and R (~1e-6 apart), each off by at most |R - rt| eb.
+template <int ELT, bool VEC, bool FAST>
 __device__ __forceinline__ void segment_sums(const VerifyArgs& a, const FinalRows& f, int c,
-                                             FF R, FF* s0, FF* s1) {
+                                             float rt, FF* za, FF* zb, FF* w, float* dd) {
     constexpr int PV = 16 / ELT;
     constexpr int NV = kSeg / (32 * PV);                  // vectors per lane: 4 (bf16), 8 (fp32)
     constexpr int NB = FAST ? 4 : 1;                      // vectors per load batch
@@ -260,8 +267,9 @@ __device__ __forceinline__ void segment_sums(const VerifyArgs& a, const FinalRow
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j0 = c * kFinalChunk + warp * kSeg;
     const ExpK k = exp_consts(a);
-    const f32x2 nRhi2 = f2_pack(-R.hi, -R.hi), nRlo2 = f2_pack(-R.lo, -R.lo);
-    KSum2 ka, kb;
+    const f32x2 nrt2 = f2_pack(-rt, -rt);
+    KSum2 ka, kb, kw;
+    f32x2 d2 = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int h0 = 0; h0 < NV; h0 += NB) {
         uint4 qa[NB], qb[NB];
@@ -278,17 +286,29 @@ __device__ __forceinline__ void segment_sums(const VerifyArgs& a, const FinalRow
             if (f.rej) vec_exps<ELT, FAST>(qb[h], f.xb, k, a, eb);
 #pragma unroll
             for (int i = 0; i < NP; ++i) {
-                if constexpr (MODE == 0) {
-                    ka.add(ea[i]);
-                    if (f.rej) kb.add(eb[i]);
-                } else {
-                    ka.add(resid_pair(ea[i], eb[i], nRhi2, nRlo2));
+                ka.add(ea[i]);
+                if (f.rej) {
+                    kb.add(eb[i]);
+                    float t0, t1, b0, b1;
+                    f2_unpack(f2_fma(nrt2, eb[i], ea[i]), t0, t1);
+                    f2_unpack(eb[i], b0, b1);
+                    kw.add(f2_pack(fmaxf(t0, 0.f), fmaxf(t1, 0.f)));
+                    d2 = f2_add(d2, f2_pack(t0 > 0.f ? b0 : 0.f, t1 > 0.f ? b1 : 0.f));
                 }
             }
         }
     }
-    *s0 = warp_sum_ff(ka.value());
-    if (MODE == 0) *s1 = f.rej ? warp_sum_ff(kb.value()) : FF{0.f, 0.f};
+    *za = warp_sum_ff(ka.value());
+    if (f.rej) {
+        *zb = warp_sum_ff(kb.value());
+        *w = warp_sum_ff(kw.value());
+        float d0, d1;
+        f2_unpack(d2, d0, d1);
+        *dd = warp_sum(d0 + d1);
+    } else {
+        *zb = *w = FF{0.f, 0.f};
+        *dd = 0.f;
+    }
 }
 
 // Inclusive scan of one float-float value per thread over a kCT-thread block
@@ -347,7 +367,8 @@ __global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs 
 }
 
 // Per (sequence, chunk): the sums of the exponentials of target row k and
-// (after a rejection) draft row k over each of the chunk's segments.
+// (after a rejection) draft row k over each of the chunk's segments, and the
+// residual sums at the approximate ratio with their slopes.
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT) sample_zsum_kernel(const VerifyArgs a) {
     const int b = blockIdx.x, c = blockIdx.y;
@@ -356,30 +377,15 @@ __global__ void __launch_bounds__(kCT) sample_zsum_kernel(const VerifyArgs a) {
     const SampleDesc d = a.desc[b];
     if (d.k < 0) return;
     const FinalRows f = final_rows<ELT>(a, b, d);
-    FF za, zb;
-    if (f.fast) segment_sums<ELT, VEC, true, 0>(a, f, c, FF{0.f, 0.f}, &za, &zb);
-    else segment_sums<ELT, VEC, false, 0>(a, f, c, FF{0.f, 0.f}, &za, &zb);
-    if ((threadIdx.x & 31) == 0)
-        a.zsum[((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5)] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
-}
-
-// Per (sequence, chunk), rejections only: the residual weight totals of the
-// chunk's segments.
-template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_wsum_kernel(const VerifyArgs a) {
-    __shared__ FF wtot[kCW];
-    const int b = blockIdx.x, c = blockIdx.y;
-    pdl_trigger();
-    pdl_wait();
-    const SampleDesc d = a.desc[b];
-    if (d.k < 0 || d.k >= a.gamma) return;               // bonus rows use the exponential sums
-    const FF R = normaliser_ratio(a, b, wtot);
-    const FinalRows f = final_rows<ELT>(a, b, d);
-    FF w, unused;
-    if (f.fast) segment_sums<ELT, VEC, true, 1>(a, f, c, R, &w, &unused);
-    else segment_sums<ELT, VEC, false, 1>(a, f, c, R, &w, &unused);
-    if ((threadIdx.x & 31) == 0)
-        a.wsum[((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5)] = make_float2(w.hi, w.lo);
+    FF za, zb, w;
+    float dd;
+    if (f.fast) segment_sums<ELT, VEC, true>(a, f, c, d.rt, &za, &zb, &w, &dd);
+    else segment_sums<ELT, VEC, false>(a, f, c, d.rt, &za, &zb, &w, &dd);
+    if ((threadIdx.x & 31) == 0) {
+        const size_t sg = ((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5);
+        a.zsum[sg] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
+        if (f.rej) a.wsum[sg] = make_float4(w.hi, w.lo, dd, 0.f);
+    }
 }
 
 // The weights of the kSearchPT consecutive elements this thread holds in
@@ -437,10 +443,12 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     const FF R = rej ? normaliser_ratio(a, b, wtot) : FF{0.f, 0.f};
     const int ns = a.C * kCW;                             // segments in the row
     const int G = (ns + kCT - 1) / kCT;                   // consecutive segments per thread
+    // residual sums at the exact ratio: w(rt) - (R - rt) dd, to first order
+    const float dR = (R.hi - d.rt) + R.lo;
     auto seg_total = [&](int s) -> FF {
         if (rej) {
-            const float2 q = a.wsum[(size_t)b * ns + s];
-            return FF{q.x, q.y};
+            const float4 q = a.wsum[(size_t)b * ns + s];
+            return ff_combine(FF{q.x, q.y}, FF{-dR * q.z, 0.f});
         }
         const float4 q = a.zsum[(size_t)b * ns + s];
         return FF{q.x, q.y};
@@ -600,7 +608,7 @@ template <int ELT>
 __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ float sM[2], slnZ[2], s_Mt, s_Md;
+    __shared__ float sM[2], slnZ[2], s_Mt, s_Md, s_Rt;
     __shared__ float s_lp[kMaxGamma], s_lq[kMaxGamma];
     __shared__ float s_zt[kMaxGamma], s_zd[kMaxGamma];   // z^t_i[x_i], z^d_i[x_i], gathered up front
     __shared__ int s_bad, s_ok, s_k;
@@ -628,7 +636,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const Veri
         s_bad = bad;
         s_ok = 1;
         s_k = -1;
-        s_Mt = s_Md = 0.f;
+        s_Mt = s_Md = s_Rt = 0.f;
         s_limit = 1;
         s_stop = 0;
         s_issued = -1;
@@ -773,6 +781,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const Veri
                     if (stop) {
                         s_Mt = sM[0];
                         s_Md = j < a.gamma ? sM[1] : 0.f;
+                        s_Rt = j < a.gamma ? expf(slnZ[0] - slnZ[1]) : 0.f;   // as the decide step
                         s_stop = 1;
                     }
                     __threadfence_block();
@@ -797,7 +806,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const Veri
         d.k = k;
         d.mt = k >= 0 ? s_Mt : 0.f;
         d.md = (k >= 0 && k < a.gamma) ? s_Md : 0.f;
-        d.pad = 0;
+        d.rt = (k >= 0 && k < a.gamma) ? s_Rt : 0.f;
         a.desc[b] = d;
     }
     for (int i = t; i <= a.gamma; i += T)
@@ -877,8 +886,6 @@ static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool dec
     }
     e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(sample_wsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
-    if (e != cudaSuccess) return e;
     return launch_pdl(sample_search_kernel<ELT, VEC>, dim3(a.B), kCT, a, st);
 }
 
@@ -914,7 +921,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     a.parts = reinterpret_cast<float2*>(w + L.part_off);
     a.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
     a.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
-    a.wsum = reinterpret_cast<float2*>(w + L.wsum_off);
+    a.wsum = reinterpret_cast<float4*>(w + L.wsum_off);
     a.err = reinterpret_cast<int*>(w + L.err_off);
     a.out_tok = out_tok;
     a.out_acc = out_acc;
