@@ -315,3 +315,19 @@ def test_empty_batch(sv):
     assert tok.shape == (0, x.gamma + 1) and acc.shape == (0,)
     tok, acc = sv.verify_greedy(zt, dev(x.draft_tokens[:0]))
     assert tok.shape == (0, x.gamma + 1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sample_many_equal_ratios(sv, dtype):
+    """Integer logits: thousands of elements share each ratio p_j/q_j, the case
+    where the residual sums' first-order move from the approximate to the exact
+    normaliser ratio could miss the most mass."""
+    rng = np.random.default_rng(17)
+    B, g, V = 48, 3, 24576
+    zt = rng.integers(-3, 4, size=(B, g + 1, V)).astype(np.float32)
+    zd = zt[:, :g] + rng.integers(-1, 2, size=(B, g, V)).astype(np.float32)
+    x = W.make_chain("chain-b256" if dtype == "f32" else "chain-b8", B=B, gamma=g, V=V)
+    x.target, x.draft = zt, zd
+    for r in range(4):
+        x.uniforms = rng.random((B, g + 1), dtype=np.float32)
+        check_sample(sv, x)
