@@ -109,9 +109,10 @@ spec_status_t spec_verify_workspace_init(void* workspace, size_t workspace_bytes
  *   out_logprobs     [B, gamma, 2] f32, nullable: ln p_i(x_i), ln q_i(x_i)
  *
  * A streaming pass over every logit row (row max and sum-exp partials) is
- * followed by four small kernels: the accept decisions, the chunk sums of the
+ * followed by two kernels: the accept decisions, then the chunk sums of the
  * exponentials and of the residual weights of the one rejected (or bonus)
- * row pair, and the inverse-CDF search.
+ * row pair, in which the last chunk of each sequence to finish runs the
+ * inverse-CDF search.
  */
 spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
                                  spec_dtype_t dtype, const int32_t* draft_tokens,

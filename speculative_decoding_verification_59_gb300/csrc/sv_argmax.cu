@@ -33,16 +33,7 @@ __global__ void __launch_bounds__(kGroup) tree_decide_kernel(const VerifyArgs a)
 }
 
 static cudaError_t launch_decide(void (*kfn)(VerifyArgs), const VerifyArgs& a, int B, cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B, 1, 1);
-    cfg.blockDim = dim3(kGroup, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kfn, a);
+    return launch_pdl(kfn, dim3(B), kGroup, 0, st, a);
 }
 
 static VerifyArgs argmax_args(const void* zt, int elt, int B, int rows, int V, void* ws) {

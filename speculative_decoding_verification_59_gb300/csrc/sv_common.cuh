@@ -243,11 +243,31 @@ __device__ __forceinline__ FF warp_incl_scan_ff(FF a) {
 }
 
 // ---- programmatic dependent launch -------------------------------------------
-// The streaming kernel lets the next kernel in the stream begin launching
-// once each of its CTAs is on its last chunk; that kernel waits (in hardware)
-// until the streaming grid has completed and its writes are visible.  Both
-// are no-ops for a kernel launched without the programmatic attribute.
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl): it may begin launching once every CTA of the
+// kernel before it in the stream has triggered (or exited), and it waits (in
+// hardware, griddepcontrol.wait) until that kernel has completed and its
+// writes are visible before it touches global memory that the earlier kernel
+// may read or write.  The streaming kernels trigger when each CTA is on its
+// last chunk, the small kernels on entry.  Both instructions are no-ops for a
+// kernel launched without the attribute.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kfn)(KArgs...), dim3 grid, int threads, size_t smem,
+                                     cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, args...);
+}
 
 }  // namespace sv

@@ -136,19 +136,11 @@ cudaError_t launch_cosine(const void* hidden, const void* query, spec_dtype_t dt
     else cosine_scores_kernel<4><<<grid, kCosThreads, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((B + kCosTopWarps - 1) / kCosTopWarps, 1, 1);
-    cfg.blockDim = dim3(kCosTopWarps * 32, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 tgrid((B + kCosTopWarps - 1) / kCosTopWarps);
     const int KC = topk_list_len(delta);
-    if (KC == 2) return cudaLaunchKernelEx(&cfg, cosine_top_kernel<2>, a);
-    if (KC == 4) return cudaLaunchKernelEx(&cfg, cosine_top_kernel<4>, a);
-    return cudaLaunchKernelEx(&cfg, cosine_top_kernel<8>, a);
+    if (KC == 2) return launch_pdl(cosine_top_kernel<2>, tgrid, kCosTopWarps * 32, 0, st, a);
+    if (KC == 4) return launch_pdl(cosine_top_kernel<4>, tgrid, kCosTopWarps * 32, 0, st, a);
+    return launch_pdl(cosine_top_kernel<8>, tgrid, kCosTopWarps * 32, 0, st, a);
 }
 
 }  // namespace sv

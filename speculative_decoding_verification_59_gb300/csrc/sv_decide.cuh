@@ -57,6 +57,7 @@ struct VerifyArgs {
     int C;                     // sampling: final-pass chunks per row
     float2* parts;             // per-warp-chunk partials
     SampleDesc* desc;          // sampling: rejection index and row maxima
+    unsigned* tick;            // sampling: per-sequence count of finished final-pass chunks
     float4* zsum;              // sampling: [B, C, 8] (Za.hi, Za.lo, Zb.hi, Zb.lo) per segment
     float4* wsum;              // sampling: [B, C, 8] (W.hi, W.lo, D, 0) per segment, rejections:
                                // residual sum at the desc's ratio rt and its slope
@@ -216,8 +217,9 @@ static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt,
         d.md = (k >= 0 && k < a.gamma) ? sm.M[a.gamma + 1 + k] : 0.f;
         d.rt = (k >= 0 && k < a.gamma) ? expf(sm.lnZ[k] - sm.lnZ[a.gamma + 1 + k]) : 0.f;
         a.desc[b] = d;
+        a.tick[b] = 0u;
     }
-    // accepted drafts and padding; slot k belongs to the search kernel
+    // accepted drafts and padding; slot k belongs to the final-pass search
     for (int i = gt; i <= a.gamma; i += kGroup)
         if (k < 0 || i != k)
             a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;

@@ -44,14 +44,15 @@ struct SampleDesc {
 };
 
 // Workspace: [error word (256 bytes reserved) | per-warp row partials |
-// SampleDesc[B] | per-segment normaliser sums | per-segment residual sums
-// and slopes].
+// SampleDesc[B] | per-sequence finish tickets | per-segment normaliser sums |
+// per-segment residual sums and slopes].
 // Every region after the error word is rewritten by the kernels of a call
-// before another kernel of that call reads it, so a workspace carries nothing
-// from one call to the next except the error word, which only accumulates
-// error bits until spec_verify_read_error clears it.
+// before another kernel of that call reads it (the tickets are zeroed by the
+// kernel that writes the SampleDesc), so a workspace carries nothing from one
+// call to the next except the error word, which only accumulates error bits
+// until spec_verify_read_error clears it.
 struct WsLayout {
-    size_t err_off, part_off, part_count, desc_off, zsum_off, wsum_off, total;
+    size_t err_off, part_off, part_count, desc_off, tick_off, zsum_off, wsum_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -66,7 +67,8 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     L.part_count = rows * (size_t)nseg(V, 4) * kWarps;
     L.desc_off = L.part_off + align256(sizeof(float2) * L.part_count);
     const size_t segs = (size_t)B * (size_t)final_chunks(V) * kFinalSegs;
-    L.zsum_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
+    L.tick_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
+    L.zsum_off = L.tick_off + align256(sizeof(int) * (size_t)B);
     L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * segs);
     L.total = L.wsum_off + align256(4 * sizeof(float) * segs);
     return L;

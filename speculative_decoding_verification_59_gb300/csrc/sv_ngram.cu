@@ -235,16 +235,8 @@ cudaError_t launch_ngram(const int32_t* tokens, const int32_t* lengths, int B, i
     ngram_scan_kernel<<<(unsigned)(B * S), kNgThreads, 0, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((B + kNgMergeWarps - 1) / kNgMergeWarps, 1, 1);
-    cfg.blockDim = dim3(kNgMergeWarps * 32, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ngram_merge_kernel, a);
+    return launch_pdl(ngram_merge_kernel, dim3((B + kNgMergeWarps - 1) / kNgMergeWarps),
+                      kNgMergeWarps * 32, 0, st, a);
 }
 
 }  // namespace sv

@@ -13,22 +13,22 @@
 // of every sequence from the single row pair it comes from -- target and
 // draft row k after a rejection at k (weights max(0, p_k - q_k)), target row
 // gamma when every draft was accepted (weights p_gamma) -- by inverse CDF in
-// index order.  Three kernels, chained with programmatic dependent launch,
+// index order.  Two kernels, chained with programmatic dependent launch,
 // keep every sequence in flight at once:
 //   sample_decide_kernel  one CTA per sequence: row statistics from the
 //                         partials, the accept decisions, every output but
 //                         the final token, and the approximate normaliser
 //                         ratio rt = Z_t/Z_d of row k from those statistics;
-//   sample_zsum_kernel    one CTA per 8192-element chunk of row k, one warp
+//   sample_final_kernel   one CTA per 8192-element chunk of row k, one warp
 //                         per 1024-element segment: sums of the exponentials
 //                         of the target and draft segment and, after a
 //                         rejection, the residual sum at ratio rt with its
-//                         slope;
-//   sample_search_kernel  one CTA per sequence: the exact ratio R from the
-//                         exponential sums, the segment residual sums moved
-//                         from rt to R to first order, prefix over them, the
-//                         owning segment, its 1024 weights recomputed at R and
-//                         scanned, the owning element.
+//                         slope.  The sequence's last chunk CTA to finish (a
+//                         ticket count) then runs the search: the exact ratio
+//                         R from the exponential sums, the segment residual
+//                         sums moved from rt to R to first order, prefix over
+//                         them, the owning segment, its 1024 weights
+//                         recomputed at R and scanned, the owning element.
 // The weights are formed from the very exponentials whose sums normalise them
 // (the same arithmetic in every kernel), and all sums are float-float (about
 // 48 bits): the CDF each sequence samples from stays within ~1e-9 of the
@@ -346,7 +346,7 @@ __device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* w
     const float4* zs = a.zsum + (size_t)b * ns;
     FF za{0.f, 0.f}, zb{0.f, 0.f};
     for (int s = threadIdx.x; s < ns; s += kCT) {
-        const float4 q = zs[s];
+        const float4 q = __ldcg(&zs[s]);
         za = ff_combine(za, FF{q.x, q.y});
         zb = ff_combine(zb, FF{q.z, q.w});
     }
@@ -364,28 +364,6 @@ __global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs 
     pdl_trigger();
     decide_sample<ELT>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
     write_sample_decision(a, blockIdx.x, threadIdx.x, dsm);
-}
-
-// Per (sequence, chunk): the sums of the exponentials of target row k and
-// (after a rejection) draft row k over each of the chunk's segments, and the
-// residual sums at the approximate ratio with their slopes.
-template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_zsum_kernel(const VerifyArgs a) {
-    const int b = blockIdx.x, c = blockIdx.y;
-    pdl_trigger();
-    pdl_wait();
-    const SampleDesc d = a.desc[b];
-    if (d.k < 0) return;
-    const FinalRows f = final_rows<ELT>(a, b, d);
-    FF za, zb, w;
-    float dd;
-    if (f.fast) segment_sums<ELT, VEC, true>(a, f, c, d.rt, &za, &zb, &w, &dd);
-    else segment_sums<ELT, VEC, false>(a, f, c, d.rt, &za, &zb, &w, &dd);
-    if ((threadIdx.x & 31) == 0) {
-        const size_t sg = ((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5);
-        a.zsum[sg] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
-        if (f.rej) a.wsum[sg] = make_float4(w.hi, w.lo, dd, 0.f);
-    }
 }
 
 // The weights of the kSearchPT consecutive elements this thread holds in
@@ -427,18 +405,27 @@ __device__ __forceinline__ void search_weights(const VerifyArgs& a, const FinalR
     }
 }
 
-// One CTA per sequence: the owning segment from the segment totals, then the
+// Shared memory of the final-pass CTAs.
+struct FinalSmem {
+    FF wtot[kCW];
+    FF lo;
+    int sel, last, seg;
+    int mine;                 // this CTA finished its sequence's last chunk
+};
+
+// The search of sequence b, by one whole CTA once every chunk's segment sums
+// are in the workspace: the owning segment from the segment totals, then the
 // owning element from that segment's weights, recomputed with the same
 // arithmetic that produced its total.
 template <int ELT, bool VEC>
-__global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) {
-    __shared__ FF wtot[kCW];
-    __shared__ int s_sel, s_last, s_seg;
-    __shared__ FF s_lo;
-    const int b = blockIdx.x, tid = threadIdx.x;
-    pdl_wait();
-    const SampleDesc d = a.desc[b];
-    if (d.k < 0) return;
+__device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, const SampleDesc& d,
+                                                FinalSmem& sm) {
+    FF* wtot = sm.wtot;
+    int& s_sel = sm.sel;
+    int& s_last = sm.last;
+    int& s_seg = sm.seg;
+    FF& s_lo = sm.lo;
+    const int tid = threadIdx.x;
     bool rej = d.k < a.gamma;
     const FF R = rej ? normaliser_ratio(a, b, wtot) : FF{0.f, 0.f};
     const int ns = a.C * kCW;                             // segments in the row
@@ -447,10 +434,10 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     const float dR = (R.hi - d.rt) + R.lo;
     auto seg_total = [&](int s) -> FF {
         if (rej) {
-            const float4 q = a.wsum[(size_t)b * ns + s];
+            const float4 q = __ldcg(&a.wsum[(size_t)b * ns + s]);
             return ff_combine(FF{q.x, q.y}, FF{-dR * q.z, 0.f});
         }
-        const float4 q = a.zsum[(size_t)b * ns + s];
+        const float4 q = __ldcg(&a.zsum[(size_t)b * ns + s]);
         return FF{q.x, q.y};
     };
 
@@ -546,6 +533,48 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
     }
 }
 
+// Ticket of a finished chunk: a gpu-scope acquire-release increment, so the
+// CTA that draws the last ticket sees every other chunk's segment sums.
+__device__ __forceinline__ unsigned take_ticket(unsigned* t) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+    return old;
+}
+
+// Per (chunk, sequence): the sums of the exponentials of target row k and
+// (after a rejection) draft row k over each of the chunk's segments, and the
+// residual sums at the approximate ratio with their slopes; then, in the
+// last of the sequence's C chunk CTAs to finish, the search.  The decide
+// kernel (or the lazy pass) zeroes the sequence's ticket count before this
+// kernel's wait returns.
+template <int ELT, bool VEC>
+__global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a) {
+    __shared__ FinalSmem sm;
+    const int c = blockIdx.x, b = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
+    const SampleDesc d = a.desc[b];
+    if (d.k < 0) return;
+    {
+        const FinalRows f = final_rows<ELT>(a, b, d);
+        FF za, zb, w;
+        float dd;
+        if (f.fast) segment_sums<ELT, VEC, true>(a, f, c, d.rt, &za, &zb, &w, &dd);
+        else segment_sums<ELT, VEC, false>(a, f, c, d.rt, &za, &zb, &w, &dd);
+        if ((threadIdx.x & 31) == 0) {
+            const size_t sg = ((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5);
+            a.zsum[sg] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
+            if (f.rej) a.wsum[sg] = make_float4(w.hi, w.lo, dd, 0.f);
+            __threadfence();
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sm.mine = take_ticket(&a.tick[b]) == (unsigned)(a.C - 1);
+    __syncthreads();
+    if (!sm.mine) return;
+    search_sequence<ELT, VEC>(a, b, d, sm);
+}
+
 // ------------------------------------------------ lazy (early-exit) pass 1
 // Source: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", section "What happens in one round", step 3: drafts are
@@ -572,7 +601,7 @@ __global__ void __launch_bounds__(kCT) sample_search_kernel(const VerifyArgs a) 
 // p, so the streaming of position j+1 overlaps the decision on position j.
 // Rows read per sequence: those of positions 0..min(k+1, gamma) after a
 // rejection at k (2 gamma + 1 when all drafts are accepted).  The final
-// sample runs the usual zsum / wsum / search kernels.
+// sample runs the usual final-pass kernel.
 constexpr int kLazyCluster = 4;
 constexpr int kLazyDecWarps = 2;
 constexpr int kLazyThreads = kRingThreads + 32 * kLazyDecWarps;
@@ -808,6 +837,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const Veri
         d.md = (k >= 0 && k < a.gamma) ? s_Md : 0.f;
         d.rt = (k >= 0 && k < a.gamma) ? s_Rt : 0.f;
         a.desc[b] = d;
+        a.tick[b] = 0u;
     }
     for (int i = t; i <= a.gamma; i += T)
         if (k < 0 || i != k)
@@ -860,33 +890,14 @@ static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- launch
-// Launch with programmatic stream serialisation: the kernel may start while
-// its predecessor drains and waits (griddepcontrol.wait) for its results.
-template <typename K>
-static cudaError_t launch_pdl(K kfn, dim3 grid, int threads, const VerifyArgs& a, cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kfn, a);
-}
-
 template <int ELT, bool VEC>
 static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool decide = true) {
     cudaError_t e = cudaSuccess;
     if (decide) {
-        e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, a, st);
+        e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, 0, st, a);
         if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(sample_zsum_kernel<ELT, VEC>, dim3(a.B, a.C), kCT, a, st);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(sample_search_kernel<ELT, VEC>, dim3(a.B), kCT, a, st);
+    return launch_pdl(sample_final_kernel<ELT, VEC>, dim3(a.C, a.B), kCT, 0, st, a);
 }
 
 cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
@@ -920,6 +931,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     a.C = final_chunks(V);
     a.parts = reinterpret_cast<float2*>(w + L.part_off);
     a.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
+    a.tick = reinterpret_cast<unsigned*>(w + L.tick_off);
     a.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
     a.wsum = reinterpret_cast<float4*>(w + L.wsum_off);
     a.err = reinterpret_cast<int*>(w + L.err_off);

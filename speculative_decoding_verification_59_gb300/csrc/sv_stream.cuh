@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         mbar_init_fence();
     }
     __syncthreads();
+    pdl_wait();                 // the kernel before may still read this workspace or write the rows
 
     if (warp == 0) {
         // ---- producer: one lane issues the bulk copies
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
 
     unsigned c0, c1;
     cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
+    pdl_wait();                 // the kernel before may still read this workspace or write the rows
     for (unsigned c = c0; c < c1; ++c) {
         if (c + 1 == c1) pdl_trigger();
         const unsigned rr = c / (unsigned)a.nseg;
@@ -577,8 +579,7 @@ cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_
         }
         long long g = (long long)di.sm_count * occ;
         if (a.total_chunks < g) g = a.total_chunks;
-        kfn<<<(int)g, kRingThreads, smem, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kfn, dim3((unsigned)g), kRingThreads, smem, st, a);
     }
     auto kfn = reg_stream_kernel<ELT, false, MODE>;
     static int occ = 0;
@@ -589,8 +590,7 @@ cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_
     }
     long long g = (long long)di.sm_count * occ;
     if (a.total_chunks < g) g = a.total_chunks;
-    kfn<<<(int)g, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kfn, dim3((unsigned)g), kThreads, 0, st, a);
 }
 
 }  // namespace sv

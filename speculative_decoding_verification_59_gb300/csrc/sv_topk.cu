@@ -98,16 +98,8 @@ static cudaError_t launch_topk_t(const VerifyArgs& a, int elt, int K, const int3
     constexpr int MODE = KC == 2 ? kModeTopK2 : KC == 4 ? kModeTopK4 : kModeTopK8;
     cudaError_t e = elt == 2 ? launch_stream<2, MODE>(a, di, st) : launch_stream<4, MODE>(a, di, st);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.B + kTopkRowsPerCta - 1) / kTopkRowsPerCta, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_merge_kernel<KC>, a, K, exclude, out_val);
+    return launch_pdl(topk_merge_kernel<KC>, dim3((a.B + kTopkRowsPerCta - 1) / kTopkRowsPerCta),
+                      kThreads, 0, st, a, K, exclude, out_val);
 }
 
 cudaError_t launch_topk(const void* logits, spec_dtype_t dt, int rows, int V, int K,
