@@ -243,15 +243,19 @@ def run_own(args):
 
     def calls(s, ev=None):
         c0, c1, c2 = copies[s % rot], copies[(s + 1) % rot], copies[(s + 2) % rot]
-        if ev is not None:
+        if ev is None:
+            check(sv.spec_verify_sample(P(c0["zt"]), P(c0["zd"]), dcode, P(c0["x"]), P(c0["u"]),
+                                        x.T, B, g, V, P(out["s_tok"]), P(out["s_acc"]), None, wp,
+                                        wb, sh), "sample")
+        else:
+            # the same work as its two halves, with events around the stats stream
             ev[0].record(stream)
-        check(sv.spec_verify_sample_stats(P(c0["zt"]), P(c0["zd"]), dcode, x.T, B, g, V, wp, wb,
-                                          sh), "stats")
-        if ev is not None:
+            check(sv.spec_verify_sample_stats(P(c0["zt"]), P(c0["zd"]), dcode, x.T, B, g, V, wp,
+                                              wb, sh), "stats")
             ev[1].record(stream)
-        check(sv.spec_verify_sample_finish(P(c0["zt"]), P(c0["zd"]), dcode, P(c0["x"]), P(c0["u"]),
-                                           x.T, B, g, V, P(out["s_tok"]), P(out["s_acc"]), None,
-                                           wp, wb, sh), "finish")
+            check(sv.spec_verify_sample_finish(P(c0["zt"]), P(c0["zd"]), dcode, P(c0["x"]),
+                                               P(c0["u"]), x.T, B, g, V, P(out["s_tok"]),
+                                               P(out["s_acc"]), None, wp, wb, sh), "finish")
         check(sv.spec_verify_greedy(P(c1["zt"]), dcode, P(c1["x"]), B, g, V, P(out["g_tok"]),
                                     P(out["g_acc"]), wp, wb, sh), "greedy")
         check(sv.spec_verify_tree_greedy(P(c2["zt"]), dcode, P(c2["tt"]), P(c2["tp"]), B, g + 1, V,
@@ -302,6 +306,17 @@ def run_own(args):
     torch.cuda.synchronize(dev)
     t_wall2 = time.time()
     stats_ms = [a.elapsed_time(b) for a, b in evs]
+    # ---- context: the stats kernel alone, K back-to-back launches between two
+    # events (no event between launches, so each overlaps the previous one's tail)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for s in range(K):
+        c0 = copies[s % rot]
+        check(sv.spec_verify_sample_stats(P(c0["zt"]), P(c0["zd"]), dcode, x.T, B, g, V, wp, wb,
+                                          sh), "stats")
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    stats_alone_ms = a0.elapsed_time(a1) / K
     barrier()
     clk = clocks.summary(t_wall0, t_wall2)
 
@@ -399,8 +414,8 @@ def run_own(args):
             "config": {
                 "workload": args.workload,
                 "B": B, "gamma": g, "V": V, "logits": x.dtype, "temperature": x.T,
-                "step": "sample (stats+finish) + greedy + chain-shaped tree, each on its own "
-                        "rotating input copy",
+                "step": "spec_verify_sample + spec_verify_greedy + spec_verify_tree_greedy "
+                        "(chain-shaped tree), each on its own rotating input copy",
                 "l2": f"{rot} rotating input copies of {acct['bytes_stats'] / 1e6:.1f} MB "
                       f"({rot * acct['bytes_stats'] / 129e6:.1f}x the 129 MB L2 in all)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -423,6 +438,9 @@ def run_own(args):
                 "timing": "CUDA events around each of the K stats launches of a second pass "
                           "over the timed steps (the first pass, which gives value, records "
                           "no events between calls)",
+                "alone": {"launch_ms_mean": stats_alone_ms,
+                          "frac": acct["bytes_stats"] / (stats_alone_ms * 1e-3) / 1e9 / peak,
+                          "how": "K back-to-back stats launches between two events"},
             },
             "e2e": {
                 "value": job_rate(world, acct["rows"], Ke, e2e_ms),

@@ -243,14 +243,17 @@ __device__ __forceinline__ FF warp_incl_scan_ff(FF a) {
 }
 
 // ---- programmatic dependent launch -------------------------------------------
-// Every kernel of the library is launched with programmatic stream
-// serialisation (launch_pdl): it may begin launching once every CTA of the
-// kernel before it in the stream has triggered (or exited), and it waits (in
-// hardware, griddepcontrol.wait) until that kernel has completed and its
-// writes are visible before it touches global memory that the earlier kernel
-// may read or write.  The streaming kernels trigger when each CTA is on its
-// last chunk, the small kernels on entry.  Both instructions are no-ops for a
-// kernel launched without the attribute.
+// The kernels of the library are launched with programmatic stream
+// serialisation (launch_pdl; the lazy pass adds the attribute to its cluster
+// launch): a kernel may begin launching once every CTA of the kernel before
+// it in the stream has triggered (or exited), and it waits (in hardware,
+// griddepcontrol.wait) until that kernel has completed and its writes are
+// visible before it touches global memory that the earlier kernel may write,
+// or may still read.  A kernel may load the call's own inputs before waiting
+// only when the kernel before it is the call's own first kernel, which waited
+// for its predecessor before it triggered.  The streaming kernels trigger
+// when each CTA is on its last chunk, the small kernels on entry.  Both
+// instructions are no-ops for a kernel launched without the attribute.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -48,6 +48,7 @@ __device__ __forceinline__ f32x2 vec_pair(const uint4& v, int i) {
 
 template <int ELT>
 __global__ void __launch_bounds__(kCosThreads) cosine_scores_kernel(const CosArgs a) {
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int r0 = blockIdx.y * kCosRowsPerCta;
@@ -132,9 +133,8 @@ cudaError_t launch_cosine(const void* hidden, const void* query, spec_dtype_t dt
     a.out_pos = out_pos;
     a.out_score = out_score;
     const dim3 grid((unsigned)B, (unsigned)((W + kCosRowsPerCta - 1) / kCosRowsPerCta), 1);
-    if (dt == SPEC_DTYPE_BF16) cosine_scores_kernel<2><<<grid, kCosThreads, 0, st>>>(a);
-    else cosine_scores_kernel<4><<<grid, kCosThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = dt == SPEC_DTYPE_BF16 ? launch_pdl(cosine_scores_kernel<2>, grid, kCosThreads, 0, st, a)
+                                          : launch_pdl(cosine_scores_kernel<4>, grid, kCosThreads, 0, st, a);
     if (e != cudaSuccess) return e;
     const dim3 tgrid((B + kCosTopWarps - 1) / kCosTopWarps);
     const int KC = topk_list_len(delta);

@@ -55,6 +55,8 @@ struct VerifyArgs {
     long long total_chunks;
     int B;
     int C;                     // sampling: final-pass chunks per row
+    int early_inputs;          // sampling: the decide kernel follows this call's own stream, so it
+                               // may load the call's inputs before griddepcontrol.wait
     float2* parts;             // per-warp-chunk partials
     SampleDesc* desc;          // sampling: rejection index and row maxima
     unsigned* tick;            // sampling: per-sequence count of finished final-pass chunks
@@ -148,6 +150,7 @@ template <int ELT>
 __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
     const int lane = gt & 31, gw = gt >> 5;
     const size_t rowbytes = (size_t)a.V * ELT;
+    if (!a.early_inputs) pdl_wait();   // first kernel of the call: the kernel before may write the inputs
     // Issue the gathers of z[x_i] first: their latency overlaps the merges.
     int xi = -1;
     float ztx = 0.f, zdx = 0.f;

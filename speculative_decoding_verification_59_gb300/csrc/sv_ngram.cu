@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kNgThreads) ngram_scan_kernel(const NgArgs a) 
     __shared__ int q[kNgMaxW];
     __shared__ int wsum[kNgThreads / 32];
     __shared__ int s_last;
+    pdl_wait();
     const int b = blockIdx.x / a.S, s = blockIdx.x % a.S, tid = threadIdx.x;
     const int32_t* t = a.tok + (size_t)b * a.n_max;
     const int n = a.len[b];
@@ -232,8 +233,7 @@ cudaError_t launch_ngram(const int32_t* tokens, const int32_t* lengths, int B, i
     a.out_count = out_count;
     a.out_matches = out_matches;
     a.out_draft = out_draft;
-    ngram_scan_kernel<<<(unsigned)(B * S), kNgThreads, 0, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(ngram_scan_kernel, dim3((unsigned)(B * S)), kNgThreads, 0, st, a);
     if (e != cudaSuccess) return e;
     return launch_pdl(ngram_merge_kernel, dim3((B + kNgMergeWarps - 1) / kNgMergeWarps),
                       kNgMergeWarps * 32, 0, st, a);

@@ -550,7 +550,7 @@ __device__ __forceinline__ unsigned take_ticket(unsigned* t) {
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a) {
     __shared__ FinalSmem sm;
-    const int c = blockIdx.x, b = blockIdx.y;
+    const int b = blockIdx.x / a.C, c = blockIdx.x - b * a.C;   // chunks of a sequence adjacent
     pdl_trigger();
     pdl_wait();
     const SampleDesc d = a.desc[b];
@@ -650,6 +650,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const Veri
     unsigned sg0, sg1;
     cta_range((unsigned)a.nseg, rank, kLazyCluster, &sg0, &sg1);
     const unsigned nmine = sg1 - sg0;                     // this CTA's block chunks of a row
+    pdl_wait();
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -879,13 +880,15 @@ static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(kLazyThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kLazyCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kfn, a);
 }
 
@@ -897,7 +900,8 @@ static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool dec
         e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, 0, st, a);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(sample_final_kernel<ELT, VEC>, dim3(a.C, a.B), kCT, 0, st, a);
+    return launch_pdl(sample_final_kernel<ELT, VEC>, dim3((unsigned)a.C * (unsigned)a.B), kCT, 0, st,
+                      a);
 }
 
 cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const int32_t* x,
@@ -939,6 +943,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     a.out_acc = out_acc;
     a.out_lp = out_lp;
 
+    a.early_inputs = (parts & kSampleStats) ? 1 : 0;
     bool mask_lp = false;
     if (parts & kSampleLazy) {
         if (vec) {
@@ -947,6 +952,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
             return elt == 2 ? launch_final_t<2, true>(a, st, false) : launch_final_t<4, true>(a, st, false);
         }
         parts = kSampleStats | kSampleFinish;             // full pass, then unread positions cleared
+        a.early_inputs = 1;
         mask_lp = out_lp != nullptr;
     }
     if (parts & kSampleStats) {

@@ -270,6 +270,14 @@ def test_sample_largest_vocabulary_and_beyond(sv):
     assert st == sv.SPEC_ERR_INVALID_ARG
 
 
+def test_sample_batch_beyond_grid_y_limit(sv):
+    """More sequences than a grid's y dimension holds (65535): the final-pass
+    kernel numbers its CTAs along x only."""
+    x = W.make_chain("chain-b256", B=70000, gamma=1, V=24)
+    res = check_sample(sv, x)
+    assert res["rows"] == 70000 * 2
+
+
 def test_no_device_error_on_valid_inputs(sv):
     """Valid calls of every mode leave the device error word clear (no bad
     input, and no bounded wait inside a kernel ever ran out)."""
