@@ -384,7 +384,8 @@ def run_own(args):
              "ngram_b64": time_ngram(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev,
                                      rank),
              "cosine_b64": time_cosine(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev,
-                                       rank)}
+                                       rank),
+             "tree_b32": time_tree(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev, rank)}
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
@@ -584,6 +585,52 @@ def time_cosine(sv, torch, W, stream, sh, steps, max_over_ranks, world, dev, ran
             "bytes_per_call": nbytes, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak,
             "peak_source": src, "l2": "2 rotating input copies, 252 MB in all (> L2)",
             "gpu_launches_per_call": 2}
+
+
+def time_tree(sv, torch, W, stream, sh, steps, max_over_ranks, world, dev, rank):
+    """Greedy draft-tree verification on the tree-b32 workload (32 sequences,
+    36-node trees: root, a 7-node main chain and 4 single-node branches at
+    each of its depths, V = 151936, bf16): every node's target row is read
+    once.  Two input copies of 350 MB rotate (700 MB, more than the L2)."""
+    t = W.make_tree("tree-b32", seed=W.WORKLOADS["tree-b32"].seed + 1000 * rank)
+    B, N, V = t.B, t.N, t.V
+    zs = [torch.from_numpy(t.target).to(dev).to(torch.bfloat16) for _ in range(2)]
+    tok = torch.from_numpy(t.node_tokens).to(dev)
+    par = torch.from_numpy(t.parents).to(dev)
+    nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    otok = torch.empty((B, N), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get(B, N, V)
+
+    def call(z):
+        st = sv.spec_verify_tree_greedy(z.data_ptr(), sv.SPEC_DTYPE_BF16, tok.data_ptr(),
+                                        par.data_ptr(), B, N, V, nodes.data_ptr(),
+                                        otok.data_ptr(), acc.data_ptr(), wp, wb, sh)
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, "tree")
+
+    for s in range(5):
+        call(zs[s % 2])
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        call(zs[s % 2])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+    nbytes = B * N * V * 2
+    peak, src = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    mean_acc = float(acc.float().mean().item())
+    del zs
+    return {"what": "greedy tree verification, 32 trees of 36 nodes (main chain of 7, "
+                    "4 branches per depth), V = 151936 bf16",
+            "ms_per_call": ms, "calls": steps, "rows_per_s": world * B * N / (ms * 1e-3),
+            "bytes_per_call": nbytes, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+            "peak_source": src, "mean_path_length": mean_acc,
+            "l2": "2 rotating input copies, 700 MB in all (> L2)", "gpu_launches_per_call": 2}
 
 
 def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, dev, acct):
