@@ -13,21 +13,15 @@ constexpr int kMaxNodesApi = 1024;
 constexpr float kMinTemperature = 1e-20f;   // log2(e)/T stays a finite float
 
 cudaError_t device_info(DeviceInfo* out) {
-    // Cached per device ordinal; the values are immutable properties.
-    static DeviceInfo cache[64];
-    static bool have[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // Immutable device properties, cached per device ordinal.
+    static DeviceSlots sms = {}, smem = {};
+    cudaError_t e = device_once(sms, &out->sm_count, [](int dev, int* v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+    });
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && have[dev]) { *out = cache[dev]; return cudaSuccess; }
-    DeviceInfo d;
-    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) { cache[dev] = d; have[dev] = true; }
-    *out = d;
-    return cudaSuccess;
+    return device_once(smem, &out->max_smem_optin, [](int dev, int* v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    });
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

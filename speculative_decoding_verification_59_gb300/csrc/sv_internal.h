@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "spec_verify.h"
 
 namespace sv {
@@ -80,6 +82,32 @@ struct DeviceInfo {
 };
 // Cached per-device properties (SM count and shared-memory limit).
 cudaError_t device_info(DeviceInfo* out);
+
+// A positive value computed once per device ordinal (a kernel's occupancy
+// after its shared-memory opt-in, say) and cached for later calls.  Several
+// host threads may race to compute it: setup must be idempotent and give the
+// same value each time; the cache slot is atomic.  Devices past kMaxDevices
+// are served uncached.
+constexpr int kMaxDevices = 64;
+using DeviceSlots = std::atomic<int>[kMaxDevices];
+
+template <typename F>
+inline cudaError_t device_once(DeviceSlots& slots, int* out, F setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int v = slots[dev].load(std::memory_order_acquire);
+        if (v > 0) { *out = v; return cudaSuccess; }
+    }
+    int v = 0;
+    e = setup(dev, &v);
+    if (e != cudaSuccess) return e;
+    if (v < 1) v = 1;
+    if (dev >= 0 && dev < kMaxDevices) slots[dev].store(v, std::memory_order_release);
+    *out = v;
+    return cudaSuccess;
+}
 
 // ---- launchers (return the first CUDA error) ------------------------------
 // parts: kSampleStats (streaming row statistics), kSampleFinish (the accept

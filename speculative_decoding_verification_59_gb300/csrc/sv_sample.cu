@@ -869,12 +869,13 @@ template <int ELT>
 static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
     auto kfn = lazy_sample_kernel<ELT>;
     const int smem = kStages * kStageBytes;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static DeviceSlots slots = {};                       // once per device: the opt-in
+    int done = 0;
+    cudaError_t e = device_once(slots, &done, [&](int, int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.B * kLazyCluster, 1, 1);
     cfg.blockDim = dim3(kLazyThreads, 1, 1);

@@ -568,26 +568,26 @@ cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_
     if (((size_t)a.V * ELT) % 16 == 0) {
         auto kfn = ring_stream_kernel<ELT, MODE>;
         const int smem = kStages * kStageBytes;
-        static int occ = 0;
-        if (occ == 0) {
-            cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            int o = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kRingThreads, smem) != cudaSuccess || o < 1)
-                o = 1;
-            occ = o;
-        }
+        // once per device: the shared-memory opt-in, then the occupancy it allows
+        static DeviceSlots slots = {};
+        int occ = 0;
+        cudaError_t e = device_once(slots, &occ, [&](int, int* o) {
+            cudaError_t r = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (r != cudaSuccess) return r;
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, kfn, kRingThreads, smem);
+        });
+        if (e != cudaSuccess) return e;
         long long g = (long long)di.sm_count * occ;
         if (a.total_chunks < g) g = a.total_chunks;
         return launch_pdl(kfn, dim3((unsigned)g), kRingThreads, smem, st, a);
     }
     auto kfn = reg_stream_kernel<ELT, false, MODE>;
-    static int occ = 0;
-    if (occ == 0) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kfn, kThreads, 0) != cudaSuccess || o < 1) o = 1;
-        occ = o;
-    }
+    static DeviceSlots slots = {};
+    int occ = 0;
+    cudaError_t e = device_once(slots, &occ, [&](int, int* o) {
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, kfn, kThreads, 0);
+    });
+    if (e != cudaSuccess) return e;
     long long g = (long long)di.sm_count * occ;
     if (a.total_chunks < g) g = a.total_chunks;
     return launch_pdl(kfn, dim3((unsigned)g), kThreads, 0, st, a);
