@@ -663,18 +663,51 @@ def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, de
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
     k = acc.cpu().numpy().astype(np.int64)
     elt = 2 if x.dtype == "bf16" else 4
-    # positions 0..min(k + 1, g) are read (one position of look-ahead past a
-    # rejection at k); position g holds the target row only
-    last = np.minimum(k + 1, g)
-    rows_read = int(np.where(last >= g, 2 * g + 1, 2 * (last + 1)).sum())
+    groups = lazy_groups(B, g, V * elt)
+    rows_read = int(sum(lazy_rows_read(int(kb), groups) for kb in k))
     bytes_read = rows_read * V * elt
-    return {"what": "lazy stochastic verification (rows after the first rejection not read) "
-                    "+ final sample, same inputs as the step",
+    return {"what": "lazy stochastic verification (rows of the position groups after the one "
+                    "holding the first rejection not read) + final sample, same inputs as the step",
             "ms_per_call": ms, "calls": steps,
             "rows_per_s": world * B * (g + 1) / (ms * 1e-3),
-            "pass1_rows_read_at_most": rows_read, "pass1_rows_full": B * (2 * g + 1),
-            "pass1_bytes_read_at_most": bytes_read, "pass1_bytes_full": acct["bytes_stats"],
-            "gpu_launches_per_call": 2}
+            "position_groups": [list(t) for t in groups],
+            "pass1_rows_read": rows_read, "pass1_rows_full": B * (2 * g + 1),
+            "pass1_bytes_read": bytes_read, "pass1_bytes_full": acct["bytes_stats"],
+            "gpu_launches_per_call": 2 * len(groups) + 1}
+
+
+def lazy_groups(B, g, rowbytes):
+    """Position groups of the lazy pass, as the library forms them: sizes
+    doubling from 2 ([0, 2), [2, 6), [6, 14), ...), the last one ending with
+    position g (the bonus row); a group runs on to the end (at most 128
+    positions) when the rows after it, for all B sequences, hold fewer than
+    96 MB (SPEC_VERIFY_LAZY_SPLIT_BYTES overrides the figure)."""
+    env = os.environ.get("SPEC_VERIFY_LAZY_SPLIT_BYTES", "")
+    try:
+        split = float(env) if env else 96.0 * (1 << 20)
+    except ValueError:
+        split = 96.0 * (1 << 20)
+    out, lo, n = [], 0, 2
+    while lo <= g and len(out) < 8:
+        hi = min(lo + min(n, 128), g + 1)
+        if B * rowbytes * ((g + 1 - hi) + (g - min(hi, g))) < split:
+            hi = min(lo + 128, g + 1)
+        out.append((lo, hi))
+        lo, n = hi, 2 * n
+    return out
+
+
+def lazy_rows_read(k, groups):
+    """Rows the lazy pass reads for a sequence finished at k (-1: bad input,
+    found in the first group): the target and draft rows of every group up
+    to the one holding k."""
+    g = groups[-1][1] - 1
+    rows = 0
+    for lo, hi in groups:
+        rows += (hi - lo) + (min(hi, g) - lo)
+        if k < hi:
+            break
+    return rows
 
 
 def oracle_slice(x, n, ttok, tpar, nthreads):

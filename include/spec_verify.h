@@ -126,15 +126,21 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
  * round", step 3: the first rejection discards every later draft, so a
  * position's rows are only needed while every earlier draft was accepted).
  * Same arguments, workspace and outputs as spec_verify_sample, with the same
- * tokens and accept counts; only the rows of positions 0..min(k + 1, gamma)
- * are read after a rejection at k (one position of look-ahead: position k+1
- * streams while position k is decided), all 2 gamma + 1 rows when every
- * draft is accepted.  out_logprobs (nullable) holds the
- * log-probabilities of positions 0..min(k, gamma - 1); later positions, and
- * every position of a bad sequence, are NaN.  One thread-block cluster per
- * sequence.  Rows whose byte length is not a multiple of 16 take the full
- * pass (every row read) with the same outputs.  Device-side bad-input
- * detection covers the rows it reads.
+ * tokens and accept counts.  The positions are streamed in groups of
+ * doubling size -- [0, 2), [2, 6), [6, 14), ... -- each group one pass over
+ * the GPU for the sequences whose drafts before it were all accepted, so
+ * after a rejection at k only the rows of the groups up to k's are read (at
+ * most positions 0..2k+1), all 2 gamma + 1 rows when every draft is
+ * accepted.  A group runs on to the end (at most 128 positions) when the
+ * rows after it, for all B sequences, hold fewer than 96 MB: a pass then
+ * costs more than it can save.  The environment variable
+ * SPEC_VERIFY_LAZY_SPLIT_BYTES overrides that figure (0: split at every
+ * boundary); the outputs do not depend on it.  out_logprobs (nullable)
+ * holds the log-probabilities of positions 0..min(k, gamma - 1); later
+ * positions, and every position of a bad sequence, are NaN.  Rows whose
+ * byte length is not a multiple of 16 take the full pass (every row read)
+ * with the same outputs.  Device-side bad-input detection covers the rows
+ * decided: positions 0..k.
  */
 spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* draft_logits,
                                       spec_dtype_t dtype, const int32_t* draft_tokens,

@@ -23,7 +23,8 @@ constexpr int kMaxGamma = 256;                   // sampling: rows per sequence 
 constexpr int kMaxNodes = 1024;                  // greedy chains and trees: rows <= 1024
 
 enum : int { kModeSample = 0, kModeGreedy = 1, kModeTree = 2,
-             kModeTopK2 = 3, kModeTopK4 = 4, kModeTopK8 = 5 };
+             kModeTopK2 = 3, kModeTopK4 = 4, kModeTopK8 = 5,
+             kModeLazy = 6 };     // sampling statistics of one position group (lazy pass)
 
 // List length of a top-K streaming mode (0 for the other modes).
 __host__ __device__ constexpr int topk_of(int mode) {
@@ -68,6 +69,18 @@ struct VerifyArgs {
     int32_t* out_acc;
     float* out_lp;             // sampling, nullable
     int32_t* out_nodes;        // trees
+    // Lazy sampling, one position group per stream + decide pair: target rows
+    // of positions [lz_lo, lz_lo + lz_nt) and draft rows of [lz_lo, lz_lo + lz_nd)
+    // of the sequences in lz_list[0 .. *lz_count) (every sequence, in order,
+    // when lz_list is null); the decide step appends the sequences that accept
+    // every draft of the group to lz_next_list / lz_next_count.  The first
+    // group's stream zeroes the lz_nzero counts at lz_zero.
+    int lz_lo, lz_nt, lz_nd, lz_nzero;
+    const int* lz_list;
+    const int* lz_count;
+    int* lz_next_list;
+    int* lz_next_count;
+    int* lz_zero;
 };
 
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

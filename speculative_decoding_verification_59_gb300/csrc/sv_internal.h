@@ -45,16 +45,24 @@ struct SampleDesc {
     float rt;     // rejection: Z_t / Z_d of row k from the row statistics (~1e-6 accurate)
 };
 
+// Lazy sampling streams the positions in groups of doubling size (2, 4, 8,
+// ...), the last group ending with target row gamma; gamma <= 256 needs at
+// most kLazyGroups of them.  Group g > 0 reads the survivor list that the
+// decide step of group g - 1 writes.
+constexpr int kLazyGroups = 8;
+
 // Workspace: [error word (256 bytes reserved) | per-warp row partials |
 // SampleDesc[B] | per-sequence finish tickets | per-segment normaliser sums |
-// per-segment residual sums and slopes].
+// per-segment residual sums and slopes | lazy survivor counts (256 bytes) and
+// lists [kLazyGroups, B]].
 // Every region after the error word is rewritten by the kernels of a call
 // before another kernel of that call reads it (the tickets are zeroed by the
-// kernel that writes the SampleDesc), so a workspace carries nothing from one
-// call to the next except the error word, which only accumulates error bits
-// until spec_verify_read_error clears it.
+// kernel that writes the SampleDesc, the survivor counts by the first lazy
+// stream), so a workspace carries nothing from one call to the next except
+// the error word, which only accumulates error bits until
+// spec_verify_read_error clears it.
 struct WsLayout {
-    size_t err_off, part_off, part_count, desc_off, tick_off, zsum_off, wsum_off, total;
+    size_t err_off, part_off, part_count, desc_off, tick_off, zsum_off, wsum_off, lz_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -72,7 +80,8 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     L.tick_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
     L.zsum_off = L.tick_off + align256(sizeof(int) * (size_t)B);
     L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * segs);
-    L.total = L.wsum_off + align256(4 * sizeof(float) * segs);
+    L.lz_off = L.wsum_off + align256(4 * sizeof(float) * segs);
+    L.total = L.lz_off + 256 + align256(sizeof(int) * (size_t)kLazyGroups * (size_t)B);
     return L;
 }
 

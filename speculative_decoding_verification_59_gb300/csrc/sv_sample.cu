@@ -34,6 +34,8 @@
 // 48 bits): the CDF each sequence samples from stays within ~1e-9 of the
 // exact one, which matters because the long tail of a 150K-token vocabulary
 // puts CDF boundaries ~1e-7 apart.
+#include <stdlib.h>
+
 #include "sv_stream.cuh"
 
 namespace sv {
@@ -578,278 +580,137 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
 // ------------------------------------------------ lazy (early-exit) pass 1
 // Source: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", section "What happens in one round", step 3: drafts are
-// checked left to right and the first rejection discards every later draft.
-// The lazy pass therefore reads a position's two rows only while the drafts
-// before it are accepted, give or take one position of look-ahead.
+// checked left to right and the first rejection discards every later draft,
+// so a position's rows are only needed while every earlier draft was
+// accepted.
 //
-// One thread-block cluster of kLazyCluster CTAs per sequence; each CTA takes
-// a fixed share of the block chunks of every row.  Per CTA:
-//   producer warp   lane 0 copies the CTA's chunks of position p (target row
-//                   p and draft row p; target row gamma last) into the same
-//                   kind of bulk-copy ring as the full pass, but only for
-//                   p <= (last position decided "accept") + 2;
-//   8 consumer warps turn the copied chunks into the full pass's per-warp
-//                   partials (warp_rowstats), position by position, exactly
-//                   the positions the producer issued;
-//   2 decision warps wait until every CTA of the cluster has the partials of
-//                   position j, merge its two rows (merge_row_stats) and take
-//                   the accept decision (accept_draft) -- the same arithmetic
-//                   as the full pass, in every CTA alike, so every decision
-//                   is bit-identical to it and all CTAs agree.
-// The cluster barrier is used split: each role arrives at phase p when its
-// part of position p is done and waits for phase p-1 only before arriving at
-// p, so the streaming of position j+1 overlaps the decision on position j.
-// Rows read per sequence: those of positions 0..min(k+1, gamma) after a
-// rejection at k (2 gamma + 1 when all drafts are accepted).  The final
-// sample runs the usual final-pass kernel.
-constexpr int kLazyCluster = 4;
-constexpr int kLazyDecWarps = 2;
-constexpr int kLazyThreads = kRingThreads + 32 * kLazyDecWarps;
-constexpr int kSmemSpinLimit = 1 << 22;
+// The positions go in groups of doubling size -- [0, 2), [2, 6), [6, 14), ...,
+// the last group ending with target row gamma -- and each group is one pass
+// over the whole GPU: the bulk-copy stream of sv_stream.cuh (kModeLazy) over
+// the group's target and draft rows of the sequences still undecided, then
+// lazy_decide_kernel, one CTA per such sequence, which merges those rows'
+// partials and takes the group's accept decisions in order.  A sequence
+// that rejects a draft (or reaches the bonus row) is finished there -- every
+// output but the final token, and the SampleDesc of the final sample -- and
+// the others go on the next group's survivor list.  The partials are the full
+// pass's bit for bit (same block chunks, same arithmetic, same merge), so
+// every decision and log-probability is too.
+//
+// A rejection at k lies in a group [lo, hi) with hi <= 2 k + 2, so the rows
+// read are at most those of positions 0..2k+1, twice the exact early exit,
+// in O(log gamma) passes: one pass per position would pay a kernel boundary
+// per position, and one cluster of CTAs per sequence that streams and
+// decides position by position is bound by that chain's latency.
 
-__device__ __forceinline__ unsigned cluster_ctarank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The two decision warps only.
-__device__ __forceinline__ void decision_sync() {
-    asm volatile("bar.sync 2, %0;" ::"n"(32 * kLazyDecWarps) : "memory");
-}
+// Positions per group: at most 128 (gamma <= 256).
+constexpr int kLazyMaxGroup = kMaxGamma / 2;
 
-// Bounded wait on a condition over shared memory.
-template <typename Pred>
-__device__ __forceinline__ bool smem_wait(Pred pred) {
-    for (int i = 0; i < kSmemSpinLimit; ++i) {
-        if (pred()) return true;
-        __nanosleep(32);
-    }
-    return false;
-}
+struct LazyDecideSmem {
+    float M[2 * kLazyMaxGroup], lnZ[2 * kLazyMaxGroup];   // group rows: target, then draft
+    float lp[kLazyMaxGroup], lq[kLazyMaxGroup];
+    float u[kLazyMaxGroup], zt[kLazyMaxGroup], zd[kLazyMaxGroup];
+    int bad, k;
+};
 
+// One CTA per sequence of the group's list (every sequence for the first
+// group).  k is the rejection index, gamma when the group holds the bonus row
+// and every draft was accepted, -1 for bad input, -2 for "undecided: next
+// group".
 template <int ELT>
-__global__ void __launch_bounds__(kLazyThreads, 2) lazy_sample_kernel(const VerifyArgs a) {
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ float sM[2], slnZ[2], s_Mt, s_Md, s_Rt;
-    __shared__ float s_lp[kMaxGamma], s_lq[kMaxGamma];
-    __shared__ float s_zt[kMaxGamma], s_zd[kMaxGamma];   // z^t_i[x_i], z^d_i[x_i], gathered up front
-    __shared__ int s_bad, s_ok, s_k;
-    __shared__ volatile int s_limit, s_stop, s_issued, s_pdone;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned rank = cluster_ctarank();
-    const int b = blockIdx.x / kLazyCluster;
+__global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a) {
+    __shared__ LazyDecideSmem sm;
+    const int gt = threadIdx.x, lane = gt & 31, gw = gt >> 5;
+    const int lo = a.lz_lo, nt = a.lz_nt, nd = a.lz_nd;
     const size_t rowbytes = (size_t)a.V * ELT;
-    const int P = a.nseg * kWarps;
-    unsigned sg0, sg1;
-    cta_range((unsigned)a.nseg, rank, kLazyCluster, &sg0, &sg1);
-    const unsigned nmine = sg1 - sg0;                     // this CTA's block chunks of a row
-    pdl_wait();
-
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < kStages; ++st) {
-            mbar_init(&full[st], 1);
-            mbar_init(&empty[st], kWarps);
+    const bool first = a.lz_list == nullptr;
+    pdl_trigger();
+    auto gather = [&](int b) {
+        for (int q = gt; q < nd; q += kGroup) {
+            const int p = lo + q;
+            const int xi = a.x[(size_t)b * a.gamma + p];
+            const bool in = xi >= 0 && xi < a.V;
+            sm.zt[q] = in ? load_logit<ELT>(sample_row(a, b, p, rowbytes), xi) : 0.f;
+            sm.zd[q] = in ? load_logit<ELT>(sample_row(a, b, a.gamma + 1 + p, rowbytes), xi) : 0.f;
+            sm.u[q] = a.u[(size_t)b * (a.gamma + 1) + p];
         }
-        mbar_init_fence();
-        int bad = 0;
-        for (int i = 0; i < a.gamma; ++i) {
+    };
+    int b = blockIdx.x, bad = 0;
+    if (first) {
+        // Inputs only: this group's stream waited for the kernel before the
+        // call, so they are final.  Every draft token of the sequence is
+        // checked here, as the full pass's decision does.
+        gather(b);
+        for (int i = gt; i < a.gamma; i += kGroup) {
             const int xi = a.x[(size_t)b * a.gamma + i];
-            if (xi < 0 || xi >= a.V) bad = SPEC_DEVERR_TOKEN_RANGE;
+            if (xi < 0 || xi >= a.V) bad = 1;
         }
-        s_bad = bad;
-        s_ok = 1;
-        s_k = -1;
-        s_Mt = s_Md = s_Rt = 0.f;
-        s_limit = 1;
-        s_stop = 0;
-        s_issued = -1;
-        s_pdone = 0;
     }
-    for (int i = threadIdx.x; i < a.gamma; i += blockDim.x) {
-        const int xi = a.x[(size_t)b * a.gamma + i];
-        const bool in = xi >= 0 && xi < a.V;
-        s_zt[i] = in ? load_logit<ELT>(sample_row(a, b, i, rowbytes), xi) : 0.f;
-        s_zd[i] = in ? load_logit<ELT>(sample_row(a, b, a.gamma + 1 + i, rowbytes), xi) : 0.f;
+    pdl_wait();                                           // the group's partials and list
+    if (!first) {
+        if ((int)blockIdx.x >= __ldcg(a.lz_count)) return;   // the whole CTA
+        b = __ldcg(a.lz_list + blockIdx.x);
+        gather(b);
+    }
+    for (int q = gw; q < nt + nd; q += kGroup / 32) {
+        const int r = q < nt ? lo + q : a.gamma + 1 + lo + (q - nt);
+        float M, lnZ;
+        merge_row_stats(a, b, r, lane, &M, &lnZ);
+        if (lane == 0) {
+            sm.M[q] = M;
+            sm.lnZ[q] = lnZ;
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (gt == 0) {
+        int k = -2, bits = bad ? SPEC_DEVERR_TOKEN_RANGE : 0;
+        for (int q = 0; !bits && q < nt; ++q) {
+            if (sm.M[q] == kNegInf || (q < nd && sm.M[nt + q] == kNegInf)) {
+                bits = SPEC_DEVERR_EMPTY_ROW;
+                break;
+            }
+            if (q == nd) { k = a.gamma; break; }          // target row gamma: every draft accepted
+            sm.lp[q] = row_log_prob(sm.zt[q], sm.M[q], sm.lnZ[q], a);
+            sm.lq[q] = row_log_prob(sm.zd[q], sm.M[nt + q], sm.lnZ[nt + q], a);
+            if (!accept_draft(sm.lp[q], sm.lq[q], sm.u[q])) { k = lo + q; break; }
+        }
+        sm.bad = bits;
+        sm.k = bits ? -1 : k;
     }
     __syncthreads();
-    pdl_trigger();
-    // rows of position p: chunk cc < nmine of target row p, else of draft row p
-    auto row_of = [&](unsigned cc, int p) { return cc < nmine ? p : a.gamma + 1 + p; };
-
-    if (!s_bad) {
-        if (warp == 0) {
-            // ---- producer
-            unsigned issued = 0;
-            bool ok = true;
-            for (int p = 0; p <= a.gamma; ++p) {
-                int go = 0;
-                if (lane == 0) {
-                    if (!smem_wait([&] { return s_stop != 0 || p <= s_limit; })) ok = false;
-                    go = ok && !s_stop;
-                    if (go) s_issued = p;
-                    else s_pdone = 1;
-                    __threadfence_block();
-                    const unsigned nchunks = (p < a.gamma ? 2u : 1u) * nmine;
-                    for (unsigned cc = 0; go && cc < nchunks; ++cc, ++issued) {
-                        const int st = (int)(issued % kStages);
-                        const unsigned use = issued / kStages;
-                        if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        const int seg = (int)(sg0 + cc % nmine);
-                        const size_t off = (size_t)seg * kStageBytes;
-                        const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
-                        mbar_arrive_expect_tx(&full[st], bytes);
-                        bulk_g2s(ring + (size_t)st * kStageBytes,
-                                 sample_row(a, b, row_of(cc, p), rowbytes) + off, bytes, &full[st]);
-                    }
-                    if (!ok) s_ok = 0;
-                }
-                go = __shfl_sync(0xffffffffu, go, 0);
-                if (!go) break;
-                if (p > 0) cluster_wait();
-                cluster_arrive();
+    const int k = sm.k;
+    if (a.out_lp && k != -1)                              // the positions decided here
+        for (int q = gt; q < nd; q += kGroup)
+            if (k == -2 || lo + q <= k) {
+                float* o = a.out_lp + ((size_t)b * a.gamma + lo + q) * 2;
+                o[0] = sm.lp[q];
+                o[1] = sm.lq[q];
             }
-            if (lane == 0) {
-                s_pdone = 1;
-                // copies still in flight must land before the CTA may exit
-                const unsigned first = issued > kStages ? issued - kStages : 0;
-                for (unsigned i = first; i < issued; ++i)
-                    if (!wait_bounded(&full[i % kStages], (i / kStages) & 1u)) {
-                        atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
-                        break;
-                    }
-            }
-        } else if (warp <= kWarps) {
-            // ---- consumers: the positions the producer issued, in order
-            const int cw = warp - 1;
-            unsigned it = 0;
-            bool ok = true;
-            for (int p = 0;; ++p) {
-                int have = 0;
-                if (lane == 0) {
-                    const bool w = smem_wait([&] { return s_issued >= p || s_pdone != 0; });
-                    have = w && s_issued >= p;
-                    if (!w) s_ok = 0;
-                }
-                have = __shfl_sync(0xffffffffu, have, 0);
-                if (!have) break;
-                const unsigned nchunks = (p < a.gamma ? 2u : 1u) * nmine;
-                for (unsigned cc = 0; cc < nchunks; ++cc, ++it) {
-                    const int st = (int)(it % kStages);
-                    if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
-                    const int seg = (int)(sg0 + cc % nmine);
-                    const size_t off = (size_t)seg * kStageBytes;
-                    const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
-                    const int wb = bytes - cw * (32 * kLaneBytes);
-                    const bool use = __all_sync(0xffffffffu, ok) && wb > 0;
-                    float2 part = make_float2(kNegInf, 0.f);
-                    if (use) {
-                        uint4 v[kVecPerLane];
-                        const unsigned char* chunk = ring + (size_t)st * kStageBytes + cw * (32 * kLaneBytes);
-                        if (wb >= 32 * kLaneBytes) {
-#pragma unroll
-                            for (int t = 0; t < kVecPerLane; ++t)
-                                v[t] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * t) * 16);
-                        } else {
-                            lane_words<ELT>(chunk, wb, v);
-                        }
-                        part = warp_rowstats<ELT>(v, a.s);
-                    }
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (ok) mbar_arrive(&empty[st]);
-                        a.parts[((size_t)b * a.rows_per_seq + row_of(cc, p)) * P + seg * kWarps + cw] = part;
-                    }
-                }
-                if (!ok && lane == 0) s_ok = 0;
-                if (p > 0) cluster_wait();
-                cluster_arrive();                         // this CTA's partials of position p are written
-            }
-        } else {
-            // ---- decision warps
-            const int dw = warp - (kWarps + 1);
-            for (int j = 0; j <= a.gamma; ++j) {
-                cluster_arrive();
-                cluster_wait();                           // every CTA's partials of position j are visible
-                if (dw == 0 || j < a.gamma) {
-                    float M, lnZ;
-                    merge_row_stats(a, b, dw == 0 ? j : a.gamma + 1 + j, lane, &M, &lnZ);
-                    if (lane == 0) { sM[dw] = M; slnZ[dw] = lnZ; }
-                }
-                decision_sync();
-                if (dw == 0 && lane == 0) {
-                    bool stop = true;
-                    if (!s_ok) {
-                        atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
-                        s_k = -1;
-                    } else if (sM[0] == kNegInf || (j < a.gamma && sM[1] == kNegInf)) {
-                        s_bad = SPEC_DEVERR_EMPTY_ROW;
-                        s_k = -1;
-                    } else if (j == a.gamma) {
-                        s_k = a.gamma;                    // every draft accepted
-                    } else {
-                        const float lp = row_log_prob(s_zt[j], sM[0], slnZ[0], a);
-                        const float lq = row_log_prob(s_zd[j], sM[1], slnZ[1], a);
-                        s_lp[j] = lp;
-                        s_lq[j] = lq;
-                        if (accept_draft(lp, lq, a.u[(size_t)b * (a.gamma + 1) + j])) {
-                            stop = false;
-                            s_limit = j + 2;
-                        } else {
-                            s_k = j;
-                        }
-                    }
-                    if (stop) {
-                        s_Mt = sM[0];
-                        s_Md = j < a.gamma ? sM[1] : 0.f;
-                        s_Rt = j < a.gamma ? expf(slnZ[0] - slnZ[1]) : 0.f;   // as the decide step
-                        s_stop = 1;
-                    }
-                    __threadfence_block();
-                }
-                decision_sync();
-                if (s_stop) break;                        // the same in both warps and every CTA
-            }
-        }
+    if (k == -2) {
+        if (gt == 0) a.lz_next_list[atomicAdd(a.lz_next_count, 1)] = b;
+        return;
     }
-    // ---- outputs of the sequence: the decision warps of CTA 0
-    if (rank != 0 || warp <= kWarps) return;
-    const int t = threadIdx.x - (kWarps + 1) * 32;
-    const int T = 32 * kLazyDecWarps;
-    int k = s_k;
-    if (s_bad) {
-        k = -1;
-        if (t == 0) atomicOr(a.err, s_bad);
-    }
-    if (t == 0) {
+    if (gt == 0) {
+        if (sm.bad) atomicOr(a.err, sm.bad);
         a.out_acc[b] = k;
         SampleDesc d;
         d.k = k;
-        d.mt = k >= 0 ? s_Mt : 0.f;
-        d.md = (k >= 0 && k < a.gamma) ? s_Md : 0.f;
-        d.rt = (k >= 0 && k < a.gamma) ? s_Rt : 0.f;
+        d.mt = k >= 0 ? sm.M[k - lo] : 0.f;
+        d.md = (k >= 0 && k < a.gamma) ? sm.M[nt + k - lo] : 0.f;
+        d.rt = (k >= 0 && k < a.gamma) ? expf(sm.lnZ[k - lo] - sm.lnZ[nt + k - lo]) : 0.f;   // as the decide step
         a.desc[b] = d;
         a.tick[b] = 0u;
     }
-    for (int i = t; i <= a.gamma; i += T)
+    // accepted drafts and padding; slot k belongs to the final-pass search
+    for (int i = gt; i <= a.gamma; i += kGroup)
         if (k < 0 || i != k)
             a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
-    if (a.out_lp)
-        for (int i = t; i < a.gamma; i += T) {
-            float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
-            const bool have = k >= 0 && i <= k;           // positions decided
-            o[0] = have ? s_lp[i] : CUDART_NAN_F;
-            o[1] = have ? s_lq[i] : CUDART_NAN_F;
-        }
+    if (a.out_lp)                                         // positions never decided
+        for (int i = gt; i < a.gamma; i += kGroup)
+            if (k < 0 || i > k) {
+                float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
+                o[0] = CUDART_NAN_F;
+                o[1] = CUDART_NAN_F;
+            }
 }
 
 // Rows that are not a multiple of 16 bytes take the full pass in lazy mode;
@@ -865,32 +726,68 @@ __global__ void lazy_mask_logprobs_kernel(const VerifyArgs a) {
         }
 }
 
+// A group boundary costs a pass: a stream and a decide kernel, about 7 us of
+// ramp and latency on GB300.  It pays when the sequences that stop before it
+// skip more HBM time than that; with half of them stopping, when the rows
+// after the boundary (for every sequence) hold at least 2 x 7 us x 6.7 TB/s,
+// about 96 MB.  Below that the group runs on to the end.  The environment
+// variable SPEC_VERIFY_LAZY_SPLIT_BYTES overrides the figure (0: always
+// split); outputs do not depend on it.
+constexpr double kLazySplitBytes = 96.0 * (1 << 20);
+
+static double lazy_split_bytes() {
+    const char* e = getenv("SPEC_VERIFY_LAZY_SPLIT_BYTES");
+    if (!e || !*e) return kLazySplitBytes;
+    char* end = nullptr;
+    const double v = strtod(e, &end);
+    return (end && *end == '\0' && v >= 0.0) ? v : kLazySplitBytes;
+}
+
+// Upper ends of the lazy position groups: sizes doubling from 2, a group
+// running on to the end (at most kLazyMaxGroup positions) when the rows after
+// it are too few to be worth a pass.  Every group has at least the doubling
+// size, so gamma <= 256 takes at most kLazyGroups of them.  Returns the count.
+static int lazy_group_ends(int B, int gamma, size_t rowbytes, int (&hi)[kLazyGroups]) {
+    const double split = lazy_split_bytes();
+    int ng = 0;
+    for (int lo = 0, n = 2; lo <= gamma && ng < kLazyGroups; n *= 2) {
+        int h = min(lo + min(n, kLazyMaxGroup), gamma + 1);
+        const double rest = (double)B * (double)rowbytes *
+                            (double)((gamma + 1 - h) + (gamma - min(h, gamma)));
+        if (rest < split) h = min(lo + kLazyMaxGroup, gamma + 1);
+        hi[ng++] = h;
+        lo = h;
+    }
+    return ng;
+}
+
+// The lazy pass: per position group a stream and a decide kernel, chained
+// with programmatic dependent launch; the first group's stream zeroes the
+// later groups' survivor counts.
 template <int ELT>
-static cudaError_t launch_lazy(const VerifyArgs& a, cudaStream_t st) {
-    auto kfn = lazy_sample_kernel<ELT>;
-    const int smem = kStages * kStageBytes;
-    static DeviceSlots slots = {};                       // once per device: the opt-in
-    int done = 0;
-    cudaError_t e = device_once(slots, &done, [&](int, int* v) {
-        *v = 1;
-        return cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    });
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.B * kLazyCluster, 1, 1);
-    cfg.blockDim = dim3(kLazyThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kLazyCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kfn, a);
+static cudaError_t launch_lazy(VerifyArgs a, const DeviceInfo& di, cudaStream_t st, char* lz) {
+    int* counts = reinterpret_cast<int*>(lz);
+    int* lists = reinterpret_cast<int*>(lz + 256);
+    int ends[kLazyGroups];
+    const int ngroups = lazy_group_ends(a.B, a.gamma, (size_t)a.V * ELT, ends);
+    for (int g = 0, lo = 0; g < ngroups; lo = ends[g], ++g) {
+        const int hi = ends[g];
+        a.lz_lo = lo;
+        a.lz_nt = hi - lo;
+        a.lz_nd = min(hi, a.gamma) - lo;
+        a.lz_list = g > 0 ? lists + (size_t)g * a.B : nullptr;
+        a.lz_count = g > 0 ? counts + g : nullptr;
+        a.lz_next_list = g + 1 < ngroups ? lists + (size_t)(g + 1) * a.B : nullptr;
+        a.lz_next_count = g + 1 < ngroups ? counts + g + 1 : nullptr;
+        a.lz_zero = counts + 1;
+        a.lz_nzero = g == 0 ? ngroups - 1 : 0;
+        a.total_chunks = (long long)a.B * (a.lz_nt + a.lz_nd) * a.nseg;   // at most
+        cudaError_t e = launch_stream<ELT, kModeLazy>(a, di, st);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(lazy_decide_kernel<ELT>, dim3((unsigned)a.B), kGroup, 0, st, a);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // ---------------------------------------------------------------- launch
@@ -948,7 +845,8 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     bool mask_lp = false;
     if (parts & kSampleLazy) {
         if (vec) {
-            e = elt == 2 ? launch_lazy<2>(a, st) : launch_lazy<4>(a, st);
+            char* lz = w + L.lz_off;
+            e = elt == 2 ? launch_lazy<2>(a, di, st, lz) : launch_lazy<4>(a, di, st, lz);
             if (e != cudaSuccess) return e;
             return elt == 2 ? launch_final_t<2, true>(a, st, false) : launch_final_t<4, true>(a, st, false);
         }

@@ -28,9 +28,36 @@ constexpr int kStages = 3;
 constexpr int kRingThreads = (kWarps + 1) * 32;
 constexpr int kStageBytes = kWarps * 32 * kLaneBytes;     // 32 KB block chunk
 
+// Row rr of a stream as the index of its partials' row (for sampling and
+// lazy groups: sequence-major, 2 gamma + 1 rows per sequence), and that row's
+// logits.  Only a lazy group maps: its row space is survivor i's target rows
+// of the group's positions, then its draft rows.  The survivor lookup is
+// cached, consecutive rows mostly belonging to one sequence.
+struct StreamRows {
+    unsigned seq_i = 0xffffffffu;
+    int seq_b = 0;
+
+    template <int MODE>
+    __device__ __forceinline__ unsigned part_row(const VerifyArgs& a, unsigned rr) {
+        if constexpr (MODE == kModeLazy) {
+            const unsigned nr = (unsigned)(a.lz_nt + a.lz_nd);
+            const unsigned i = rr / nr;
+            const int q = (int)(rr - i * nr);
+            if (i != seq_i) {
+                seq_i = i;
+                seq_b = a.lz_list ? __ldcg(a.lz_list + i) : (int)i;
+            }
+            const int r = q < a.lz_nt ? a.lz_lo + q : a.gamma + 1 + a.lz_lo + (q - a.lz_nt);
+            return (unsigned)seq_b * (unsigned)a.rows_per_seq + (unsigned)r;
+        } else {
+            return rr;
+        }
+    }
+};
+
 template <int MODE>
 __device__ __forceinline__ const char* stream_row(const VerifyArgs& a, unsigned rr, size_t rowbytes) {
-    if constexpr (MODE == kModeSample) {
+    if constexpr (MODE == kModeSample || MODE == kModeLazy) {
         const unsigned b = rr / (unsigned)a.rows_per_seq;
         return sample_row(a, (int)b, (int)(rr - b * (unsigned)a.rows_per_seq), rowbytes);
     } else {
@@ -364,7 +391,6 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     constexpr int KT = topk_of(MODE);
     const size_t rowbytes = (size_t)a.V * ELT;
     const int P = a.nseg * kWarps;
-    const unsigned total = (unsigned)a.total_chunks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -375,6 +401,12 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     }
     __syncthreads();
     pdl_wait();                 // the kernel before may still read this workspace or write the rows
+    unsigned total = (unsigned)a.total_chunks;
+    if constexpr (MODE == kModeLazy) {
+        if (a.lz_count) total = (unsigned)__ldcg(a.lz_count) * (unsigned)(a.lz_nt + a.lz_nd) * (unsigned)a.nseg;
+        if (blockIdx.x == 0 && (int)threadIdx.x < a.lz_nzero) a.lz_zero[threadIdx.x] = 0;
+    }
+    StreamRows rows;
 
     if (warp == 0) {
         // ---- producer: one lane issues the bulk copies
@@ -391,8 +423,9 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
                 const size_t off = (size_t)seg * kStageBytes;
                 const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
                 if (c + 1 == c1) pdl_trigger();
+                const unsigned pr = rows.part_row<MODE>(a, rr);
                 mbar_arrive_expect_tx(&full[st], bytes);
-                bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, rr, rowbytes) + off, bytes,
+                bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, pr, rowbytes) + off, bytes,
                          &full[st]);
             }
             if (!ok) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
@@ -418,6 +451,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
         const unsigned rr = c / (unsigned)a.nseg;
         const int seg = (int)(c - rr * (unsigned)a.nseg);
+        const unsigned pr = rows.part_row<MODE>(a, rr);
         const size_t off = (size_t)seg * kStageBytes;
         const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
         const int wb = bytes - cw * (32 * kLaneBytes);            // valid bytes of this warp chunk
@@ -434,14 +468,14 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
                 lane_words<ELT>(chunk, wb, v);
             }
             const int base = (int)(off / ELT) + cw * (32 * kLaneBytes / ELT);
-            if constexpr (MODE == kModeSample) part = warp_rowstats<ELT>(v, a.s);
+            if constexpr (MODE == kModeSample || MODE == kModeLazy) part = warp_rowstats<ELT>(v, a.s);
             else if constexpr (KT > 0)
                 warp_topk_chunk<ELT, KT>(v, chunk, wb, base,
                                          a.parts + ((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT));
             else part = warp_argmax_chunk<ELT>(v, base);
         } else {
-            part = MODE == kModeSample ? make_float2(kNegInf, 0.f)
-                                       : make_float2(kNegInf, __int_as_float(0x7fffffff));
+            part = (MODE == kModeSample || MODE == kModeLazy) ? make_float2(kNegInf, 0.f)
+                                                              : make_float2(kNegInf, __int_as_float(0x7fffffff));
             if constexpr (KT > 0)
                 if (lane < topk_slots(KT))
                     a.parts[((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT) + lane] = part;
@@ -449,7 +483,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         __syncwarp();
         if (lane == 0) {
             if (ok) mbar_arrive(&empty[st]);
-            if constexpr (KT == 0) a.parts[(size_t)rr * P + seg * kWarps + cw] = part;
+            if constexpr (KT == 0) a.parts[(size_t)pr * P + seg * kWarps + cw] = part;
         }
     }
     if (!ok && lane == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
@@ -581,16 +615,20 @@ cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_
         if (a.total_chunks < g) g = a.total_chunks;
         return launch_pdl(kfn, dim3((unsigned)g), kRingThreads, smem, st, a);
     }
-    auto kfn = reg_stream_kernel<ELT, false, MODE>;
-    static DeviceSlots slots = {};
-    int occ = 0;
-    cudaError_t e = device_once(slots, &occ, [&](int, int* o) {
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, kfn, kThreads, 0);
-    });
-    if (e != cudaSuccess) return e;
-    long long g = (long long)di.sm_count * occ;
-    if (a.total_chunks < g) g = a.total_chunks;
-    return launch_pdl(kfn, dim3((unsigned)g), kThreads, 0, st, a);
+    if constexpr (MODE == kModeLazy) {
+        return cudaErrorInvalidValue;      // lazy groups stream 16-byte rows only
+    } else {
+        auto kfn = reg_stream_kernel<ELT, false, MODE>;
+        static DeviceSlots slots = {};
+        int occ = 0;
+        cudaError_t e = device_once(slots, &occ, [&](int, int* o) {
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, kfn, kThreads, 0);
+        });
+        if (e != cudaSuccess) return e;
+        long long g = (long long)di.sm_count * occ;
+        if (a.total_chunks < g) g = a.total_chunks;
+        return launch_pdl(kfn, dim3((unsigned)g), kThreads, 0, st, a);
+    }
 }
 
 }  // namespace sv

@@ -96,3 +96,80 @@ def test_lazy_identical_models_read_every_position(sv):
     full, lazy = both(sv, x)
     check_same(full, lazy)
     assert (lazy[1] == x.gamma).all()
+
+
+@pytest.fixture
+def every_group(monkeypatch):
+    """Split at every group boundary whatever the sizes (the library otherwise
+    merges the groups of small problems into one pass)."""
+    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", "0")
+
+
+@pytest.mark.parametrize("gamma", [1, 2, 5, 6, 13, 14, 30])
+def test_lazy_group_boundaries(sv, every_group, gamma):
+    """Positions go in groups [0, 2), [2, 6), [6, 14), [14, 30), ...: draft
+    counts on either side of a boundary, with the chain-b64 generator's three
+    draft-noise levels (acceptance from ~0.3 to ~0.9) and fresh uniforms."""
+    x = W.make_chain("chain-b64", B=12, gamma=gamma, V=4096)
+    rng = np.random.default_rng(gamma)
+    for rnd in range(3):
+        u = x.uniforms if rnd == 0 else rng.random((x.B, x.gamma + 1), dtype=np.float32)
+        full, lazy = both(sv, x, u)
+        check_same(full, lazy)
+        ref = oracle.verify_sample(x.target, x.draft, x.draft_tokens, u, x.T, want_ratio=True,
+                                   want_cdf=True)
+        res = compare_sample(lazy[0], lazy[1], ref, x.draft_tokens, u)
+        assert not res["failures"], res["failures"][:5]
+
+
+def test_lazy_largest_gamma_every_group(sv, every_group):
+    """gamma = 256 (the most drafts a call takes) with p = q: every draft is
+    accepted, so all eight position groups run, the largest of 128 positions."""
+    x = W.make_chain("chain-b8", B=2, gamma=256, V=2048)
+    x.draft = x.target[:, :x.gamma].copy()
+    full, lazy = both(sv, x)
+    check_same(full, lazy)
+    assert (lazy[1] == x.gamma).all()
+
+
+def test_lazy_every_sequence_rejects_first_draft(sv, every_group):
+    """The first draft is the target's least likely token, on which the draft
+    model puts nearly all its mass (logit 40): p/q is ~0, so every sequence
+    rejects it and the later groups run with empty survivor lists."""
+    x = W.make_chain("chain-b8", B=6, gamma=7, V=8192)
+    x.draft, x.draft_tokens = x.draft.copy(), x.draft_tokens.copy()
+    for b in range(x.B):
+        j = int(np.argmin(x.target[b, 0]))
+        x.draft_tokens[b, 0] = j
+        x.draft[b, 0, j] = 40.0
+    full, lazy = both(sv, x)
+    check_same(full, lazy)
+    assert (lazy[1] == 0).all()
+
+
+def test_lazy_empty_row_in_a_later_group(sv, every_group):
+    """An all -inf target row at position 4 (the second group) of a sequence
+    whose drafts before it are all accepted: the sequence is bad (-1), as in
+    the full pass, and the error word says why."""
+    x = W.make_chain("chain-b8", B=3, gamma=7, V=4096)
+    x.draft = x.target[:, :x.gamma].copy()             # every draft accepted ...
+    x.target = x.target.copy()
+    x.target[1, 4, :] = -np.inf                        # ... until row 4 of sequence 1
+    x.draft[1, 4, :] = -np.inf
+    ws = sv.Workspace()
+    full, lazy = both(sv, x, ws=ws)
+    check_same(full, lazy)
+    assert lazy[1][1] == -1 and (lazy[0][1] == -1).all()
+    assert (lazy[1][[0, 2]] == x.gamma).all()
+    assert ws.read_error() & sv.SPEC_DEVERR_EMPTY_ROW
+
+
+@pytest.mark.parametrize("split", ["0", "100000000000"])
+def test_lazy_schedule_does_not_change_results(sv, monkeypatch, split):
+    """chain-b64 at full size with every boundary taken (three groups) and with
+    none (one group): the same tokens, counts and log-probabilities as the
+    full pass either way."""
+    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", split)
+    x = W.make_chain("chain-b64")
+    full, lazy = both(sv, x)
+    check_same(full, lazy)
