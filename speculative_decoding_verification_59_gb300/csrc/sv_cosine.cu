@@ -9,8 +9,9 @@
 // Algorithm 1 (SemanticFallback: top-delta positions).
 //
 // Each window row is read once: one warp per row accumulates h.q, h.h and
-// q.q in fp32 with packed f32x2 FMAs over 16-byte vectors (the query vector
-// comes through L1, shared by the CTA's warps).  A row with a zero norm, or
+// q.q in fp32 with packed f32x2 FMAs over 16-byte vectors, a batch of
+// kCosBatch vectors per lane loaded at once (the query vectors come through
+// L1, shared by the CTA's warps).  A row with a zero norm, or
 // a zero query, scores 0.  One warp per sequence then keeps the delta best
 // scores (larger first, lower window index first among equal scores) and
 // maps them to context positions.  The pass is a batched matrix-vector
@@ -20,8 +21,8 @@
 namespace sv {
 
 constexpr int kCosThreads = 256;
-constexpr int kCosRowsPerCta = 32;               // 4 rows per warp
-constexpr int kCosBatch = 4;                     // 16-byte vectors in flight per lane
+constexpr int kCosRowsPerCta = kCosThreads / 32; // one row per warp
+constexpr int kCosBatch = 4;                     // 16-byte vectors per lane per batch
 
 struct CosArgs {
     const char* H;            // [B, W, d]
@@ -46,45 +47,56 @@ __device__ __forceinline__ f32x2 vec_pair(const uint4& v, int i) {
     }
 }
 
+// One warp per window row.  A batch that lies wholly inside the row is
+// loaded without per-vector bounds tests, so its loads issue together; the
+// query vectors are read as they are used.  (One warp per row gives a grid of
+// B x W/8 CTAs, 1920 for the cosine-b64 windows: measured 26.7 us against
+// 31.6 us for four rows per warp.)
 template <int ELT>
 __global__ void __launch_bounds__(kCosThreads) cosine_scores_kernel(const CosArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
-    const int r0 = blockIdx.y * kCosRowsPerCta;
+    const int r = blockIdx.y * kCosRowsPerCta + warp;
+    if (r >= a.W) return;
     const int nvec = a.d * ELT / 16;
     constexpr int NP = 8 / ELT;                           // pairs per vector
-    const char* qrow = a.q + (size_t)b * a.d * ELT;
-    for (int r = r0 + warp; r < min(r0 + kCosRowsPerCta, a.W); r += kCosThreads / 32) {
-        const char* hrow = a.H + ((size_t)b * a.W + r) * a.d * ELT;
-        f32x2 dot = f2_pack(0.f, 0.f), nh = dot, nq = dot;
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kCosBatch) {
-            uint4 hv[kCosBatch], qv[kCosBatch];
+    const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (size_t)b * a.d * ELT);
+    const char* hrow = a.H + ((size_t)b * a.W + r) * a.d * ELT;
+    f32x2 dot = f2_pack(0.f, 0.f), nh = dot, nq = dot;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kCosBatch) {
+        uint4 hv[kCosBatch];
+        const bool whole = v0 + 32 * (kCosBatch - 1) < nvec;
+        if (whole) {
+#pragma unroll
+            for (int u = 0; u < kCosBatch; ++u) hv[u] = ld_stream16(hrow + (size_t)(v0 + 32 * u) * 16);
+        } else {
 #pragma unroll
             for (int u = 0; u < kCosBatch; ++u) {
                 const int v = v0 + 32 * u;
                 hv[u] = v < nvec ? ld_stream16(hrow + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
-                qv[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(qrow) + v)
-                                 : make_uint4(0u, 0u, 0u, 0u);
             }
-#pragma unroll
-            for (int u = 0; u < kCosBatch; ++u)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const f32x2 h2 = vec_pair<ELT>(hv[u], i), q2 = vec_pair<ELT>(qv[u], i);
-                    dot = f2_fma(h2, q2, dot);
-                    nh = f2_fma(h2, h2, nh);
-                    nq = f2_fma(q2, q2, nq);
-                }
         }
-        float d0, d1, h0, h1, q0, q1;
-        f2_unpack(dot, d0, d1);
-        f2_unpack(nh, h0, h1);
-        f2_unpack(nq, q0, q1);
-        const float sd = warp_sum(d0 + d1), sh = warp_sum(h0 + h1), sq = warp_sum(q0 + q1);
-        if (lane == 0)
-            a.scores[(size_t)b * a.W + r] = (sh > 0.f && sq > 0.f) ? sd / sqrtf(sh) / sqrtf(sq) : 0.f;
+#pragma unroll
+        for (int u = 0; u < kCosBatch; ++u) {
+            const int v = v0 + 32 * u;
+            const uint4 qv = (whole || v < nvec) ? __ldg(qrow + v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const f32x2 h2 = vec_pair<ELT>(hv[u], i), q2 = vec_pair<ELT>(qv, i);
+                dot = f2_fma(h2, q2, dot);
+                nh = f2_fma(h2, h2, nh);
+                nq = f2_fma(q2, q2, nq);
+            }
+        }
     }
+    float d0, d1, h0, h1, q0, q1;
+    f2_unpack(dot, d0, d1);
+    f2_unpack(nh, h0, h1);
+    f2_unpack(nq, q0, q1);
+    const float sd = warp_sum(d0 + d1), sh = warp_sum(h0 + h1), sq = warp_sum(q0 + q1);
+    if (lane == 0)
+        a.scores[(size_t)b * a.W + r] = (sh > 0.f && sq > 0.f) ? sd / sqrtf(sh) / sqrtf(sq) : 0.f;
 }
 
 constexpr int kCosTopWarps = 8;

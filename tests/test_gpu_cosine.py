@@ -68,8 +68,11 @@ def test_cosine_full_workload(sv):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("W_,d,delta", [(1, 8, 1), (2, 8, 4), (33, 64, 3), (240, 2560, 8), (257, 4096, 4)])
+@pytest.mark.parametrize("W_,d,delta", [(1, 8, 1), (2, 8, 4), (33, 64, 3), (240, 2560, 8), (257, 4096, 4),
+                                        (37, 2048, 4), (5, 16384, 2), (3, 1024, 8)])
 def test_cosine_shapes(sv, dtype, W_, d, delta):
+    """Window sizes from one row to more than a CTA's worth of rows, hidden
+    sizes from one 16-byte vector to 32 KB (ragged batches of vectors)."""
     c = W.make_cosine("cosine-b64", B=5, W=W_, d=d, seed=W_ + d)
     H, q = c.hidden, c.query
     if dtype == "f32":
@@ -79,9 +82,12 @@ def test_cosine_shapes(sv, dtype, W_, d, delta):
     check(sv, H, q, delta, dtype, None if W_ % 2 else c.positions)
 
 
-def test_cosine_zero_rows_and_ties(sv):
+@pytest.mark.parametrize("d", [128, 2048])
+def test_cosine_zero_rows_and_ties(sv, d):
+    """A short and a long hidden state (d = 2048 takes several batches of
+    vectors per lane)."""
     rng = np.random.default_rng(11)
-    B, Wn, d = 3, 40, 128
+    B, Wn = 3, 40
     H = rng.standard_normal((B, Wn, d)).astype(np.float32)
     q = rng.standard_normal((B, d)).astype(np.float32)
     H[0, 5] = 0.0                      # zero row: score 0
