@@ -84,6 +84,9 @@ struct VerifyArgs {
 };
 
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier for a group of NT threads.
+template <int NT>
+__device__ __forceinline__ void group_sync_n() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
 // Row r of sequence b of a sampling batch: r <= gamma is target row r, r > gamma
 // is draft row r-gamma-1.
@@ -159,7 +162,7 @@ __device__ __forceinline__ bool accept_draft(float lp, float lq, float u) {
 // rate): ln p_i(x_i) and ln q_i(x_i) carry errors of ~1e-6, far inside the
 // 1e-4 decision margin and the 1e-5 bar on returned probabilities.  Leaves
 // the rejection index in sm.k (-1: bad input) and the row statistics in sm.
-template <int ELT>
+template <int ELT, int NT>
 __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
     const int lane = gt & 31, gw = gt >> 5;
     const size_t rowbytes = (size_t)a.V * ELT;
@@ -179,8 +182,8 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
     // Everything above reads inputs only; the partials below come from the
     // stream, which may still be finishing.
     pdl_wait();
-    group_sync();
-    for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
+    group_sync_n<NT>();
+    for (int r = gw; r < a.rows_per_seq; r += NT / 32) {
         float M, lnZ;
         merge_row_stats(a, b, r, lane, &M, &lnZ);
         if (lane == 0) {
@@ -188,9 +191,9 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             sm.lnZ[r] = lnZ;
         }
     }
-    group_sync();
-    for (int i = gt; i < a.gamma; i += kGroup) {
-        if (i != gt) {                                     // gamma > kGroup: late gathers
+    group_sync_n<NT>();
+    for (int i = gt; i < a.gamma; i += NT) {
+        if (i != gt) {                                     // gamma > NT: late gathers
             xi = a.x[(size_t)b * a.gamma + i];
             if (xi >= 0 && xi < a.V) {
                 ztx = load_logit<ELT>(sample_row(a, b, i, rowbytes), xi);
@@ -205,9 +208,9 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             sm.lq[i] = row_log_prob(zdx, sm.M[a.gamma + 1 + i], sm.lnZ[a.gamma + 1 + i], a);
         }
     }
-    for (int r = gt; r < a.rows_per_seq; r += kGroup)
+    for (int r = gt; r < a.rows_per_seq; r += NT)
         if (sm.M[r] == kNegInf) atomicOr(&sm.bad, SPEC_DEVERR_EMPTY_ROW);
-    group_sync();
+    group_sync_n<NT>();
     if (gt == 0) {
         int k = -1;
         if (!sm.bad) {
@@ -217,11 +220,12 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
         }
         sm.k = k;
     }
-    group_sync();
+    group_sync_n<NT>();
 }
 
 // Every output of the sampling decision but the final token, and the
 // SampleDesc the final-sample kernels read.
+template <int NT>
 static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt, const SampleDecideSmem& sm) {
     const int k = sm.k;
     if (gt == 0) {
@@ -236,11 +240,11 @@ static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt,
         a.tick[b] = 0u;
     }
     // accepted drafts and padding; slot k belongs to the final-pass search
-    for (int i = gt; i <= a.gamma; i += kGroup)
+    for (int i = gt; i <= a.gamma; i += NT)
         if (k < 0 || i != k)
             a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
     if (a.out_lp)
-        for (int i = gt; i < a.gamma; i += kGroup) {
+        for (int i = gt; i < a.gamma; i += NT) {
             float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
             o[0] = k >= 0 ? sm.lp[i] : CUDART_NAN_F;
             o[1] = k >= 0 ? sm.lq[i] : CUDART_NAN_F;

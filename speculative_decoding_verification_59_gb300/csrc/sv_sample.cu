@@ -352,20 +352,37 @@ __device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* w
         za = ff_combine(za, FF{q.x, q.y});
         zb = ff_combine(zb, FF{q.z, q.w});
     }
-    FF Za, Zb;
-    block_incl_scan_ff(za, wtot, &Za);
-    block_incl_scan_ff(zb, wtot, &Zb);
+    // both totals in one block reduction (wtot holds kCW pairs)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    za = warp_sum_ff(za);
+    zb = warp_sum_ff(zb);
+    __syncthreads();                                      // wtot may still be read by a caller's scan
+    if (lane == 0) {
+        wtot[warp] = za;
+        wtot[kCW + warp] = zb;
+    }
+    __syncthreads();
+    FF Za{0.f, 0.f}, Zb{0.f, 0.f};
+    for (int w = 0; w < kCW; ++w) {
+        Za = ff_combine(Za, wtot[w]);
+        Zb = ff_combine(Zb, wtot[kCW + w]);
+    }
+    __syncthreads();
     return ff_div(Za, Zb);
 }
 
 // One CTA per sequence: the accept decisions and every output but the final
 // token, and the SampleDesc the chunk kernels read.
+// 16 warps: one row's partials per warp for gamma <= 7 (15 rows), so the
+// merge is a single round of loads.
+constexpr int kSampleDecideThreads = 512;
+
 template <int ELT>
-__global__ void __launch_bounds__(kGroup) sample_decide_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kSampleDecideThreads) sample_decide_kernel(const VerifyArgs a) {
     __shared__ SampleDecideSmem dsm;
     pdl_trigger();
-    decide_sample<ELT>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
-    write_sample_decision(a, blockIdx.x, threadIdx.x, dsm);
+    decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
+    write_sample_decision<kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);
 }
 
 // The weights of the kSearchPT consecutive elements this thread holds in
@@ -409,7 +426,7 @@ __device__ __forceinline__ void search_weights(const VerifyArgs& a, const FinalR
 
 // Shared memory of the final-pass CTAs.
 struct FinalSmem {
-    FF wtot[kCW];
+    FF wtot[2 * kCW];
     FF lo;
     int sel, last, seg;
     int mine;                 // this CTA finished its sequence's last chunk
@@ -567,11 +584,16 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
             const size_t sg = ((size_t)b * a.C + c) * kCW + (threadIdx.x >> 5);
             a.zsum[sg] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
             if (f.rej) a.wsum[sg] = make_float4(w.hi, w.lo, dd, 0.f);
-            __threadfence();
         }
     }
+    // The CTA's sums, ordered before the ticket by the barrier, are published
+    // at gpu scope by the ticket thread's fence (the pattern of a grid-wide
+    // barrier: bar.sync, then one thread fences and increments).
     __syncthreads();
-    if (threadIdx.x == 0) sm.mine = take_ticket(&a.tick[b]) == (unsigned)(a.C - 1);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        sm.mine = take_ticket(&a.tick[b]) == (unsigned)(a.C - 1);
+    }
     __syncthreads();
     if (!sm.mine) return;
     search_sequence<ELT, VEC>(a, b, d, sm);
@@ -795,7 +817,7 @@ template <int ELT, bool VEC>
 static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool decide = true) {
     cudaError_t e = cudaSuccess;
     if (decide) {
-        e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kGroup, 0, st, a);
+        e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kSampleDecideThreads, 0, st, a);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(sample_final_kernel<ELT, VEC>, dim3((unsigned)a.C * (unsigned)a.B), kCT, 0, st,
