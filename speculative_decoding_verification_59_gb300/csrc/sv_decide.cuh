@@ -100,7 +100,6 @@ struct SampleDecideSmem {
     float M[2 * kMaxGamma + 1];       // row max
     float lnZ[2 * kMaxGamma + 1];     // ln sum exp((z - M)/T)
     float lp[kMaxGamma], lq[kMaxGamma];
-    float u[kMaxGamma];               // accept uniforms
     int bad, k;
 };
 
@@ -160,10 +159,13 @@ __device__ __forceinline__ bool accept_draft(float lp, float lq, float u) {
 // float-float) and the accept decisions u_i < p_i(x_i)/q_i(x_i) in single
 // precision (GB300's double-precision rate is a small fraction of its float
 // rate): ln p_i(x_i) and ln q_i(x_i) carry errors of ~1e-6, far inside the
-// 1e-4 decision margin and the 1e-5 bar on returned probabilities.  Leaves
-// the rejection index in sm.k (-1: bad input) and the row statistics in sm.
+// 1e-4 decision margin and the 1e-5 bar on returned probabilities.  Every
+// position's test runs on its own thread; the first rejection is the smallest
+// rejected index.  Returns the rejection index k (gamma when every draft is
+// accepted, -1 for bad input) in every thread and leaves the row statistics
+// in sm.
 template <int ELT, int NT>
-__device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
+__device__ int decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
     const int lane = gt & 31, gw = gt >> 5;
     const size_t rowbytes = (size_t)a.V * ELT;
     if (!a.early_inputs) pdl_wait();   // first kernel of the call: the kernel before may write the inputs
@@ -177,8 +179,11 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             zdx = load_logit<ELT>(sample_row(a, b, a.gamma + 1 + gt, rowbytes), xi);
         }
     }
-    if (gt < a.gamma) sm.u[gt] = a.u[(size_t)b * (a.gamma + 1) + gt];
-    if (gt == 0) sm.bad = 0;
+    const float ui = gt < a.gamma ? a.u[(size_t)b * (a.gamma + 1) + gt] : 0.f;
+    if (gt == 0) {
+        sm.bad = 0;
+        sm.k = a.gamma;
+    }
     // Everything above reads inputs only; the partials below come from the
     // stream, which may still be finishing.
     pdl_wait();
@@ -204,30 +209,25 @@ __device__ void decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSm
             atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
             sm.lp[i] = sm.lq[i] = 0.f;
         } else {
-            sm.lp[i] = row_log_prob(ztx, sm.M[i], sm.lnZ[i], a);
-            sm.lq[i] = row_log_prob(zdx, sm.M[a.gamma + 1 + i], sm.lnZ[a.gamma + 1 + i], a);
+            const float lp = row_log_prob(ztx, sm.M[i], sm.lnZ[i], a);
+            const float lq = row_log_prob(zdx, sm.M[a.gamma + 1 + i], sm.lnZ[a.gamma + 1 + i], a);
+            sm.lp[i] = lp;
+            sm.lq[i] = lq;
+            const float u = i == gt ? ui : a.u[(size_t)b * (a.gamma + 1) + i];
+            if (!accept_draft(lp, lq, u)) atomicMin(&sm.k, i);
         }
     }
     for (int r = gt; r < a.rows_per_seq; r += NT)
         if (sm.M[r] == kNegInf) atomicOr(&sm.bad, SPEC_DEVERR_EMPTY_ROW);
     group_sync_n<NT>();
-    if (gt == 0) {
-        int k = -1;
-        if (!sm.bad) {
-            k = a.gamma;                                   // left to right; first rejection wins
-            for (int i = 0; i < a.gamma; ++i)
-                if (!accept_draft(sm.lp[i], sm.lq[i], sm.u[i])) { k = i; break; }
-        }
-        sm.k = k;
-    }
-    group_sync_n<NT>();
+    return sm.bad ? -1 : sm.k;
 }
 
 // Every output of the sampling decision but the final token, and the
 // SampleDesc the final-sample kernels read.
 template <int NT>
-static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt, const SampleDecideSmem& sm) {
-    const int k = sm.k;
+static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt, int k,
+                                             const SampleDecideSmem& sm) {
     if (gt == 0) {
         if (sm.bad) atomicOr(a.err, sm.bad);
         a.out_acc[b] = k;

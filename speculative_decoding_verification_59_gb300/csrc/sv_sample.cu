@@ -341,18 +341,9 @@ __device__ __forceinline__ FF block_excl_from_incl(FF r, const FF* wtot_scanned)
     return warp > 0 ? wtot_scanned[warp - 1] : FF{0.f, 0.f};
 }
 
-// The ratio Za / Zb of the two row normalisers of sequence b, from the
-// segment sums (block-wide, identical in every CTA that calls it).
-__device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* wtot) {
-    const int ns = a.C * kCW;
-    const float4* zs = a.zsum + (size_t)b * ns;
-    FF za{0.f, 0.f}, zb{0.f, 0.f};
-    for (int s = threadIdx.x; s < ns; s += kCT) {
-        const float4 q = __ldcg(&zs[s]);
-        za = ff_combine(za, FF{q.x, q.y});
-        zb = ff_combine(zb, FF{q.z, q.w});
-    }
-    // both totals in one block reduction (wtot holds kCW pairs)
+// The ratio Za / Zb of the two row normalisers of sequence b from each
+// thread's share of the segment sums (one block reduction of both).
+__device__ __forceinline__ FF normaliser_ratio_of(FF za, FF zb, FF* wtot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     za = warp_sum_ff(za);
     zb = warp_sum_ff(zb);
@@ -371,6 +362,20 @@ __device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* w
     return ff_div(Za, Zb);
 }
 
+// The same from the segment sums in the workspace (thread t takes segments
+// t, t + kCT, ...).
+__device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* wtot) {
+    const int ns = a.C * kCW;
+    const float4* zs = a.zsum + (size_t)b * ns;
+    FF za{0.f, 0.f}, zb{0.f, 0.f};
+    for (int s = threadIdx.x; s < ns; s += kCT) {
+        const float4 q = __ldcg(&zs[s]);
+        za = ff_combine(za, FF{q.x, q.y});
+        zb = ff_combine(zb, FF{q.z, q.w});
+    }
+    return normaliser_ratio_of(za, zb, wtot);
+}
+
 // One CTA per sequence: the accept decisions and every output but the final
 // token, and the SampleDesc the chunk kernels read.
 // 16 warps: one row's partials per warp for gamma <= 7 (15 rows), so the
@@ -381,8 +386,8 @@ template <int ELT>
 __global__ void __launch_bounds__(kSampleDecideThreads) sample_decide_kernel(const VerifyArgs a) {
     __shared__ SampleDecideSmem dsm;
     pdl_trigger();
-    decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
-    write_sample_decision<kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);
+    const int k = decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
+    write_sample_decision<kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, k, dsm);
 }
 
 // The weights of the kSearchPT consecutive elements this thread holds in
@@ -446,18 +451,24 @@ __device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, cons
     FF& s_lo = sm.lo;
     const int tid = threadIdx.x;
     bool rej = d.k < a.gamma;
-    const FF R = rej ? normaliser_ratio(a, b, wtot) : FF{0.f, 0.f};
     const int ns = a.C * kCW;                             // segments in the row
     const int G = (ns + kCT - 1) / kCT;                   // consecutive segments per thread
+    // With one segment per thread (V <= kCT kSeg) each thread loads its
+    // segment's sums once, normaliser and residual sums together; otherwise
+    // they are read where needed.
+    const bool one = G == 1;
+    float4 qz = make_float4(0.f, 0.f, 0.f, 0.f), qw = qz;
+    if (one && tid < ns) {
+        qz = __ldcg(&a.zsum[(size_t)b * ns + tid]);
+        if (rej) qw = __ldcg(&a.wsum[(size_t)b * ns + tid]);
+    }
+    FF R{0.f, 0.f};
+    if (rej) R = one ? normaliser_ratio_of(FF{qz.x, qz.y}, FF{qz.z, qz.w}, wtot) : normaliser_ratio(a, b, wtot);
     // residual sums at the exact ratio: w(rt) - (R - rt) dd, to first order
     const float dR = (R.hi - d.rt) + R.lo;
     auto seg_total = [&](int s) -> FF {
-        if (rej) {
-            const float4 q = __ldcg(&a.wsum[(size_t)b * ns + s]);
-            return ff_combine(FF{q.x, q.y}, FF{-dR * q.z, 0.f});
-        }
-        const float4 q = __ldcg(&a.zsum[(size_t)b * ns + s]);
-        return FF{q.x, q.y};
+        const float4 q = one ? (rej ? qw : qz) : __ldcg(rej ? &a.wsum[(size_t)b * ns + s] : &a.zsum[(size_t)b * ns + s]);
+        return rej ? ff_combine(FF{q.x, q.y}, FF{-dR * q.z, 0.f}) : FF{q.x, q.y};
     };
 
     // Thread totals over its segments and their prefix; fall back to p_k if
