@@ -282,20 +282,25 @@ __host__ __device__ constexpr int topk_slots(int K) { return 2 * K; }
 
 // Top-K candidates of one warp chunk whose first element is row index base,
 // of which valid_bytes lie inside the row; v holds the lane's vectors, chunk
-// the same bytes in shared memory.  Every element of the chunk's top K is at
-// least thr, the K-th largest of the 32 lane maxima (those are K distinct
-// elements), so only vectors whose maximum reaches thr are opened: each lane
-// marks its elements >= thr in a 64-bit mask (bit 8 t + e for element e of
-// vector t).  When the warp marks at most 2K elements (nearly always: a few
-// more than K) they are written as they are, unsorted, into the chunk's 2K
-// slots -- the merge orders them.  Otherwise the lanes insert their marked
-// elements into sorted lists and the warp merges the lists into the chunk's
-// exact top K.  Marked elements are read back from shared memory in one loop,
-// which keeps the kernel's instruction footprint small.
+// the same bytes in shared memory.  The chunk must yield every element of
+// the row's top K that it holds; those are all at least any lower bound of
+// the row's K-th largest element.  thr is such a bound: on the warp's first
+// chunk of a row (have_thr false) the K-th largest of the 32 lane maxima
+// (K distinct elements of the row), afterwards the bound carried from the
+// warp's earlier chunks of the same row, which skips the K warp-max rounds.
+// Only vectors whose maximum reaches thr are opened: each lane marks its
+// elements >= thr in a 64-bit mask (bit 8 t + e for element e of vector t).
+// When the warp marks at most 2K elements (nearly always: a few more than K)
+// they are written as they are, unsorted, into the chunk's 2K slots -- the
+// merge orders them.  Otherwise the lanes insert their marked elements into
+// sorted lists and the warp merges the lists into the chunk's exact top K,
+// whose K-th value then raises thr.  Marked elements are read back from
+// shared memory in one loop, which keeps the kernel's instruction footprint
+// small.
 template <int ELT, int K>
 __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
                                                 const unsigned char* chunk, int valid_bytes,
-                                                int base, float2* out) {
+                                                int base, float2* out, float& thr, bool have_thr) {
     const int lane = threadIdx.x & 31;
     constexpr int PV = 16 / ELT;
     constexpr int KS = topk_slots(K);
@@ -306,12 +311,15 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
         vm[t] = vec_max_value<ELT>(vec_max_bits<ELT>(v[t]));
         lm = fmaxf(lm, vm[t]);
     }
-    float x = lm, thr = kNegInf;
+    if (!have_thr) {                                       // warp-uniform
+        float x = lm;
+        thr = kNegInf;
 #pragma unroll
-    for (int r = 0; r < K; ++r) {
-        thr = warp_max(x);
-        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
-        if (lane == __ffs(own) - 1) x = kNegInf;
+        for (int r = 0; r < K; ++r) {
+            thr = warp_max(x);
+            const unsigned own = __ballot_sync(0xffffffffu, x == thr);
+            if (lane == __ffs(own) - 1) x = kNegInf;
+        }
     }
     unsigned long long mask = 0ull;
 #pragma unroll
@@ -381,6 +389,7 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
 #pragma unroll
         for (int r = 0; r < K; ++r) out[r] = make_float2(ov[r], __int_as_float(oi[r]));
     if (lane >= K && lane < KS) out[lane] = make_float2(kNegInf, __int_as_float(0x7fffffff));
+    thr = fmaxf(thr, ov[K - 1]);                          // more than 2K marked: K of them reach it
 }
 
 template <int ELT, int MODE>
@@ -443,6 +452,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     // ---- consumers.  A timed-out wait flags the error and stops the warp
     // from touching the ring.
     const int cw = warp - 1;
+    unsigned tk_row = 0xffffffffu;                        // top-K: row of the carried bound
+    float tk_thr = kNegInf;
     unsigned c0, c1, it = 0;
     cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
     bool ok = true;
@@ -469,9 +480,12 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
             }
             const int base = (int)(off / ELT) + cw * (32 * kLaneBytes / ELT);
             if constexpr (MODE == kModeSample || MODE == kModeLazy) part = warp_rowstats<ELT>(v, a.s);
-            else if constexpr (KT > 0)
+            else if constexpr (KT > 0) {
                 warp_topk_chunk<ELT, KT>(v, chunk, wb, base,
-                                         a.parts + ((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT));
+                                         a.parts + ((size_t)rr * P + seg * kWarps + cw) * topk_slots(KT),
+                                         tk_thr, tk_row == rr);
+                tk_row = rr;
+            }
             else part = warp_argmax_chunk<ELT>(v, base);
         } else {
             part = (MODE == kModeSample || MODE == kModeLazy) ? make_float2(kNegInf, 0.f)
