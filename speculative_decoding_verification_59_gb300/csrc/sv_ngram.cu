@@ -10,22 +10,24 @@
 // pages rank candidates by hidden-state similarity; that rerank is outside
 // this library, and the most recent match is the reuse position here.
 //
-// Pass 1 (ngram_scan_kernel): each sequence's context is split into S
-// segments (one 1024-position tile each, up to 64 segments), one CTA each,
-// so that many short CTAs overlap their load latencies.  A CTA walks its
-// segment in tiles of 1024 positions; thread t tests the 4
-// positions of one 16-byte load, holding the 8 tokens before them from two
-// more loads (L1 hits: the neighbouring threads' own vectors), against the
-// query reversed in registers -- every index a compile-time constant.  Block
-// scans of the per-thread match counts keep the segment's match list in
-// position order.  Pass 2 (ngram_merge_kernel, one warp per sequence)
-// concatenates the segments' lists, counts, and copies the draft.
+// Pass 1 (ngram_scan_kernel<W>, the window length a template argument):
+// each sequence's context is split into S segments (one 4096-position tile
+// each, up to 64 segments), one CTA each, so that many short CTAs overlap
+// their load latencies.  A CTA walks its segment in tiles of 4096 positions;
+// thread t tests the 16 positions of four 16-byte loads, holding the tokens
+// before them from one or two more loads (L1 hits: the neighbouring thread's
+// own vectors), against the query reversed in registers -- W compares per
+// position, every index a compile-time constant.  Block scans of the
+// per-thread match counts keep the segment's match list in position order.
+// Pass 2 (ngram_merge_kernel, one warp per sequence) concatenates the
+// segments' lists, counts, and copies the draft.
 #include "sv_common.cuh"
 
 namespace sv {
 
 constexpr int kNgThreads = 256;
-constexpr int kNgTile = kNgThreads * 4;          // positions per tile
+constexpr int kNgPer = 16;                       // positions per thread and tile
+constexpr int kNgTile = kNgThreads * kNgPer;     // positions per tile
 constexpr int kNgMaxW = 8;
 constexpr int kNgMaxSeg = 64;
 
@@ -73,7 +75,9 @@ __device__ __forceinline__ int4 ld_tok4(const int32_t* p) {
     return __ldg(reinterpret_cast<const int4*>(p));
 }
 
+template <int W>
 __global__ void __launch_bounds__(kNgThreads) ngram_scan_kernel(const NgArgs a) {
+    static_assert(W >= 1 && W <= kNgMaxW, "window length");
     __shared__ int q[kNgMaxW];
     __shared__ int wsum[kNgThreads / 32];
     __shared__ int s_last;
@@ -90,35 +94,49 @@ __global__ void __launch_bounds__(kNgThreads) ngram_scan_kernel(const NgArgs a) 
         }
         return;
     }
-    if (tid < a.w) q[tid] = n >= a.w ? t[n - a.w + tid] : 0;
+    if (tid < W) q[tid] = n >= W ? t[n - W + tid] : 0;
     if (tid == 0) s_last = -1;
     __syncthreads();
     // the query reversed: qr[j] must equal the token j places before a candidate's end
-    int qr[kNgMaxW];
+    int qr[W];
 #pragma unroll
-    for (int j = 0; j < kNgMaxW; ++j) qr[j] = j < a.w ? q[a.w - 1 - j] : 0;
+    for (int j = 0; j < W; ++j) qr[j] = q[W - 1 - j];
     // positions of this segment that can match: [lo, hi)
-    const int lo = max(s * a.seg_len, a.w - 1);
+    const int lo = max(s * a.seg_len, W - 1);
     const int hi = min((s + 1) * a.seg_len, n - 1);
     int count = 0;
     int32_t* segm = a.seg_matches + so * a.max_matches;
     for (int p0 = s * a.seg_len; p0 < hi; p0 += kNgTile) {
-        const int p = p0 + 4 * tid;
+        const int p = p0 + kNgPer * tid;
         unsigned mask = 0u;
-        if (p < hi && p + 3 >= lo) {
-            // x[k] = token at p - 8 + k, k = 0..11 (-1 before the stream starts)
-            int x[12];
-            const int4 c = ld_tok4(t + p);
-            const int4 m1 = p >= 4 ? ld_tok4(t + p - 4) : make_int4(-1, -1, -1, -1);
-            const int4 m2 = p >= 8 ? ld_tok4(t + p - 8) : make_int4(-1, -1, -1, -1);
+        if (p < hi && p + kNgPer - 1 >= lo) {
+            // x[k] = token at p - 8 + k, k = 0..8+kNgPer-1 (-1 outside [0, n_max))
+            int x[8 + kNgPer];
+            const int4 none = make_int4(-1, -1, -1, -1);
+            const int4 m2 = (W > 5 && p >= 8) ? ld_tok4(t + p - 8) : none;
+            const int4 m1 = (W > 1 && p >= 4) ? ld_tok4(t + p - 4) : none;
             x[0] = m2.x; x[1] = m2.y; x[2] = m2.z; x[3] = m2.w;
             x[4] = m1.x; x[5] = m1.y; x[6] = m1.z; x[7] = m1.w;
-            x[8] = c.x;  x[9] = c.y;  x[10] = c.z; x[11] = c.w;
+            int4 c[kNgPer / 4];
+            if (p + kNgPer <= a.n_max) {                   // all four loads issue together
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+                for (int v = 0; v < kNgPer / 4; ++v) c[v] = ld_tok4(t + p + 4 * v);
+            } else {
+#pragma unroll
+                for (int v = 0; v < kNgPer / 4; ++v) c[v] = p + 4 * v < a.n_max ? ld_tok4(t + p + 4 * v) : none;
+            }
+#pragma unroll
+            for (int v = 0; v < kNgPer / 4; ++v) {
+                x[8 + 4 * v] = c[v].x;
+                x[9 + 4 * v] = c[v].y;
+                x[10 + 4 * v] = c[v].z;
+                x[11 + 4 * v] = c[v].w;
+            }
+#pragma unroll
+            for (int e = 0; e < kNgPer; ++e) {
                 bool eq = p + e >= lo && p + e < hi;
 #pragma unroll
-                for (int j = 0; j < kNgMaxW; ++j) eq = eq && (j >= a.w || x[8 + e - j] == qr[j]);
+                for (int j = 0; j < W; ++j) eq = eq && x[8 + e - j] == qr[j];
                 mask |= (eq ? 1u : 0u) << e;
             }
         }
@@ -126,11 +144,10 @@ __global__ void __launch_bounds__(kNgThreads) ngram_scan_kernel(const NgArgs a) 
         int total;
         const int off = block_excl_scan_int(__popc(mask), wsum, &total);
         int k = count + off;
-        for (int e = 0; e < 4; ++e)
-            if (mask & (1u << e)) {
-                if (k < a.max_matches) segm[k] = p + e;
-                ++k;
-            }
+        for (unsigned m = mask; m; m &= m - 1u) {
+            if (k < a.max_matches) segm[k] = p + __ffs(m) - 1;
+            ++k;
+        }
         if (mask) atomicMax(&s_last, p + 31 - __clz(mask));
         count += total;
     }
@@ -174,14 +191,29 @@ __global__ void __launch_bounds__(kNgMergeWarps * 32) ngram_merge_kernel(const N
     const int t0 = __shfl_sync(0xffffffffu, i0, 31);
     const int total = t0 + __shfl_sync(0xffffffffu, i1, 31);
     const int off0 = i0 - c0, off1 = t0 + i1 - c1;
-    const int32_t* m0 = a.seg_matches + ((size_t)b * a.S + s0) * a.max_matches;
-    const int32_t* m1 = a.seg_matches + ((size_t)b * a.S + s1) * a.max_matches;
-    for (int k = 0; k < c0 && off0 + k < a.max_matches; ++k) om[off0 + k] = __ldcg(m0 + k);
-    for (int k = 0; k < c1 && off1 + k < a.max_matches; ++k) om[off1 + k] = __ldcg(m1 + k);
+    // Lane l copies the lists of its segments l and l + 32, four loads in
+    // flight at a time.
+    auto copy_list = [&](const int32_t* m, int cnt, int off) {
+        for (int k0 = 0; k0 < cnt && off + k0 < a.max_matches; k0 += 4) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + u;
+                v[u] = (k < cnt && off + k < a.max_matches) ? __ldcg(m + k) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + u;
+                if (k < cnt && off + k < a.max_matches) om[off + k] = v[u];
+            }
+        }
+    };
+    copy_list(a.seg_matches + ((size_t)b * a.S + s0) * a.max_matches, c0, off0);
+    copy_list(a.seg_matches + ((size_t)b * a.S + s1) * a.max_matches, c1, off1);
     for (int k = total + lane; k < a.max_matches; k += 32) om[k] = -1;
     if (lane == 0) a.out_count[b] = total;
-    // the reuse position: the last match of the highest segment with one
     const unsigned h1 = __ballot_sync(0xffffffffu, c1 > 0), h0 = __ballot_sync(0xffffffffu, c0 > 0);
+    // the reuse position: the last match of the highest segment with one
     int last = -1;
     if (h1 || h0) {
         const int sl = h1 ? 32 + 31 - __clz(h1) : 31 - __clz(h0);
@@ -233,7 +265,17 @@ cudaError_t launch_ngram(const int32_t* tokens, const int32_t* lengths, int B, i
     a.out_count = out_count;
     a.out_matches = out_matches;
     a.out_draft = out_draft;
-    e = launch_pdl(ngram_scan_kernel, dim3((unsigned)(B * S)), kNgThreads, 0, st, a);
+    const dim3 grid((unsigned)(B * S));
+    switch (w) {
+        case 1: e = launch_pdl(ngram_scan_kernel<1>, grid, kNgThreads, 0, st, a); break;
+        case 2: e = launch_pdl(ngram_scan_kernel<2>, grid, kNgThreads, 0, st, a); break;
+        case 3: e = launch_pdl(ngram_scan_kernel<3>, grid, kNgThreads, 0, st, a); break;
+        case 4: e = launch_pdl(ngram_scan_kernel<4>, grid, kNgThreads, 0, st, a); break;
+        case 5: e = launch_pdl(ngram_scan_kernel<5>, grid, kNgThreads, 0, st, a); break;
+        case 6: e = launch_pdl(ngram_scan_kernel<6>, grid, kNgThreads, 0, st, a); break;
+        case 7: e = launch_pdl(ngram_scan_kernel<7>, grid, kNgThreads, 0, st, a); break;
+        default: e = launch_pdl(ngram_scan_kernel<8>, grid, kNgThreads, 0, st, a); break;
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(ngram_merge_kernel, dim3((B + kNgMergeWarps - 1) / kNgMergeWarps),
                       kNgMergeWarps * 32, 0, st, a);

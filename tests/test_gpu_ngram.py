@@ -31,9 +31,12 @@ def check(sv, tokens, lengths, w, L, cap, ws=None):
     return ref
 
 
-@pytest.mark.parametrize("w", [1, 2, 3, 4, 8])
-@pytest.mark.parametrize("n_max", [4, 1024, 5000, 70000])
+@pytest.mark.parametrize("w", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("n_max", [4, 1024, 5000, 70000, 300000])
 def test_ngram_small_alphabet(sv, w, n_max):
+    """Every window length (each has its own kernel), contexts from one
+    16-byte vector to more than 64 tiles of 4096 positions (segments of two
+    tiles), over a 3-token alphabet: matches nearly everywhere."""
     if n_max % 4:
         n_max += 4 - n_max % 4
     rng = np.random.default_rng(w * 1000 + n_max)
