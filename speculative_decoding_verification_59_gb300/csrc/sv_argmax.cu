@@ -17,23 +17,26 @@
 namespace sv {
 
 // One CTA per sequence, chained behind the argmax stream (waits in hardware
-// until the stream's partials are visible).
-__global__ void __launch_bounds__(kGroup) greedy_decide_kernel(const VerifyArgs a) {
+// until the stream's partials are visible).  32 warps: a row's partials per
+// warp and round of loads (a 36-node tree takes two rounds).
+constexpr int kArgmaxDecideThreads = 1024;
+
+__global__ void __launch_bounds__(kArgmaxDecideThreads) greedy_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
-    prefetch_tokens(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
+    prefetch_tokens<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
     pdl_wait();
-    decide_greedy(a, blockIdx.x, threadIdx.x, sm);
+    decide_greedy<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm);
 }
 
-__global__ void __launch_bounds__(kGroup) tree_decide_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kArgmaxDecideThreads) tree_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
-    prefetch_tokens(a, blockIdx.x, threadIdx.x, true, sm);
+    prefetch_tokens<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, true, sm);
     pdl_wait();
-    decide_tree(a, blockIdx.x, threadIdx.x, sm);
+    decide_tree<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm);
 }
 
 static cudaError_t launch_decide(void (*kfn)(VerifyArgs), const VerifyArgs& a, int B, cudaStream_t st) {
-    return launch_pdl(kfn, dim3(B), kGroup, 0, st, a);
+    return launch_pdl(kfn, dim3(B), kArgmaxDecideThreads, 0, st, a);
 }
 
 static VerifyArgs argmax_args(const void* zt, int elt, int B, int rows, int V, void* ws) {

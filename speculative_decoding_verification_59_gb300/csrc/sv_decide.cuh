@@ -8,8 +8,9 @@
 // efficient model-free speculative decoding", section 3.3 and Algorithm 1
 // (VerifyAndAccept over the draft tree).
 //
-// A decision is taken by a group of kGroup threads (a whole 256-thread CTA)
-// synchronised on named barrier 1; gt is the thread's index in the group.
+// A decision is taken by a group of NT threads (a whole CTA: 256 threads, 512
+// for sampling, 1024 for greedy chains and trees) synchronised on named
+// barrier 1; gt is the thread's index in the group.
 // Each runs in its own kernel, one CTA per sequence (sv_argmax.cu for greedy
 // chains and trees, sv_sample.cu for sampling).
 #pragma once
@@ -264,20 +265,22 @@ struct ArgmaxDecideSmem {
 // The sequence's tokens (and parents) into shared memory.  They are inputs,
 // so a decide kernel loads them before waiting for the stream's partials;
 // the merge that follows ends with a group barrier that publishes them.
+template <int NT>
 __device__ __forceinline__ void prefetch_tokens(const VerifyArgs& a, int b, int gt, bool tree,
                                                 ArgmaxDecideSmem& sm) {
     const int n = tree ? a.rows_per_seq : a.gamma;
-    for (int i = gt; i < n; i += kGroup) {
+    for (int i = gt; i < n; i += NT) {
         sm.x[i] = a.x[(size_t)b * n + i];
         if (tree) sm.par[i] = a.par[(size_t)b * n + i];
     }
 }
 
 // Argmax of every row of sequence b from the (value, index) partials.
+template <int NT>
 __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, int gt, int* g) {
     const int lane = gt & 31, gw = gt >> 5;
     const int P = a.nseg * kWarps;
-    for (int r = gw; r < a.rows_per_seq; r += kGroup / 32) {
+    for (int r = gw; r < a.rows_per_seq; r += NT / 32) {
         const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
         float bv = kNegInf;
         int bi = 0x7fffffff;
@@ -298,14 +301,15 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
         warp_argmax(bv, bi);
         if (lane == 0) g[r] = bi;
     }
-    group_sync();
+    group_sync_n<NT>();
 }
 
 // Greedy chain: k = first i with x_i != argmax of row i, else gamma; output
 // x_0..x_{k-1} then the target argmax of row k.
+template <int NT>
 static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
     const int G = a.gamma;
-    merge_argmax_rows(a, b, gt, sm.g);
+    merge_argmax_rows<NT>(a, b, gt, sm.g);
     if (gt == 0) {
         int bad = 0;
         for (int i = 0; i < G; ++i) {
@@ -323,9 +327,9 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
         sm.k = k;
         a.out_acc[b] = k;
     }
-    group_sync();
+    group_sync_n<NT>();
     const int k = sm.k;
-    for (int i = gt; i <= G; i += kGroup) {
+    for (int i = gt; i <= G; i += NT) {
         int v = -1;
         if (k >= 0) v = i < k ? sm.x[i] : (i == k ? sm.g[k] : -1);
         a.out_tok[(size_t)b * (G + 1) + i] = v;
@@ -335,13 +339,14 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
 // Draft tree: a node is accepted when its parent is and its token is the
 // argmax of the parent's row; output the longest accepted root path (ties:
 // lowest node ids) and the argmax of the path's last node.
+template <int NT>
 static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
     const int N = a.rows_per_seq;
     const int* tok = sm.x;                                 // prefetched
     const int* par = sm.par;
     if (gt == 0) sm.bad = 0;
-    merge_argmax_rows(a, b, gt, sm.g);                     // ends with group_sync
-    for (int n = gt; n < N; n += kGroup) {
+    merge_argmax_rows<NT>(a, b, gt, sm.g);                     // ends with group_sync
+    for (int n = gt; n < N; n += NT) {
         const int p = par[n];
         if (n == 0 ? p != -1 : (p < 0 || p >= n)) atomicOr(&sm.bad, SPEC_DEVERR_TREE_PARENT);
         if (n > 0) {
@@ -351,7 +356,7 @@ static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDec
         sm.depth[n] = 0;
         sm.best[n] = -1;
     }
-    group_sync();
+    group_sync_n<NT>();
     int32_t* on = a.out_nodes + (size_t)b * N;
     int32_t* ot = a.out_tok + (size_t)b * N;
     if (gt == 0) {
@@ -382,9 +387,9 @@ static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDec
         sm.len = len;
         a.out_acc[b] = len;
     }
-    group_sync();
+    group_sync_n<NT>();
     const int len = sm.len;
-    for (int n = gt; n < N; n += kGroup) {
+    for (int n = gt; n < N; n += NT) {
         if (len < 0 || n >= len) on[n] = -1;
         if (len < 0 || n > len) ot[n] = -1;
     }

@@ -645,12 +645,15 @@ struct LazyDecideSmem {
     int bad, k;
 };
 
+// 16 warps: the 13 rows of a [2, 8) group are merged in one round of loads.
+constexpr int kLazyDecideThreads = 512;
+
 // One CTA per sequence of the group's list (every sequence for the first
 // group).  k is the rejection index, gamma when the group holds the bonus row
 // and every draft was accepted, -1 for bad input, -2 for "undecided: next
 // group".
 template <int ELT>
-__global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kLazyDecideThreads) lazy_decide_kernel(const VerifyArgs a) {
     __shared__ LazyDecideSmem sm;
     const int gt = threadIdx.x, lane = gt & 31, gw = gt >> 5;
     const int lo = a.lz_lo, nt = a.lz_nt, nd = a.lz_nd;
@@ -658,7 +661,7 @@ __global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a)
     const bool first = a.lz_list == nullptr;
     pdl_trigger();
     auto gather = [&](int b) {
-        for (int q = gt; q < nd; q += kGroup) {
+        for (int q = gt; q < nd; q += kLazyDecideThreads) {
             const int p = lo + q;
             const int xi = a.x[(size_t)b * a.gamma + p];
             const bool in = xi >= 0 && xi < a.V;
@@ -673,7 +676,7 @@ __global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a)
         // call, so they are final.  Every draft token of the sequence is
         // checked here, as the full pass's decision does.
         gather(b);
-        for (int i = gt; i < a.gamma; i += kGroup) {
+        for (int i = gt; i < a.gamma; i += kLazyDecideThreads) {
             const int xi = a.x[(size_t)b * a.gamma + i];
             if (xi < 0 || xi >= a.V) bad = 1;
         }
@@ -684,7 +687,7 @@ __global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a)
         b = __ldcg(a.lz_list + blockIdx.x);
         gather(b);
     }
-    for (int q = gw; q < nt + nd; q += kGroup / 32) {
+    for (int q = gw; q < nt + nd; q += kLazyDecideThreads / 32) {
         const int r = q < nt ? lo + q : a.gamma + 1 + lo + (q - nt);
         float M, lnZ;
         merge_row_stats(a, b, r, lane, &M, &lnZ);
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a)
     __syncthreads();
     const int k = sm.k;
     if (a.out_lp && k != -1)                              // the positions decided here
-        for (int q = gt; q < nd; q += kGroup)
+        for (int q = gt; q < nd; q += kLazyDecideThreads)
             if (k == -2 || lo + q <= k) {
                 float* o = a.out_lp + ((size_t)b * a.gamma + lo + q) * 2;
                 o[0] = sm.lp[q];
@@ -734,11 +737,11 @@ __global__ void __launch_bounds__(kGroup) lazy_decide_kernel(const VerifyArgs a)
         a.tick[b] = 0u;
     }
     // accepted drafts and padding; slot k belongs to the final-pass search
-    for (int i = gt; i <= a.gamma; i += kGroup)
+    for (int i = gt; i <= a.gamma; i += kLazyDecideThreads)
         if (k < 0 || i != k)
             a.out_tok[(size_t)b * (a.gamma + 1) + i] = (k >= 0 && i < k) ? a.x[(size_t)b * a.gamma + i] : -1;
     if (a.out_lp)                                         // positions never decided
-        for (int i = gt; i < a.gamma; i += kGroup)
+        for (int i = gt; i < a.gamma; i += kLazyDecideThreads)
             if (k < 0 || i > k) {
                 float* o = a.out_lp + ((size_t)b * a.gamma + i) * 2;
                 o[0] = CUDART_NAN_F;
@@ -817,7 +820,7 @@ static cudaError_t launch_lazy(VerifyArgs a, const DeviceInfo& di, cudaStream_t 
         a.total_chunks = (long long)a.B * (a.lz_nt + a.lz_nd) * a.nseg;   // at most
         cudaError_t e = launch_stream<ELT, kModeLazy>(a, di, st);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(lazy_decide_kernel<ELT>, dim3((unsigned)a.B), kGroup, 0, st, a);
+        e = launch_pdl(lazy_decide_kernel<ELT>, dim3((unsigned)a.B), kLazyDecideThreads, 0, st, a);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
