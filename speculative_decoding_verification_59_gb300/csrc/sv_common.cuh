@@ -244,9 +244,8 @@ __device__ __forceinline__ FF warp_incl_scan_ff(FF a) {
 
 // ---- programmatic dependent launch -------------------------------------------
 // The kernels of the library are launched with programmatic stream
-// serialisation (launch_pdl; the lazy pass adds the attribute to its cluster
-// launch): a kernel may begin launching once every CTA of the kernel before
-// it in the stream has triggered (or exited), and it waits (in hardware,
+// serialisation (launch_pdl): a kernel may begin launching once every CTA of
+// the kernel before it in the stream has triggered (or exited), and it waits (in hardware,
 // griddepcontrol.wait) until that kernel has completed and its writes are
 // visible before it touches global memory that the earlier kernel may write,
 // or may still read.  A kernel may load the call's own inputs before waiting
