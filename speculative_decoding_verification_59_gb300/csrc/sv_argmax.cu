@@ -30,9 +30,10 @@ __global__ void __launch_bounds__(kArgmaxDecideThreads) greedy_decide_kernel(con
 
 __global__ void __launch_bounds__(kArgmaxDecideThreads) tree_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
+    __shared__ TreeWalkSmem tw;
     prefetch_tokens<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, true, sm);
     pdl_wait();
-    decide_tree<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm);
+    decide_tree<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm, tw);
 }
 
 static cudaError_t launch_decide(void (*kfn)(VerifyArgs), const VerifyArgs& a, int B, cudaStream_t st) {

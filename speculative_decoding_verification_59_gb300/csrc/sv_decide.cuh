@@ -255,11 +255,18 @@ static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt,
 // ---------------------------------------------------------- greedy and trees
 struct ArgmaxDecideSmem {
     int g[kMaxNodes];                 // row argmax
-    int depth[kMaxNodes];             // trees: longest accepted continuation
-    int best[kMaxNodes];              // trees: child that continues it
     int x[kMaxNodes];                 // draft tokens (chains) / node tokens (trees)
     int par[kMaxNodes];               // trees: parents
-    int k, len, bad;
+    int k, len, bad, last;
+};
+
+// The tree walk's per-node state.
+struct TreeWalkSmem {
+    int up[kMaxNodes];                // ancestor pointers being doubled
+    int acc[kMaxNodes];               // accepted (every node to the root matched)
+    int dep[kMaxNodes];               // depth below the root
+    int sub[kMaxNodes];               // deepest accepted depth in the subtree
+    int key[kMaxNodes];               // (sub, lowest id) of the best child
 };
 
 // The sequence's tokens (and parents) into shared memory.  They are inputs,
@@ -275,31 +282,92 @@ __device__ __forceinline__ void prefetch_tokens(const VerifyArgs& a, int b, int 
     }
 }
 
-// Argmax of every row of sequence b from the (value, index) partials.
-template <int NT>
+// Argmax of every row of sequence b from the (value, index) partials (every
+// slot of a row is written, those past the row's end as (-inf, INT_MAX)).
+// Rows of at most 32 partials share a warp: aligned groups of G lanes (G the
+// power of two at or above the row's partial count), one row per group,
+// reduced by xor shuffles inside the group.  Longer rows take a warp each,
+// kRows rows' loads in flight at once when a warp has several rows.
+template <int NT, bool MANY_ROWS = false>
 __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, int gt, int* g) {
     const int lane = gt & 31, gw = gt >> 5;
-    const int P = a.nseg * kWarps;
-    for (int r = gw; r < a.rows_per_seq; r += NT / 32) {
-        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
-        float bv = kNegInf;
-        int bi = 0x7fffffff;
-        constexpr int kHeld = 4;                           // loads in flight per lane
-        for (int p0 = lane; p0 < P; p0 += 32 * kHeld) {
-            float2 q[kHeld];
+    constexpr int NW = NT / 32;
+    const int P = a.nseg * kWarps, np = P;              // row stride and partials
+    const int R = a.rows_per_seq;
+    const float2* base = a.parts + (size_t)b * R * P;
+    if (np <= 32) {
+        int G = 1;
+        while (G < np) G <<= 1;
+        const int per = 32 / G, grp = lane / G, li = lane - grp * G;
+        for (int r0 = gw * per; r0 < R; r0 += NW * per) {
+            const int r = r0 + grp;
+            float bv = kNegInf;
+            int bi = 0x7fffffff;
+            if (r < R && li < np) {
+                const float2 q = __ldcg(base + (size_t)r * P + li);
+                bv = q.x;
+                bi = __float_as_int(q.y);
+            }
+            for (int o = G >> 1; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (am_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            if (li == 0 && r < R) g[r] = bi;
+        }
+    } else if (!MANY_ROWS || R <= NW) {                   // a row per warp and round
+        for (int r = gw; r < R; r += NW) {
+            const float2* pr = base + (size_t)r * P;
+            float bv = kNegInf;
+            int bi = 0x7fffffff;
+            constexpr int kHeld = 4;                       // loads in flight per lane
+            for (int p0 = lane; p0 < np; p0 += 32 * kHeld) {
+                float2 q[kHeld];
 #pragma unroll
-            for (int h = 0; h < kHeld; ++h) {
-                const int p = p0 + 32 * h;
-                q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+                for (int h = 0; h < kHeld; ++h) {
+                    const int p = p0 + 32 * h;
+                    q[h] = p < np ? __ldcg(&pr[p]) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+                }
+#pragma unroll
+                for (int h = 0; h < kHeld; ++h) {
+                    const int qi = __float_as_int(q[h].y);
+                    if (am_better(q[h].x, qi, bv, bi)) { bv = q[h].x; bi = qi; }
+                }
+            }
+            warp_argmax(bv, bi);
+            if (lane == 0) g[r] = bi;
+        }
+    } else if constexpr (MANY_ROWS) {
+        constexpr int kRows = 4, kHeld = 4;              // rows and loads per lane in flight
+        for (int r0 = gw; r0 < R; r0 += NW * kRows) {
+            float bv[kRows];
+            int bi[kRows];
+#pragma unroll
+            for (int j = 0; j < kRows; ++j) { bv[j] = kNegInf; bi[j] = 0x7fffffff; }
+            for (int p0 = lane; p0 < np; p0 += 32 * kHeld) {
+                float2 q[kRows][kHeld];
+#pragma unroll
+                for (int j = 0; j < kRows; ++j)
+#pragma unroll
+                    for (int h = 0; h < kHeld; ++h) {
+                        const int r = r0 + NW * j, p = p0 + 32 * h;
+                        q[j][h] = (r < R && p < np) ? __ldcg(base + (size_t)r * P + p)
+                                                    : make_float2(kNegInf, __int_as_float(0x7fffffff));
+                    }
+#pragma unroll
+                for (int j = 0; j < kRows; ++j)
+#pragma unroll
+                    for (int h = 0; h < kHeld; ++h) {
+                        const int qi = __float_as_int(q[j][h].y);
+                        if (am_better(q[j][h].x, qi, bv[j], bi[j])) { bv[j] = q[j][h].x; bi[j] = qi; }
+                    }
             }
 #pragma unroll
-            for (int h = 0; h < kHeld; ++h) {
-                const int qi = __float_as_int(q[h].y);
-                if (am_better(q[h].x, qi, bv, bi)) { bv = q[h].x; bi = qi; }
+            for (int j = 0; j < kRows; ++j) {
+                warp_argmax(bv[j], bi[j]);
+                if (lane == 0 && r0 + NW * j < R) g[r0 + NW * j] = bi[j];
             }
         }
-        warp_argmax(bv, bi);
-        if (lane == 0) g[r] = bi;
     }
     group_sync_n<NT>();
 }
@@ -339,59 +407,130 @@ static __device__ void decide_greedy(const VerifyArgs& a, int b, int gt, ArgmaxD
 // Draft tree: a node is accepted when its parent is and its token is the
 // argmax of the parent's row; output the longest accepted root path (ties:
 // lowest node ids) and the argmax of the path's last node.
+//
+// Trees of fewer than kTreeParallelNodes nodes take one thread's sweep over
+// the nodes in descending id order (children have larger ids than their
+// parent, so a node is final before its parent reads it; on equal length the
+// lower child id wins), then the walk from the root.  Larger trees take one
+// thread per node (N <= NT), in O(log depth) rounds of pointer doubling:
+//   1. acceptance and depth: each node follows a pointer that doubles its
+//      reach every round, AND-ing the matches and adding the depths of the
+//      segments it jumps;
+//   2. sub(n), the deepest accepted depth in n's subtree: every accepted node
+//      pushes its value (atomic max) to the ancestor its pointer reaches, the
+//      pointer doubling each round, so after round k a node holds the values
+//      of its descendants up to 2^(k+1) - 1 below it (concurrent pushes only
+//      add descendants' depths, which a max tolerates);
+//   3. each accepted node offers (sub, lowest id) to its parent (atomic max):
+//      the parent's chosen child continues the longest path, the lowest id
+//      among equals -- the rule of a sweep that walks from the root;
+//   4. a node is on the path when every link from it to the root is a chosen
+//      one (pointer doubling again); its output slot is its depth - 1, and
+//      the path has sub(root) nodes.
+constexpr int kTreeParallelNodes = 64;
+
 template <int NT>
-static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm) {
-    const int N = a.rows_per_seq;
+static __device__ void decide_tree(const VerifyArgs& a, int b, int gt, ArgmaxDecideSmem& sm,
+                                   TreeWalkSmem& tw) {
+    const int N = a.rows_per_seq;                          // <= NT
     const int* tok = sm.x;                                 // prefetched
     const int* par = sm.par;
     if (gt == 0) sm.bad = 0;
-    merge_argmax_rows<NT>(a, b, gt, sm.g);                     // ends with group_sync
-    for (int n = gt; n < N; n += NT) {
+    merge_argmax_rows<NT, true>(a, b, gt, sm.g);           // ends with group_sync
+    const int n = gt;
+    const bool own = n < N;
+    if (own) {
         const int p = par[n];
         if (n == 0 ? p != -1 : (p < 0 || p >= n)) atomicOr(&sm.bad, SPEC_DEVERR_TREE_PARENT);
         if (n > 0) {
             const int t = tok[n];
             if (t < 0 || t >= a.V) atomicOr(&sm.bad, SPEC_DEVERR_TOKEN_RANGE);
         }
-        sm.depth[n] = 0;
-        sm.best[n] = -1;
     }
     group_sync_n<NT>();
     int32_t* on = a.out_nodes + (size_t)b * N;
     int32_t* ot = a.out_tok + (size_t)b * N;
-    if (gt == 0) {
-        int len = -1;
-        if (sm.bad) {
-            atomicOr(a.err, sm.bad);
-        } else {
-            // Children have larger ids than their parent, so one descending
-            // sweep finalises each node before its parent reads it; on equal
-            // length the lower child id wins.  Nodes whose parent is not
-            // accepted are never reached from the root, which enforces the
-            // parent condition.
-            for (int n = N - 1; n >= 1; --n) {
-                const int p = par[n];
-                if (tok[n] != sm.g[p]) continue;
-                if (1 + sm.depth[n] >= sm.depth[p]) { sm.depth[p] = 1 + sm.depth[n]; sm.best[p] = n; }
+    const int bad = sm.bad;
+    int len = -1;
+    if (!bad && N < kTreeParallelNodes) {
+        // the sweep: sm.sub holds a node's longest accepted continuation, sm.key its child
+        if (own) { tw.sub[n] = 0; tw.key[n] = -1; }
+        __syncthreads();
+        if (gt == 0) {
+            for (int m = N - 1; m >= 1; --m) {
+                const int p = par[m];
+                if (tok[m] != sm.g[p]) continue;
+                if (1 + tw.sub[m] >= tw.sub[p]) { tw.sub[p] = 1 + tw.sub[m]; tw.key[p] = m; }
             }
-            len = 0;
-            int cur = 0;
-            while (sm.best[cur] >= 0) {
-                cur = sm.best[cur];
-                on[len] = cur;
-                ot[len] = tok[cur];
-                ++len;
+            int l = 0, cur = 0;
+            while (tw.key[cur] >= 0) {
+                cur = tw.key[cur];
+                on[l] = cur;
+                ot[l] = tok[cur];
+                ++l;
             }
-            ot[len] = sm.g[cur];
+            ot[l] = sm.g[cur];
+            sm.len = l;
         }
-        sm.len = len;
+        __syncthreads();
+        len = sm.len;
+    } else if (!bad) {
+        // 1. acceptance and depth
+        int u = own && n > 0 ? par[n] : -1;
+        int ac = own && (n == 0 || tok[n] == sm.g[par[n]]) ? 1 : 0;
+        int d = own && n > 0 ? 1 : 0;
+        if (own) { tw.up[n] = u; tw.acc[n] = ac; tw.dep[n] = d; }
+        while (__syncthreads_or(u >= 0)) {
+            int nu = -1;
+            if (u >= 0) { ac &= tw.acc[u]; d += tw.dep[u]; nu = tw.up[u]; }
+            __syncthreads();
+            u = nu;
+            if (own) { tw.up[n] = u; tw.acc[n] = ac; tw.dep[n] = d; }
+        }
+        // 2. deepest accepted depth of every subtree
+        int w = own && n > 0 ? par[n] : -1;
+        if (own) { tw.sub[n] = ac ? d : -1; tw.up[n] = w; tw.key[n] = -1; }
+        while (__syncthreads_or(w >= 0)) {
+            const int v = own ? tw.sub[n] : -1;
+            if (w >= 0 && v >= 0) atomicMax(&tw.sub[w], v);
+            const int nw = w >= 0 ? tw.up[w] : -1;
+            __syncthreads();
+            w = nw;
+            if (own) tw.up[n] = w;
+        }
+        // 3. the chosen child of every node: longest continuation, lowest id
+        if (own && n > 0 && ac) atomicMax(&tw.key[par[n]], (tw.sub[n] << 11) | (2047 - n));
+        __syncthreads();
+        // 4. the path: nodes whose every link to the root is a chosen one
+        auto chosen = [&](int p) { const int k = tw.key[p]; return k >= 0 ? 2047 - (k & 2047) : -1; };
+        int v2 = own && n > 0 ? par[n] : -1;
+        int ok = own && (n == 0 || chosen(par[n]) == n) ? 1 : 0;
+        if (own) { tw.up[n] = v2; tw.acc[n] = ok; }
+        while (__syncthreads_or(v2 >= 0)) {
+            int nv = -1;
+            if (v2 >= 0) { ok &= tw.acc[v2]; nv = tw.up[v2]; }
+            __syncthreads();
+            v2 = nv;
+            if (own) { tw.up[n] = v2; tw.acc[n] = ok; }
+        }
+        len = tw.sub[0];                                   // the root is accepted: depth 0 or more
+        if (gt == 0) sm.last = 0;
+        __syncthreads();
+        if (own && n > 0 && ok) {
+            on[d - 1] = n;
+            ot[d - 1] = tok[n];
+            if (d == len) sm.last = n;
+        }
+        __syncthreads();
+        if (gt == 0) ot[len] = sm.g[sm.last];
+    }
+    if (gt == 0) {
+        if (bad) atomicOr(a.err, bad);
         a.out_acc[b] = len;
     }
-    group_sync_n<NT>();
-    const int len = sm.len;
-    for (int n = gt; n < N; n += NT) {
-        if (len < 0 || n >= len) on[n] = -1;
-        if (len < 0 || n > len) ot[n] = -1;
+    for (int m = gt; m < N; m += NT) {
+        if (len < 0 || m >= len) on[m] = -1;
+        if (len < 0 || m > len) ot[m] = -1;
     }
 }
 

@@ -107,9 +107,14 @@ def test_tree_small(sv, B, V, depth, branches):
     check_tree(sv, W.make_tree(B=B, V=V, depth=depth, branches=branches))
 
 
-def test_tree_random_topologies_with_ties(sv):
-    rng = np.random.default_rng(1)
-    B, N, V = 24, 40, 600
+@pytest.mark.parametrize("N", [40, 200])
+def test_tree_random_topologies_with_ties(sv, N):
+    """Random parents, integer logits (massive argmax ties) and 80% of tokens
+    equal to the parent's argmax, so sibling paths of equal length are common:
+    the lowest node ids must win.  40 nodes take the decide kernel's sweep,
+    200 its pointer-doubling walk."""
+    rng = np.random.default_rng(N)
+    B, V = 24, 600
     z = rng.integers(-2, 3, (B, N, V)).astype(np.float32)
     par = np.empty((B, N), np.int32)
     tok = np.empty((B, N), np.int32)
@@ -308,9 +313,12 @@ def test_greedy_longest_chain(sv):
     assert ref["accepted"].tolist() == [700, 1023]
 
 
-def test_tree_largest(sv):
-    # 1 + 31 + 31 * 32 = 1024 nodes, the most a tree call takes
-    t = W.make_tree(B=2, V=2048, depth=31, branches=32, match_prob=0.9)
+@pytest.mark.parametrize("depth,branches,match", [(31, 32, 0.9), (1023, 0, 1.0), (1023, 0, 0.995)])
+def test_tree_largest(sv, depth, branches, match):
+    """1024 nodes, the most a tree call takes: 1 + 31 + 31 * 32 (wide and shallow),
+    or a chain of 1023 below the root, every node accepted (the walk is 1023
+    long) or a few mismatches along it."""
+    t = W.make_tree(B=2, V=2048, depth=depth, branches=branches, match_prob=match)
     assert t.node_tokens.shape[1] == 1024
     check_tree(sv, t)
 
