@@ -293,8 +293,8 @@ spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype
  * library places in the device memory of every GPU it is loaded on, held
  * until the process exits.  Problems whose scratch need,
  * spec_verify_workspace_size(B, gamma, V), exceeds it are rejected with
- * SPEC_ERR_EXCEEDS_STATIC_SCRATCH before anything is launched (the five
- * benchmark workloads need at most about 2.4 MB).
+ * SPEC_ERR_EXCEEDS_STATIC_SCRATCH before anything is launched (B = 256
+ * sequences of 4 drafts over 128256 fp32 logits need 3.4 MB).
  *
  * The first call on each device, made while that device is current, looks up
  * the array's device address (cudaGetSymbolAddress, which may also load the
