@@ -104,10 +104,58 @@ struct SampleDecideSmem {
     int bad, k;
 };
 
-// Row r of sequence b from its warp partials (one warp, every lane gets the
-// result): M = max m_p and lnZ = ln sum_p Z_p 2^((m_p - M) s - r_p), with
-// r_p = partial_residual(m_p) (float-float sum, each lane holding up to
-// kHeld partials in registers).  lnZ is 0 for a row without a finite logit.
+// Rows r[0..RB) of sequence b from their warp partials (one warp, every lane
+// gets the results; rows at or past rows_per_seq are skipped): M = max m_p and
+// lnZ = ln sum_p Z_p 2^((m_p - M) s - r_p), with r_p = partial_residual(m_p)
+// (float-float sum).  Each lane holds up to KH partials of each row in
+// registers, all rows' loads in flight together, and adds a row's partials in
+// increasing p whatever RB and KH are, so every row's result is bit-identical
+// across batch shapes.  lnZ is 0 for a row without a finite logit.
+template <int RB, int KH>
+__device__ __forceinline__ void merge_rows_stats(const VerifyArgs& a, int b, const int (&r)[RB], int lane,
+                                                 float (&Mout)[RB], float (&lnZout)[RB]) {
+    const int P = a.nseg * kWarps;
+    float2 q[RB][KH];
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r[j]) * P;
+#pragma unroll
+        for (int h = 0; h < KH; ++h) {
+            const int p = lane + 32 * h;
+            q[j][h] = (r[j] < a.rows_per_seq && p < P) ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+        if (r[j] >= a.rows_per_seq) continue;             // warp-uniform
+        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r[j]) * P;
+        float m = kNegInf;
+#pragma unroll
+        for (int h = 0; h < KH; ++h) m = fmaxf(m, q[j][h].x);
+        for (int p = lane + 32 * KH; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
+        m = warp_max(m);
+        FF z{0.f, 0.f};
+        if (m != kNegInf) {
+#pragma unroll
+            for (int h = 0; h < KH; ++h)
+                if (q[j][h].x != kNegInf)
+                    ff_add(z, q[j][h].y * ex2_approx(fmaf(q[j][h].x - m, a.s, -partial_residual(q[j][h].x, a.s))));
+            for (int p = lane + 32 * KH; p < P; p += 32) {
+                const float2 t = __ldcg(&pr[p]);
+                if (t.x != kNegInf)
+                    ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
+            }
+        }
+        z = ff_norm(warp_sum_ff(z));
+        Mout[j] = m;
+        lnZout[j] = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
+    }
+}
+
+// One row, eight partials per lane in registers: the same sums as
+// merge_rows_stats, written out for the sampling decide (a template-built
+// version of this one-row merge measured 4 us slower in the chained
+// chain-b64 step, with the same registers and shared memory).
 __device__ __forceinline__ void merge_row_stats(const VerifyArgs& a, int b, int r, int lane,
                                                 float* Mout, float* lnZout) {
     constexpr int kHeld = 8;
@@ -141,6 +189,36 @@ __device__ __forceinline__ void merge_row_stats(const VerifyArgs& a, int b, int 
     *lnZout = m == kNegInf ? 0.f : logf(z.hi) + z.lo / z.hi;
 }
 
+// Rows [0, n) of sequence b given by row(q), the warps of an NT-thread group
+// sharing them: a row per warp and round while they fit, else four rows per
+// warp and round.  Stores (M, lnZ) of row q at M[q], lnZ[q].
+template <int NT, typename RowOf>
+__device__ __forceinline__ void merge_rows_group(const VerifyArgs& a, int b, int n, RowOf row, int gt,
+                                                 float* M, float* lnZ) {
+    constexpr int NW = NT / 32;
+    const int lane = gt & 31, gw = gt >> 5;
+    if (n <= NW) {
+        if (gw < n) {
+            float m, l;
+            merge_row_stats(a, b, row(gw), lane, &m, &l);
+            if (lane == 0) { M[gw] = m; lnZ[gw] = l; }
+        }
+        return;
+    }
+    constexpr int RB = 4;
+    for (int q0 = gw; q0 < n; q0 += NW * RB) {
+        int rr[RB];
+#pragma unroll
+        for (int j = 0; j < RB; ++j) rr[j] = q0 + NW * j < n ? row(q0 + NW * j) : a.rows_per_seq;
+        float m[RB], l[RB];
+        merge_rows_stats<RB, 4>(a, b, rr, lane, m, l);
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < RB; ++j)
+                if (q0 + NW * j < n) { M[q0 + NW * j] = m[j]; lnZ[q0 + NW * j] = l[j]; }
+    }
+}
+
 // ln p(x) = (z_x - M)/T - lnZ for a row with max M and normaliser lnZ.
 __device__ __forceinline__ float row_log_prob(float zx, float M, float lnZ, const VerifyArgs& a) {
     return (zx - M) / a.T - lnZ;
@@ -167,7 +245,6 @@ __device__ __forceinline__ bool accept_draft(float lp, float lq, float u) {
 // in sm.
 template <int ELT, int NT>
 __device__ int decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSmem& sm) {
-    const int lane = gt & 31, gw = gt >> 5;
     const size_t rowbytes = (size_t)a.V * ELT;
     if (!a.early_inputs) pdl_wait();   // first kernel of the call: the kernel before may write the inputs
     // Issue the gathers of z[x_i] first: their latency overlaps the merges.
@@ -189,10 +266,10 @@ __device__ int decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSme
     // stream, which may still be finishing.
     pdl_wait();
     group_sync_n<NT>();
-    for (int r = gw; r < a.rows_per_seq; r += NT / 32) {
+    for (int r = (gt >> 5); r < a.rows_per_seq; r += NT / 32) {
         float M, lnZ;
-        merge_row_stats(a, b, r, lane, &M, &lnZ);
-        if (lane == 0) {
+        merge_row_stats(a, b, r, gt & 31, &M, &lnZ);
+        if ((gt & 31) == 0) {
             sm.M[r] = M;
             sm.lnZ[r] = lnZ;
         }

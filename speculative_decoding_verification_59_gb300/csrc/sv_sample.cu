@@ -655,7 +655,7 @@ constexpr int kLazyDecideThreads = 512;
 template <int ELT>
 __global__ void __launch_bounds__(kLazyDecideThreads) lazy_decide_kernel(const VerifyArgs a) {
     __shared__ LazyDecideSmem sm;
-    const int gt = threadIdx.x, lane = gt & 31, gw = gt >> 5;
+    const int gt = threadIdx.x;
     const int lo = a.lz_lo, nt = a.lz_nt, nd = a.lz_nd;
     const size_t rowbytes = (size_t)a.V * ELT;
     const bool first = a.lz_list == nullptr;
@@ -687,15 +687,8 @@ __global__ void __launch_bounds__(kLazyDecideThreads) lazy_decide_kernel(const V
         b = __ldcg(a.lz_list + blockIdx.x);
         gather(b);
     }
-    for (int q = gw; q < nt + nd; q += kLazyDecideThreads / 32) {
-        const int r = q < nt ? lo + q : a.gamma + 1 + lo + (q - nt);
-        float M, lnZ;
-        merge_row_stats(a, b, r, lane, &M, &lnZ);
-        if (lane == 0) {
-            sm.M[q] = M;
-            sm.lnZ[q] = lnZ;
-        }
-    }
+    merge_rows_group<kLazyDecideThreads>(
+        a, b, nt + nd, [&](int q) { return q < nt ? lo + q : a.gamma + 1 + lo + (q - nt); }, gt, sm.M, sm.lnZ);
     bad = __syncthreads_or(bad);
     if (gt == 0) {
         int k = -2, bits = bad ? SPEC_DEVERR_TOKEN_RANGE : 0;
