@@ -25,7 +25,9 @@ pytestmark = pytest.mark.gpu
 
 RATE_BAR = 1e-4
 ROWS_TARGET = 100_000
-OUT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+# Per-workload reports (counts and every excused case) go to this directory
+# when the variable names one that exists.
+OUT = os.environ.get("SPEC_VERIFY_REPORT_DIR", "")
 
 
 @pytest.fixture(scope="module")
@@ -78,7 +80,7 @@ def test_sampling_mismatch_rate(sv, name):
                "mean_tokens_per_round": float(np.mean(accepted)) + 1.0,
                "max_prob_rel_err": lp_err, "excused_events": events[:50]}
     print(json.dumps(summary))
-    if os.path.isdir(OUT):
+    if OUT and os.path.isdir(OUT):
         with open(os.path.join(OUT, f"rate_{name}.json"), "w") as f:
             json.dump(summary, f)
     assert not failures, failures[:5]
