@@ -663,7 +663,7 @@ def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, de
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
     k = acc.cpu().numpy().astype(np.int64)
     elt = 2 if x.dtype == "bf16" else 4
-    groups = lazy_groups(B, g, V * elt)
+    groups = sv.lazy_groups(B, g, V, dcode)
     rows_read = int(sum(lazy_rows_read(int(kb), groups) for kb in k))
     bytes_read = rows_read * V * elt
     return {"what": "lazy stochastic verification (rows of the position groups after the one "
@@ -674,27 +674,6 @@ def time_lazy(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, de
             "pass1_rows_read": rows_read, "pass1_rows_full": B * (2 * g + 1),
             "pass1_bytes_read": bytes_read, "pass1_bytes_full": acct["bytes_stats"],
             "gpu_launches_per_call": 2 * len(groups) + 1}
-
-
-def lazy_groups(B, g, rowbytes):
-    """Position groups of the lazy pass, as the library forms them: sizes
-    doubling from 2 ([0, 2), [2, 6), [6, 14), ...), the last one ending with
-    position g (the bonus row); a group runs on to the end (at most 128
-    positions) when the rows after it, for all B sequences, hold fewer than
-    96 MB (SPEC_VERIFY_LAZY_SPLIT_BYTES overrides the figure)."""
-    env = os.environ.get("SPEC_VERIFY_LAZY_SPLIT_BYTES", "")
-    try:
-        split = float(env) if env else 96.0 * (1 << 20)
-    except ValueError:
-        split = 96.0 * (1 << 20)
-    out, lo, n = [], 0, 2
-    while lo <= g and len(out) < 8:
-        hi = min(lo + min(n, 128), g + 1)
-        if B * rowbytes * ((g + 1 - hi) + (g - min(hi, g))) < split:
-            hi = min(lo + 128, g + 1)
-        out.append((lo, hi))
-        lo, n = hi, 2 * n
-    return out
 
 
 def lazy_rows_read(k, groups):

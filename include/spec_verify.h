@@ -150,6 +150,21 @@ spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* dra
                                       cudaStream_t stream);
 
 /*
+ * The position groups that spec_verify_sample_lazy streams for B sequences of
+ * gamma drafts over V logits of the given dtype ([SD] "What happens in one
+ * round", step 3, read as in spec_verify_sample_lazy): writes the groups'
+ * upper ends, exclusive, to ends[0 .. count) in ascending order (group g
+ * covers positions ends[g-1] .. ends[g]-1, from 0; the last end is gamma + 1)
+ * and returns count, at most 8.  The sizes double from 2 -- [0,2), [2,6),
+ * [6,14), ... -- and a group runs on to the end (at most 128 positions) when
+ * the rows after it, for all B sequences, hold fewer than 96 MB (or
+ * SPEC_VERIFY_LAZY_SPLIT_BYTES when that variable is set).  Host only, no CUDA
+ * call; returns 0 for invalid arguments (B < 1, gamma outside 0..256, V < 1,
+ * an unknown dtype, ends NULL).  ends must hold 8 entries.
+ */
+int spec_verify_lazy_groups(int B, int gamma, int V, spec_dtype_t dtype, int32_t* ends);
+
+/*
  * The two halves of spec_verify_sample, for callers that want to overlap or
  * time them separately; spec_verify_sample is exactly _stats then _finish on
  * the same stream with the same arguments and workspace.

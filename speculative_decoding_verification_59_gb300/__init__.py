@@ -51,6 +51,7 @@ SIGNATURES = {
                             _P], _I),
     "spec_verify_sample_lazy": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _S,
                                  _P], _I),
+    "spec_verify_lazy_groups": ([_I, _I, _I, _I, _P], _I),
     "spec_verify_sample_stats": ([_P, _P, _I, ctypes.c_float, _I, _I, _I, _P, _S, _P], _I),
     "spec_verify_sample_finish": ([_P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P,
                                    _S, _P], _I),
@@ -149,6 +150,24 @@ def spec_verify_sample_lazy(target, draft, dtype, draft_tokens, uniforms, temper
                                                   temperature, B, gamma, V, out_tokens,
                                                   out_num_accepted, out_logprobs, ws, ws_bytes,
                                                   stream)
+
+
+def spec_verify_lazy_groups(B, gamma, V, dtype, ends) -> int:
+    return load_library().spec_verify_lazy_groups(B, gamma, V, dtype, ends)
+
+
+def lazy_groups(B: int, gamma: int, V: int, dtype: int):
+    """Position groups of spec_verify_sample_lazy as [(lo, hi), ...] (host only,
+    no GPU needed); raises for invalid arguments."""
+    ends = (ctypes.c_int32 * 8)()
+    n = spec_verify_lazy_groups(B, gamma, V, dtype, ctypes.addressof(ends))
+    if n < 1:
+        raise ValueError(f"spec_verify_lazy_groups: invalid arguments {(B, gamma, V, dtype)}")
+    out, lo = [], 0
+    for g in range(n):
+        out.append((lo, int(ends[g])))
+        lo = int(ends[g])
+    return out
 
 
 def spec_verify_sample_stats(target, draft, dtype, temperature, B, gamma, V, ws, ws_bytes,

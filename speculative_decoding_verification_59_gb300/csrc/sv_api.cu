@@ -98,6 +98,15 @@ spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* dra
                          workspace_bytes, stream, kSampleLazy);
 }
 
+int spec_verify_lazy_groups(int B, int gamma, int V, spec_dtype_t dtype, int32_t* ends) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
+    if (B < 1 || gamma < 0 || gamma > kMaxGammaApi || V < 1 || !ends) return 0;
+    int e[kLazyGroups];
+    const int n = lazy_groups_host(B, gamma, (size_t)V * elt_size(dtype), e);
+    for (int g = 0; g < n; ++g) ends[g] = e[g];
+    return n;
+}
+
 spec_status_t spec_verify_sample_stats(const void* target_logits, const void* draft_logits,
                                        spec_dtype_t dtype, float temperature, int B, int gamma,
                                        int V, void* workspace, size_t workspace_bytes,

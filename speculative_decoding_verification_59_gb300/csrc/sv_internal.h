@@ -118,6 +118,10 @@ inline cudaError_t device_once(DeviceSlots& slots, int* out, F setup) {
     return cudaSuccess;
 }
 
+// Upper ends of the lazy pass's position groups (host only; ends holds
+// kLazyGroups entries); returns their count.
+int lazy_groups_host(int B, int gamma, size_t rowbytes, int* ends);
+
 // ---- launchers (return the first CUDA error) ------------------------------
 // parts: kSampleStats (streaming row statistics), kSampleFinish (the accept
 // decisions and the final residual/bonus token), both, or kSampleLazy.

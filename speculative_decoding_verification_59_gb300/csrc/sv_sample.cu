@@ -790,6 +790,13 @@ static int lazy_group_ends(int B, int gamma, size_t rowbytes, int (&hi)[kLazyGro
     return ng;
 }
 
+int lazy_groups_host(int B, int gamma, size_t rowbytes, int* ends) {
+    int hi[kLazyGroups];
+    const int n = lazy_group_ends(B, gamma, rowbytes, hi);
+    for (int g = 0; g < n; ++g) ends[g] = hi[g];
+    return n;
+}
+
 // The lazy pass: per position group a stream and a decide kernel, chained
 // with programmatic dependent launch; the first group's stream zeroes the
 // later groups' survivor counts.

@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(spec_verify_[a-z_]+)\s*\(",
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(spec_[a-z_]+)\s*\(",
                        text, flags=re.M)
     return sorted(set(names))
 
@@ -35,6 +35,35 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in sv.SIGNATURES, n
+
+
+def test_lazy_groups_schedule(lib, monkeypatch):
+    """The lazy pass's position groups, from the host-only schedule call: the
+    benchmark workloads' groups, the doubling schedule with every boundary
+    taken, and its invariants for every gamma."""
+    monkeypatch.delenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", raising=False)
+    bf16, f32 = sv.SPEC_DTYPE_BF16, sv.SPEC_DTYPE_F32
+    assert sv.lazy_groups(64, 7, 151936, bf16) == [(0, 2), (2, 8)]        # 58 MB after [2, 6)
+    assert sv.lazy_groups(8, 7, 151936, bf16) == [(0, 8)]                 # 32 MB after [0, 2)
+    assert sv.lazy_groups(256, 4, 128256, f32) == [(0, 2), (2, 5)]
+    assert sv.lazy_groups(1, 0, 1000, f32) == [(0, 1)]
+    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", "0")
+    assert sv.lazy_groups(1, 7, 1000, f32) == [(0, 2), (2, 6), (6, 8)]
+    assert sv.lazy_groups(1, 256, 1000, f32) == [(0, 2), (2, 6), (6, 14), (14, 30), (30, 62),
+                                                 (62, 126), (126, 254), (254, 257)]
+    for split in ("0", "100000000000"):
+        monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", split)
+        for gamma in range(0, 257):
+            gr = sv.lazy_groups(3, gamma, 4096, bf16)
+            assert gr[0][0] == 0 and gr[-1][1] == gamma + 1 and len(gr) <= 8
+            for (lo, hi), (lo2, _) in zip(gr, gr[1:]):
+                assert hi == lo2
+            for g, (lo, hi) in enumerate(gr):
+                assert 0 < hi - lo <= 128
+                assert hi - lo >= min(2 << g, gamma + 1 - lo, 128)
+    with pytest.raises(ValueError):
+        sv.lazy_groups(0, 7, 1000, f32)
+    assert sv.spec_verify_lazy_groups(1, 257, 1000, f32, ctypes.addressof((ctypes.c_int32 * 8)())) == 0
 
 
 def test_workspace_size_monotone_and_invalid(lib):
