@@ -239,6 +239,32 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _check_tensor(t, name: str, shape, dtypes, device=None):
+    """Raises unless t is a contiguous CUDA tensor of one of dtypes, of the
+    given shape (None entries match anything) and, when given, on device: the
+    C ABI reads raw device memory, so a strided, host-resident or mistyped
+    tensor would be read as garbage rather than rejected."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor, got {type(t).__name__}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor, got device {t.device}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the other arguments on {device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if len(t.shape) != len(shape) or any(w is not None and w != h for w, h in zip(shape, t.shape)):
+        raise ValueError(f"{name} must have shape {tuple('*' if w is None else w for w in shape)}, "
+                         f"got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _logits_dtypes():
+    torch = _torch()
+    return (torch.float32, torch.bfloat16)
+
+
 def _stream(stream) -> int:
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
@@ -297,15 +323,24 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, 
     lazy=True: spec_verify_sample_lazy (same outputs, rows after the first
     rejection not read, their log-probabilities NaN)."""
     torch = _torch()
+    _check_tensor(target, "target", (None, None, None), _logits_dtypes())
     B, g1, V = target.shape
     g = g1 - 1
     dev = target.device
+    if g > 0:
+        _check_tensor(draft, "draft", (B, g, V), (target.dtype,), dev)
+        _check_tensor(draft_tokens, "draft_tokens", (B, g), (torch.int32,), dev)
+    _check_tensor(uniforms, "uniforms", (B, g1), (torch.float32,), dev)
     if out is None:
         tok = torch.empty((B, g1), dtype=torch.int32, device=dev)
         acc = torch.empty((B,), dtype=torch.int32, device=dev)
         lp = torch.empty((B, g, 2), dtype=torch.float32, device=dev) if logprobs else None
     else:
         tok, acc, lp = out
+        _check_tensor(tok, "out tokens", (B, g1), (torch.int32,), dev)
+        _check_tensor(acc, "out num_accepted", (B,), (torch.int32,), dev)
+        if lp is not None:
+            _check_tensor(lp, "out logprobs", (B, g, 2), (torch.float32,), dev)
     ws = _ws(workspace, dev)
     wp, wb = ws.get(B, g, V, stream)
     fn = spec_verify_sample_lazy if lazy else spec_verify_sample
@@ -322,14 +357,20 @@ def topk_exclude(logits, K: int, exclude=None, *, values=False,
     CUDA tensor (bf16 or fp32), exclude int32 with one entry per row or None.
     Returns idx [..., K] int32 (and, with values=True, the logits [..., K])."""
     torch = _torch()
+    _check_tensor(logits, "logits", (None,) * max(logits.dim(), 1), _logits_dtypes())
     V = logits.shape[-1]
     rows = logits.numel() // V
     dev = logits.device
+    if exclude is not None:
+        _check_tensor(exclude, "exclude", tuple(logits.shape[:-1]), (torch.int32,), dev)
     if out is None:
         idx = torch.empty((*logits.shape[:-1], K), dtype=torch.int32, device=dev)
         val = torch.empty((*logits.shape[:-1], K), dtype=torch.float32, device=dev) if values else None
     else:
         idx, val = out
+        _check_tensor(idx, "out idx", (*logits.shape[:-1], K), (torch.int32,), dev)
+        if val is not None:
+            _check_tensor(val, "out values", (*logits.shape[:-1], K), (torch.float32,), dev)
     ws = _ws(workspace, dev)
     wp, wb = ws.get_bytes(spec_topk_workspace_size(rows, V, K), stream)
     st = spec_topk_exclude(_ptr(logits), _dtype_code(logits), rows, V, K, _ptr(exclude), _ptr(idx),
@@ -344,8 +385,10 @@ def ngram_retrieve(tokens, lengths, w: int, L: int, max_matches: int, *,
     (n_max a multiple of 4), lengths [B] int32, CUDA tensors.  Returns
     (count [B], matches [B, max_matches], draft [B, L])."""
     torch = _torch()
+    _check_tensor(tokens, "tokens", (None, None), (torch.int32,))
     B, n_max = tokens.shape
     dev = tokens.device
+    _check_tensor(lengths, "lengths", (B,), (torch.int32,), dev)
     cnt = torch.empty((B,), dtype=torch.int32, device=dev)
     mat = torch.empty((B, max_matches), dtype=torch.int32, device=dev)
     dr = torch.empty((B, max(L, 1)), dtype=torch.int32, device=dev)
@@ -363,8 +406,12 @@ def cosine_topk(hidden, query, delta: int, positions=None, *,
     [B, d] (same dtype, bf16 or fp32), positions [B, W] int32 or None, CUDA
     tensors.  Returns (idx [B, delta], pos [B, delta], score [B, delta])."""
     torch = _torch()
+    _check_tensor(hidden, "hidden", (None, None, None), _logits_dtypes())
     B, W, d = hidden.shape
     dev = hidden.device
+    _check_tensor(query, "query", (B, d), (hidden.dtype,), dev)
+    if positions is not None:
+        _check_tensor(positions, "positions", (B, W), (torch.int32,), dev)
     idx = torch.empty((B, delta), dtype=torch.int32, device=dev)
     pos = torch.empty((B, delta), dtype=torch.int32, device=dev)
     sc = torch.empty((B, delta), dtype=torch.float32, device=dev)
@@ -380,14 +427,19 @@ def verify_greedy(target, draft_tokens, *, workspace: Optional[Workspace] = None
                   stream=None):
     """Greedy verification (see spec_verify_greedy).  Returns (tokens, num_accepted)."""
     torch = _torch()
+    _check_tensor(target, "target", (None, None, None), _logits_dtypes())
     B, g1, V = target.shape
     g = g1 - 1
     dev = target.device
+    if g > 0:
+        _check_tensor(draft_tokens, "draft_tokens", (B, g), (torch.int32,), dev)
     if out is None:
         tok = torch.empty((B, g1), dtype=torch.int32, device=dev)
         acc = torch.empty((B,), dtype=torch.int32, device=dev)
     else:
         tok, acc = out
+        _check_tensor(tok, "out tokens", (B, g1), (torch.int32,), dev)
+        _check_tensor(acc, "out num_accepted", (B,), (torch.int32,), dev)
     ws = _ws(workspace, dev)
     wp, wb = ws.get(B, g, V, stream)
     st = spec_verify_greedy(_ptr(target), _dtype_code(target), _ptr(draft_tokens) if g > 0 else None,
@@ -401,14 +453,20 @@ def verify_tree_greedy(target, node_tokens, parents, *, workspace: Optional[Work
     """Greedy tree verification (see spec_verify_tree_greedy).  Returns
     (path_nodes [B, N], tokens [B, N], num_accepted [B])."""
     torch = _torch()
+    _check_tensor(target, "target", (None, None, None), _logits_dtypes())
     B, N, V = target.shape
     dev = target.device
+    _check_tensor(node_tokens, "node_tokens", (B, N), (torch.int32,), dev)
+    _check_tensor(parents, "parents", (B, N), (torch.int32,), dev)
     if out is None:
         nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
         tok = torch.empty((B, N), dtype=torch.int32, device=dev)
         acc = torch.empty((B,), dtype=torch.int32, device=dev)
     else:
         nodes, tok, acc = out
+        _check_tensor(nodes, "out path_nodes", (B, N), (torch.int32,), dev)
+        _check_tensor(tok, "out tokens", (B, N), (torch.int32,), dev)
+        _check_tensor(acc, "out num_accepted", (B,), (torch.int32,), dev)
     ws = _ws(workspace, dev)
     wp, wb = ws.get(B, N, V, stream)
     st = spec_verify_tree_greedy(_ptr(target), _dtype_code(target), _ptr(node_tokens),

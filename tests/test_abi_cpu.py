@@ -195,3 +195,29 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sv, "_lib", None)
     with pytest.raises(ImportError):
         sv.load_library()
+
+
+def test_tensor_helpers_reject_bad_tensors():
+    """The tensor-level helpers check device, dtype, shape and contiguity
+    before anything reaches the C ABI (which would read raw memory)."""
+    torch = pytest.importorskip("torch")
+    z = torch.zeros((2, 4, 64))
+    x = torch.zeros((2, 3), dtype=torch.int32)
+    u = torch.zeros((2, 4))
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.verify_sample(z, z[:, :3], x, u, 1.0)
+    with pytest.raises(TypeError, match="torch tensor"):
+        sv.verify_greedy(z.numpy(), x)
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.verify_tree_greedy(z, x, x)
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.topk_exclude(z.reshape(8, 64), 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.ngram_retrieve(torch.zeros((2, 8), dtype=torch.int32), torch.zeros(2, dtype=torch.int32),
+                          3, 7, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.cosine_topk(z, z[:, 0], 4)
+    # dtype and shape are checked the same way (on the first, CUDA-independent, failing
+    # property): a mistyped logits tensor is a TypeError
+    with pytest.raises((TypeError, ValueError)):
+        sv.verify_sample(z.to(torch.float64), z[:, :3], x, u, 1.0)
