@@ -347,3 +347,21 @@ def test_sample_many_equal_ratios(sv, dtype):
     for r in range(4):
         x.uniforms = rng.random((B, g + 1), dtype=np.float32)
         check_sample(sv, x)
+
+
+@pytest.mark.parametrize("name,V", [("chain-b8", 8), ("chain-b8", 16), ("chain-b8", 24),
+                                    ("chain-b256", 4), ("chain-b256", 8)])
+def test_rows_of_one_to_three_vectors(sv, name, V):
+    """Rows of 16 to 48 bytes take the bulk-copy ring (their length is a
+    multiple of 16): a stage and a warp chunk hold a few bytes, the rest of the
+    warp chunk reads as -inf.  Sampling, lazy sampling, greedy and tree
+    verification against the oracle."""
+    x = W.make_chain(name, B=5, gamma=3, V=V)
+    check_sample(sv, x)
+    tok, acc = sv.verify_sample(dev_logits(x.target, x.dtype), dev_logits(x.draft, x.dtype),
+                                dev(x.draft_tokens), dev(x.uniforms), x.T, lazy=True)
+    full = run_sample(sv, x)
+    torch.cuda.synchronize()
+    assert np.array_equal(tok.cpu().numpy(), full[0]) and np.array_equal(acc.cpu().numpy(), full[1])
+    check_greedy(sv, x.target, x.dtype, x.greedy_tokens)
+    check_tree(sv, W.make_tree(B=3, V=V, depth=3, branches=2))
