@@ -4,7 +4,7 @@
 // Source: "AdaPLD: adaptive retrieval and reuse for efficient model-free
 // speculative decoding", section 3.3 (strict hit path: the branches are the
 // target model's top K next tokens, without the token the copied main path
-// already starts with) and Algorithm 1 (TopKNextTokens(M, x_{<=p*}, K) \
+// already starts with) and Algorithm 1 (TopKNextTokens(M, x_{<=p*}, K) minus
 // {d_main[1]}; without the exclusion on the semantic hit path).
 //
 // The top K of a row is taken by (larger logit, lower index): temperature does
