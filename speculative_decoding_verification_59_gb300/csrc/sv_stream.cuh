@@ -348,15 +348,23 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
         *y += 0.0f;                                        // -0.0 counts as +0.0
         *j = base + (lane + 32 * t) * PV + e;
     };
-    // exclusive prefix of the lanes' counts
+    // inclusive prefix of the lanes' counts: a popcount of a ballot when no
+    // lane marks more than one element (the common case), else a warp scan
     const int n = __popcll(mask);
-    int incl = n;
+    const unsigned has = __ballot_sync(0xffffffffu, n > 0);
+    int incl, total;
+    if (__ballot_sync(0xffffffffu, n > 1) == 0u) {        // warp-uniform
+        incl = __popc(has & ((2u << lane) - 1u));
+        total = __popc(has);
+    } else {
+        incl = n;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        total = __shfl_sync(0xffffffffu, incl, 31);
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (total <= KS) {                                     // warp-uniform
         int slot = incl - n;
 #pragma unroll 1
