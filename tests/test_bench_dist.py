@@ -88,3 +88,16 @@ def test_reference_arm_prints_the_contract_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["workload"] == "chain-small"
+
+
+def test_lazy_rows_read_accounting():
+    """Rows the lazy pass reads per sequence, as bench.py reports them: every
+    group up to the one holding the sequence's rejection (or the bonus row),
+    target and draft rows of its positions (the last position has no draft
+    row)."""
+    import bench
+    groups = [(0, 2), (2, 8)]                          # chain-b64's schedule, gamma = 7
+    assert [bench.lazy_rows_read(k, groups) for k in (-1, 0, 1)] == [4, 4, 4]
+    assert all(bench.lazy_rows_read(k, groups) == 4 + 6 + 5 for k in range(2, 8))
+    assert bench.lazy_rows_read(0, [(0, 1)]) == 1       # gamma = 0: the bonus row only
+    assert bench.lazy_rows_read(4, [(0, 2), (2, 5)]) == 4 + 3 + 2
