@@ -320,8 +320,9 @@ def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, *, 
     draft [B, g, V] (same dtype), draft_tokens [B, g] int32, uniforms
     [B, g+1] float32, all contiguous CUDA tensors.  Returns (tokens [B, g+1],
     num_accepted [B]) or, with logprobs=True, also [B, g, 2] log-probabilities.
-    lazy=True: spec_verify_sample_lazy (same outputs, rows after the first
-    rejection not read, their log-probabilities NaN)."""
+    lazy=True: spec_verify_sample_lazy (same tokens and counts; the rows of the
+    position groups after the one holding a sequence's first rejection are not
+    read, and the log-probabilities of positions after the rejection are NaN)."""
     torch = _torch()
     _check_tensor(target, "target", (None, None, None), _logits_dtypes())
     B, g1, V = target.shape
