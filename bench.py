@@ -163,6 +163,13 @@ class ClockSampler:
             if len(parts) >= 10:
                 self.samples.append((time.time(), parts))
 
+    def wait_first(self, timeout_s=5.0):
+        """Blocks (at most timeout_s) until nvidia-smi has delivered a sample, so
+        that even a timed region of a few milliseconds falls inside the record."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            time.sleep(0.02)
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -171,11 +178,19 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, run=None):
+        """Clocks over the timed region [t0, t1] (with 0.15 s of slack).  A
+        region shorter than the 100 ms sampling period may hold no sample; the
+        samples of the whole GPU run `run` = (start, end) then stand in."""
         win = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
-        if not win and self.samples:                       # short run: nearest samples
+        window = "timed region"
+        if not win and run is not None:
+            win = [p for (t, p) in self.samples if run[0] <= t <= run[1]]
+            window = "whole GPU run (the timed region is shorter than the sampling period)"
+        if not win and self.samples:                       # nearest sample
             mid = 0.5 * (t0 + t1)
             win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            window = "nearest sample"
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
 
@@ -188,7 +203,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for p in win for i in range(4) if p[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": num(win[0][3]), "reasons": reasons, "samples": len(win)}
+                "sm_max_mhz": num(win[0][3]), "reasons": reasons, "samples": len(win),
+                "window": window}
 
 
 # ------------------------------------------------------------------ own arm
@@ -274,6 +290,8 @@ def run_own(args):
     except Exception:
         pass
     clocks = ClockSampler(gpu_id)
+    clocks.wait_first()
+    t_run0 = time.time()
 
     # warm-up (also settles clocks)
     for s in range(args.warmup):
@@ -318,7 +336,9 @@ def run_own(args):
     torch.cuda.synchronize(dev)
     stats_alone_ms = a0.elapsed_time(a1) / K
     barrier()
-    clk = clocks.summary(t_wall0, t_wall2)
+    # ---- each call of the step on its own
+    n_call = max(50, min(K, 500))
+    per_call = time_per_call(sv, torch, copies, x, stream, sh, dev, n_call, world, max_over_ranks)
 
     # outputs of the last step, for tau
     s_acc = out["s_acc"].cpu().numpy()
@@ -376,6 +396,18 @@ def run_own(args):
     f1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+    # the box's own pinned host-to-device rate for the same input set, one
+    # cudaMemcpyAsync per tensor on the copy stream, for reading e2e against
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nrep = 5
+    with torch.cuda.stream(copy_stream):
+        h0.record(copy_stream)
+        for _ in range(nrep):
+            for k, v in host.items():
+                stages[0][k].copy_(v, non_blocking=True)
+        h1.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    h2d_ref_gbs = nrep * bi / (h0.elapsed_time(h1) * 1e-3) / 1e9
     # ---- next-step paths, timed on their own (not part of the step above)
     nx = max(50, min(K, 500))
     extra = {"topk_k4": time_topk(sv, torch, copies, x, stream, sh, nx, max_over_ranks, world, dev),
@@ -386,12 +418,23 @@ def run_own(args):
              "cosine_b64": time_cosine(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev,
                                        rank),
              "tree_b32": time_tree(sv, torch, W, stream, sh, nx, max_over_ranks, world, dev, rank)}
+    # ---- the other chain workloads, sample and greedy calls on their own
+    configs = {}
+    if not args.no_configs:
+        for name in ("chain-small", "chain-b8", "chain-b256"):
+            if name != args.workload:
+                configs[name] = time_config(sv, torch, W, name, stream, sh, dev, nx, world,
+                                            max_over_ranks, rank)
+    t_run1 = time.time()
+    clk = clocks.summary(t_wall0, t_wall2, run=(t_run0, t_run1))
     clocks.stop()
 
     # ---- CPU baseline: the fp64 oracle on host cores (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_timing(x, ttok, tpar, budget_s=args.cpu_budget)
+        one = oracle_timing(x, ttok, tpar, budget_s=0.5 * args.cpu_budget, threads=1)
+        cpu["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
 
     if rank == 0:
         peak, peak_src = measured_peaks()
@@ -416,7 +459,9 @@ def run_own(args):
                 "workload": args.workload,
                 "B": B, "gamma": g, "V": V, "logits": x.dtype, "temperature": x.T,
                 "step": "spec_verify_sample + spec_verify_greedy + spec_verify_tree_greedy "
-                        "(chain-shaped tree), each on its own rotating input copy",
+                        "(chain-shaped tree), each on its own rotating input copy; value counts "
+                        "the rows of all three modes, 3 B (gamma+1) per step (per_call has each "
+                        "mode on its own)",
                 "l2": f"{rot} rotating input copies of {acct['bytes_stats'] / 1e6:.1f} MB "
                       f"({rot * acct['bytes_stats'] / 129e6:.1f}x the 129 MB L2 in all)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -451,15 +496,157 @@ def run_own(args):
                 "steps": Ke,
                 "pipelining": "double-buffered: step i+1's host-to-device copy runs on a copy "
                               "stream while step i's kernels run",
+                "h2d_reference_gbs": h2d_ref_gbs,
+                "h2d_reference": "the same pinned input set copied alone, one cudaMemcpyAsync "
+                                 "per tensor, 5 repetitions between CUDA events",
+                "h2d_gbs_implied": bi * Ke / (e2e_ms * 1e-3) / 1e9,
             },
-            "gpu_launches": 7 * K,
+            "gpu_launches": (sample_launches(x) + 4) * K,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "per_call": per_call,
+            "configs": configs,
             "extra_paths": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_loop(torch, stream, dev, call, n, warm=3):
+    """Mean milliseconds per call of n back-to-back calls call(0..n-1) between
+    two CUDA events on the launching stream (no event between the calls),
+    after `warm` untimed calls."""
+    for s in range(warm):
+        call(s)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(n):
+        call(s)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / n
+
+
+def call_entry(ms, rows, nbytes, peak, peak_src, launches, roofline=True):
+    d = {"us_per_call": 1e3 * ms, "rows_per_s": rows / (ms * 1e-3),
+         "algorithmic_bytes_per_call": nbytes, "gpu_launches_per_call": launches}
+    if roofline:
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        d["hbm"] = {"achieved_gbs": gbs, "peak_gbs": peak, "peak_source": peak_src,
+                    "frac": gbs / peak, "frac_of_8tbs_nominal": gbs / 8000.0}
+    else:
+        d["hbm"] = None
+        d["note"] = "latency-bound (tens of KB per call): no roofline claim"
+    return d
+
+
+def sample_launches(x):
+    """Kernel launches of one spec_verify_sample call: the fused persistent
+    kernel for rows of a multiple of 16 bytes, else stream + decide + final."""
+    elt = 2 if x.dtype == "bf16" else 4
+    return 3
+
+
+def time_per_call(sv, torch, copies, x, stream, sh, dev, n, world, max_over_ranks):
+    """Each of the step's three calls on its own: n back-to-back calls over the
+    rotating input copies, CUDA events on the launching stream."""
+    B, g, V = x.B, x.gamma, x.V
+    dcode = sv.SPEC_DTYPE_BF16 if x.dtype == "bf16" else sv.SPEC_DTYPE_F32
+    elt = 2 if x.dtype == "bf16" else 4
+    rot = len(copies)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get(B, g + 1, V)
+    tok = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    nodes = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    P = lambda t: t.data_ptr()  # noqa: E731
+
+    def check(st, what):
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, what)
+
+    def sample(s):
+        c = copies[s % rot]
+        check(sv.spec_verify_sample(P(c["zt"]), P(c["zd"]), dcode, P(c["x"]), P(c["u"]), x.T, B,
+                                    g, V, P(tok), P(acc), None, wp, wb, sh), "sample")
+
+    def greedy(s):
+        c = copies[s % rot]
+        check(sv.spec_verify_greedy(P(c["zt"]), dcode, P(c["x"]), B, g, V, P(tok), P(acc), wp, wb,
+                                    sh), "greedy")
+
+    def tree(s):
+        c = copies[s % rot]
+        check(sv.spec_verify_tree_greedy(P(c["zt"]), dcode, P(c["tt"]), P(c["tp"]), B, g + 1, V,
+                                         P(nodes), P(tok), P(acc), wp, wb, sh), "tree")
+
+    peak, src = measured_peaks()
+    rows = world * B * (g + 1)
+    b_s = B * (2 * g + 1) * V * elt
+    b_g = B * (g + 1) * V * elt
+    out = {}
+    for name, fn, nb, launches in (("sample", sample, b_s, sample_launches(x)),
+                                   ("greedy", greedy, b_g, 2), ("tree", tree, b_g, 2)):
+        ms = max_over_ranks(time_loop(torch, stream, dev, fn, n), world, dev)
+        out[name] = call_entry(ms, rows, world * nb, peak, src, launches)
+    out["how"] = (f"{n} back-to-back calls of each entry point over {rot} rotating input copies, "
+                  "CUDA events on the launching stream; rows = B (gamma+1) per call")
+    return out
+
+
+def time_config(sv, torch, W, name, stream, sh, dev, n, world, max_over_ranks, rank):
+    """spec_verify_sample and spec_verify_greedy on another chain workload, each
+    timed on its own over rotating input copies (together more than 4x the
+    129 MB L2 where the copies fit in a few GB; chain-small's 36 KB stay in L2)."""
+    x = W.make_chain(name, seed=rank_seed(W.WORKLOADS[name].seed, rank))
+    B, g, V = x.B, x.gamma, x.V
+    tdt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    dcode = sv.SPEC_DTYPE_BF16 if x.dtype == "bf16" else sv.SPEC_DTYPE_F32
+    elt = 2 if x.dtype == "bf16" else 4
+    b_s = B * (2 * g + 1) * V * elt
+    b_g = B * (g + 1) * V * elt
+    rot = max(1, min(8, -(-4 * 129_000_000 // b_s))) if b_s > 1_000_000 else 1
+    zt = torch.from_numpy(x.target).to(tdt)
+    zd = torch.from_numpy(x.draft).to(tdt)
+    copies = [{"zt": zt.to(dev), "zd": zd.to(dev)} for _ in range(rot)]
+    xd = torch.from_numpy(x.draft_tokens).to(dev)
+    ud = torch.from_numpy(x.uniforms).to(dev)
+    tok = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.Workspace(dev)
+    wp, wb = ws.get(B, g, V)
+
+    def check(st, what):
+        if st != sv.SPEC_OK:
+            raise sv.SpecVerifyError(st, what)
+
+    def sample(s):
+        c = copies[s % rot]
+        check(sv.spec_verify_sample(c["zt"].data_ptr(), c["zd"].data_ptr(), dcode, xd.data_ptr(),
+                                    ud.data_ptr(), x.T, B, g, V, tok.data_ptr(), acc.data_ptr(),
+                                    None, wp, wb, sh), "sample")
+
+    def greedy(s):
+        c = copies[s % rot]
+        check(sv.spec_verify_greedy(c["zt"].data_ptr(), dcode, xd.data_ptr(), B, g, V,
+                                    tok.data_ptr(), acc.data_ptr(), wp, wb, sh), "greedy")
+
+    peak, src = measured_peaks()
+    big = b_s > 1_000_000
+    rows = world * B * (g + 1)
+    res = {"B": B, "gamma": g, "V": V, "logits": x.dtype, "temperature": x.T}
+    for mode, fn, nb, launches in (("sample", sample, b_s, sample_launches(x)),
+                                   ("greedy", greedy, b_g, 2)):
+        ms = max_over_ranks(time_loop(torch, stream, dev, fn, n), world, dev)
+        res[mode] = call_entry(ms, rows, world * nb, peak, src, launches, roofline=big)
+    res["l2"] = (f"{rot} rotating input copies of {b_s / 1e6:.1f} MB" if big else
+                 "one input copy (L2-resident: the workload is smaller than the L2)")
+    res["calls"] = n
+    del copies
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_topk(sv, torch, copies, x, stream, sh, steps, max_over_ranks, world, dev):
@@ -701,8 +888,10 @@ def oracle_slice(x, n, ttok, tpar, nthreads):
     return 3 * n * (x.gamma + 1)
 
 
-def oracle_timing(x, ttok, tpar, budget_s=10.0):
-    cores = os.cpu_count() or 1
+def oracle_timing(x, ttok, tpar, budget_s=10.0, threads=None):
+    """The oracle, as it stands, over the first n sequences of the batch,
+    repeated until budget_s of wall time: one sequence per thread."""
+    cores = threads or os.cpu_count() or 1
     n = min(x.B, max(1, cores))
     rows, t = 0, 0.0
     reps = 0
@@ -713,7 +902,7 @@ def oracle_timing(x, ttok, tpar, budget_s=10.0):
         reps += 1
     return {"value": rows / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{reps} x the first {n} sequences of the batch (sample + greedy + tree), "
-                      f"{t:.1f} s wall on {cores} threads"}
+                      f"{t:.1f} s wall on {cores} thread{'s' if cores > 1 else ''}"}
 
 
 # ------------------------------------------------------------ reference arm
@@ -770,6 +959,8 @@ def main(argv=None):
                     choices=["chain-small", "chain-b8", "chain-b64", "chain-b256"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other chain workloads (chain-small, chain-b8, chain-b256)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--rotate", type=int, default=ROTATE,
                     help="input copies the calls rotate over (1 keeps profiler captures small)")
