@@ -543,9 +543,8 @@ def call_entry(ms, rows, nbytes, peak, peak_src, launches, roofline=True):
 
 
 def sample_launches(x):
-    """Kernel launches of one spec_verify_sample call: the fused persistent
-    kernel for rows of a multiple of 16 bytes, else stream + decide + final."""
-    elt = 2 if x.dtype == "bf16" else 4
+    """Kernel launches of one spec_verify_sample call: the statistics stream,
+    the decisions and the final pass (with the search)."""
     return 3
 
 

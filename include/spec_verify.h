@@ -329,6 +329,23 @@ spec_status_t spec_verify_sample_noalloc(const void* target_logits, const void* 
                                          cudaStream_t stream);
 
 /*
+ * Test hook for the kernels' bounded waits (the source pages have no
+ * counterpart).  Every wait of the streaming kernels on a shared-memory
+ * barrier of their bulk-copy ring gives up after a number of polls (seconds of
+ * wall time by default: spec_verify_default_wait_limit()), sets
+ * SPEC_DEVERR_TIMEOUT in the workspace error word and lets the kernel return
+ * instead of hanging.  spec_verify_set_wait_limit sets that number for every
+ * launch made afterwards in the process, from any thread; 0 makes such waits
+ * give up without polling, so a test can drive the timeout path without
+ * breaking a kernel.  Results of a call whose wait gave up are not valid; the
+ * workspace stays usable for later calls.  A kernel's final wait for its own
+ * bulk copies in flight always keeps the default bound.  Host only; set it
+ * back to the default after the test.
+ */
+void spec_verify_set_wait_limit(uint32_t polls);
+uint32_t spec_verify_default_wait_limit(void);
+
+/*
  * Synchronises `stream`, returns the accumulated SPEC_DEVERR_* bits of the
  * workspace in *code and clears them.  SPEC_OK when the read succeeded (code
  * may still be nonzero).

@@ -67,6 +67,8 @@ SIGNATURES = {
     "spec_cosine_topk": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P], _I),
     "spec_verify_read_error": ([_P, _P, _P], _I),
     "spec_verify_status_string": ([_I], ctypes.c_char_p),
+    "spec_verify_set_wait_limit": ([ctypes.c_uint32], None),
+    "spec_verify_default_wait_limit": ([], ctypes.c_uint32),
 }
 
 
@@ -211,6 +213,14 @@ def spec_verify_read_error(ws: int, stream: int = 0):
     code = ctypes.c_int32(0)
     st = load_library().spec_verify_read_error(ws, stream, ctypes.addressof(code))
     return st, code.value
+
+
+def spec_verify_set_wait_limit(polls: int) -> None:
+    load_library().spec_verify_set_wait_limit(polls)
+
+
+def spec_verify_default_wait_limit() -> int:
+    return load_library().spec_verify_default_wait_limit()
 
 
 def spec_verify_status_string(status: int) -> str:

@@ -4,6 +4,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "sv_internal.h"
 
 namespace sv {
@@ -23,6 +25,10 @@ cudaError_t device_info(DeviceInfo* out) {
         return cudaDeviceGetAttribute(v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     });
 }
+
+static std::atomic<uint32_t> g_wait_limit{kWaitLimitDefault};
+
+uint32_t ring_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -238,6 +244,12 @@ spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32
     *code = v;
     return SPEC_OK;
 }
+
+void spec_verify_set_wait_limit(uint32_t polls) {
+    g_wait_limit.store(polls, std::memory_order_relaxed);
+}
+
+uint32_t spec_verify_default_wait_limit(void) { return kWaitLimitDefault; }
 
 const char* spec_verify_status_string(spec_status_t status) {
     switch (status) {

@@ -44,6 +44,7 @@ static VerifyArgs argmax_args(const void* zt, int elt, int B, int rows, int V, v
     const WsLayout L = ws_layout(B, rows, V);
     char* w = static_cast<char*>(ws);
     VerifyArgs a = {};
+    a.wait_limit = ring_wait_limit();
     a.zt = static_cast<const char*>(zt);
     a.rows_per_seq = rows;
     a.V = V;

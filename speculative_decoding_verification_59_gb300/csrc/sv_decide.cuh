@@ -82,6 +82,10 @@ struct VerifyArgs {
     int* lz_next_list;
     int* lz_next_count;
     int* lz_zero;
+    // Polls of a bounded wait on a ring barrier before it reports
+    // SPEC_DEVERR_TIMEOUT (kWaitLimit unless a test lowers it); the wait for a
+    // CTA's own copies in flight before it exits always takes kWaitLimit.
+    uint32_t wait_limit;
 };
 
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

@@ -118,6 +118,12 @@ inline cudaError_t device_once(DeviceSlots& slots, int* out, F setup) {
     return cudaSuccess;
 }
 
+// Polls of a bounded barrier wait inside the ring kernels before it gives up
+// (seconds of wall time), and the value for launches made from now on: this
+// default, unless spec_verify_set_wait_limit changed it.
+constexpr uint32_t kWaitLimitDefault = 1u << 24;
+uint32_t ring_wait_limit();
+
 // Upper ends of the lazy pass's position groups (host only; ends holds
 // kLazyGroups entries); returns their count.
 int lazy_groups_host(int B, int gamma, size_t rowbytes, int* ends);

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
             for (unsigned c = c0; c < c1; ++c, ++issued) {
                 const int st = (int)(issued % kStages);
                 const unsigned use = issued / kStages;
-                if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u)) { ok = false; break; }
+                if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u, a.wait_limit)) { ok = false; break; }
                 const unsigned rr = c / (unsigned)a.nseg;
                 const int seg = (int)(c - rr * (unsigned)a.nseg);
                 const size_t off = (size_t)seg * kStageBytes;
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     bool ok = true;
     for (unsigned c = c0; c < c1; ++c, ++it) {
         const int st = (int)(it % kStages);
-        if (ok && !wait_bounded(&full[st], (it / kStages) & 1u)) ok = false;
+        if (ok && !wait_bounded(&full[st], (it / kStages) & 1u, a.wait_limit)) ok = false;
         const unsigned rr = c / (unsigned)a.nseg;
         const int seg = (int)(c - rr * (unsigned)a.nseg);
         const unsigned pr = rows.part_row<MODE>(a, rr);

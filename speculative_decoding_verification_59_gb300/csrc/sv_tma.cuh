@@ -4,15 +4,18 @@
 // the barrier's phase parity.
 //
 // Every wait is bounded: wait_bounded() gives up after kWaitLimit polls
-// (seconds of wall time) and reports failure, so a kernel can raise
-// SPEC_DEVERR_TIMEOUT and leave instead of hanging.
+// (seconds of wall time; fewer when a test lowers the launch's limit) and
+// reports failure, so a kernel can raise SPEC_DEVERR_TIMEOUT and leave
+// instead of hanging.
 #pragma once
 
 #include <stdint.h>
 
+#include "sv_internal.h"
+
 namespace sv {
 
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = kWaitLimitDefault;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -51,9 +54,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Polls the barrier until the phase with the given parity completes; false
-// after kWaitLimit polls.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+// after `limit` polls (none for limit 0).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

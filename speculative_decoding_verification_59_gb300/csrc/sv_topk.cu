@@ -111,6 +111,7 @@ cudaError_t launch_topk(const void* logits, spec_dtype_t dt, int rows, int V, in
     const int elt = elt_size(dt);
     char* w = static_cast<char*>(ws);
     VerifyArgs a = {};
+    a.wait_limit = ring_wait_limit();
     a.zt = static_cast<const char*>(logits);
     a.rows_per_seq = 1;
     a.V = V;
