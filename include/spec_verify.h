@@ -133,9 +133,10 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
  * most positions 0..2k+1), all 2 gamma + 1 rows when every draft is
  * accepted.  A group runs on to the end (at most 128 positions) when the
  * rows after it, for all B sequences, hold fewer than 96 MB: a pass then
- * costs more than it can save.  The environment variable
- * SPEC_VERIFY_LAZY_SPLIT_BYTES overrides that figure (0: split at every
- * boundary); the outputs do not depend on it.  out_logprobs (nullable)
+ * costs more than it can save.  spec_verify_set_lazy_split_bytes, or the
+ * environment variable SPEC_VERIFY_LAZY_SPLIT_BYTES read once at the first
+ * lazy call or groups query of the process, overrides that figure (0: split
+ * at every boundary); the outputs do not depend on it.  out_logprobs (nullable)
  * holds the log-probabilities of positions 0..min(k, gamma - 1); later
  * positions, and every position of a bad sequence, are NaN.  Rows whose
  * byte length is not a multiple of 16 take the full pass (every row read)
@@ -157,12 +158,22 @@ spec_status_t spec_verify_sample_lazy(const void* target_logits, const void* dra
  * covers positions ends[g-1] .. ends[g]-1, from 0; the last end is gamma + 1)
  * and returns count, at most 8.  The sizes double from 2 -- [0,2), [2,6),
  * [6,14), ... -- and a group runs on to the end (at most 128 positions) when
- * the rows after it, for all B sequences, hold fewer than 96 MB (or
- * SPEC_VERIFY_LAZY_SPLIT_BYTES when that variable is set).  Host only, no CUDA
+ * the rows after it, for all B sequences, hold fewer than 96 MB (or the
+ * figure set as described for spec_verify_sample_lazy).  Host only, no CUDA
  * call; returns 0 for invalid arguments (B < 1, gamma outside 0..256, V < 1,
- * an unknown dtype, ends NULL).  ends must hold 8 entries.
+ * an unknown dtype, ends NULL).  ends must hold 8 entries.  The groups of a
+ * lazy call are those this function returns with the same figure in force.
  */
 int spec_verify_lazy_groups(int B, int gamma, int V, spec_dtype_t dtype, int32_t* ends);
+
+/*
+ * Sets the figure of spec_verify_sample_lazy's group rule: a group runs on to
+ * the end when the rows after it hold fewer than `bytes` (0: split at every
+ * boundary; negative: back to the built-in 96 MB).  Process-wide, for calls
+ * and queries made afterwards from any thread; it replaces the value of
+ * SPEC_VERIFY_LAZY_SPLIT_BYTES.  Host only.
+ */
+void spec_verify_set_lazy_split_bytes(double bytes);
 
 /*
  * The two halves of spec_verify_sample, for callers that want to overlap or
@@ -314,7 +325,9 @@ spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype
  * The first call on each device, made while that device is current, looks up
  * the array's device address (cudaGetSymbolAddress, which may also load the
  * library's kernels onto that device); make that first call before any stream
- * capture.  Every call on a device shares the one array, so calls whose work
+ * capture.  The address is kept for the life of the process: after
+ * cudaDeviceReset (or any other reset of the device's primary context) in the
+ * same process, this entry point must not be called again on that device.  Every call on a device shares the one array, so calls whose work
  * overlaps on the GPU (different streams without ordering, or host threads
  * racing on one device) race on it and give undefined results; order them.
  * Bad input is reported per sequence (num_accepted = -1, tokens -1) only: the

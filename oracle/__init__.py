@@ -54,8 +54,6 @@ def _load():
             lib.oracle_topk_exclude.restype = I
             lib.oracle_ngram_retrieve.argtypes = [P, P, I, I, I, I, I, P, P, P, I]
             lib.oracle_ngram_retrieve.restype = I
-            lib.oracle_softmax_row.argtypes = [P, I, ctypes.c_double, P]
-            lib.oracle_softmax_row.restype = I
             _lib = lib
     return _lib
 
@@ -197,12 +195,3 @@ def cosine_topk(hidden, query, delta, positions=None):
         pos = np.where(idx >= 0, np.take_along_axis(P, np.maximum(idx, 0), axis=1), -1)
     return {"idx": idx, "pos": pos.astype(np.int32), "score": sc, "scores": scores}
 
-
-def softmax_row(z, T):
-    lib = _load()
-    z = _f32(z)
-    out = np.empty(z.shape[0], np.float64)
-    rc = lib.oracle_softmax_row(_ptr(z), z.shape[0], float(T), _ptr(out))
-    if rc != 0:
-        raise ValueError("oracle_softmax_row: row has no distribution (rc=%d)" % rc)
-    return out

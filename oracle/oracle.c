@@ -57,14 +57,6 @@ static double prob(const float* z, rowstat_t st, double T, int j) {
     return exp(log_prob(z, st, T, j));
 }
 
-int oracle_softmax_row(const float* z, int V, double T, double* out_p) {
-    if (!z || !out_p || V <= 0 || !(T > 0.0) || !isfinite(T)) return -1;
-    rowstat_t st = row_stats(z, V, T);
-    if (st.m == -INFINITY) return 1;
-    for (int j = 0; j < V; ++j) out_p[j] = prob(z, st, T, j);
-    return 0;
-}
-
 /* ---- stochastic verification of one chain ------------------------------ */
 static void fill_bad(int32_t* tok, int n, int32_t* acc) {
     for (int i = 0; i < n; ++i) tok[i] = -1;

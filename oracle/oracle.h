@@ -119,9 +119,6 @@ int oracle_ngram_retrieve(const int32_t* tokens, const int32_t* lengths, int B, 
                           int L, int max_matches, int32_t* out_count, int32_t* out_matches,
                           int32_t* out_draft, int nthreads);
 
-/* Temperature softmax of one row, p_j = exp(z_j/T - lse), in double. */
-int oracle_softmax_row(const float* z, int V, double T, double* out_p);
-
 #ifdef __cplusplus
 }
 #endif

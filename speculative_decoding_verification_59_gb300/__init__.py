@@ -68,6 +68,7 @@ SIGNATURES = {
     "spec_verify_read_error": ([_P, _P, _P], _I),
     "spec_verify_status_string": ([_I], ctypes.c_char_p),
     "spec_verify_set_wait_limit": ([ctypes.c_uint32], None),
+    "spec_verify_set_lazy_split_bytes": ([ctypes.c_double], None),
     "spec_verify_default_wait_limit": ([], ctypes.c_uint32),
 }
 
@@ -213,6 +214,10 @@ def spec_verify_read_error(ws: int, stream: int = 0):
     code = ctypes.c_int32(0)
     st = load_library().spec_verify_read_error(ws, stream, ctypes.addressof(code))
     return st, code.value
+
+
+def spec_verify_set_lazy_split_bytes(nbytes: float) -> None:
+    load_library().spec_verify_set_lazy_split_bytes(float(nbytes))
 
 
 def spec_verify_set_wait_limit(polls: int) -> None:

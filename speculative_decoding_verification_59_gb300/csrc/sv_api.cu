@@ -30,7 +30,26 @@ static std::atomic<uint32_t> g_wait_limit{kWaitLimitDefault};
 
 uint32_t ring_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
-static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static bool aligned(const void* p, size_t a) { return is_aligned(p, a); }
+
+spec_status_t check_sample_args(const void* target_logits, const void* draft_logits,
+                                spec_dtype_t dtype, const int32_t* draft_tokens,
+                                const float* uniforms, float temperature, int B, int gamma, int V,
+                                const int32_t* out_tokens, const int32_t* out_num_accepted,
+                                bool finish) {
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 0 || gamma > kMaxGammaApi || V <= 0) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature >= kMinTemperature) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || (gamma > 0 && !draft_logits)) return SPEC_ERR_INVALID_ARG;
+    if (finish && (!uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16) || (gamma > 0 && !aligned(draft_logits, 16)))
+        return SPEC_ERR_MISALIGNED;
+    if (finish && !sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
 
 static spec_status_t check_ws(void* ws, size_t bytes, int B, int g, int V) {
     if (!ws) return SPEC_ERR_INVALID_ARG;
@@ -64,19 +83,13 @@ static spec_status_t sample_common(const void* target_logits, const void* draft_
                                    int V, int32_t* out_tokens, int32_t* out_num_accepted,
                                    float* out_logprobs, void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream, int parts) {
-    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || gamma < 0 || gamma > kMaxGammaApi || V <= 0) return SPEC_ERR_INVALID_ARG;
-    if (!(temperature >= kMinTemperature) || !isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
-    if (B == 0) return SPEC_OK;
-    if (!target_logits || (gamma > 0 && !draft_logits)) return SPEC_ERR_INVALID_ARG;
     const bool finish = (parts & (kSampleFinish | kSampleLazy)) != 0;
-    if (finish && (!uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)))
-        return SPEC_ERR_INVALID_ARG;
-    if (!aligned(target_logits, 16) || (gamma > 0 && !aligned(draft_logits, 16)))
-        return SPEC_ERR_MISALIGNED;
-    spec_status_t s = check_ws(workspace, workspace_bytes, B, gamma, V);
+    spec_status_t s = check_sample_args(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                                        temperature, B, gamma, V, out_tokens, out_num_accepted,
+                                        finish);
+    if (s != SPEC_OK || B == 0) return s;
+    s = check_ws(workspace, workspace_bytes, B, gamma, V);
     if (s != SPEC_OK) return s;
-    if (finish && !sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
     return to_status(launch_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                                    temperature, B, gamma, V, out_tokens, out_num_accepted,
                                    out_logprobs, workspace, stream, parts));
@@ -244,6 +257,8 @@ spec_status_t spec_verify_read_error(void* workspace, cudaStream_t stream, int32
     *code = v;
     return SPEC_OK;
 }
+
+void spec_verify_set_lazy_split_bytes(double bytes) { set_lazy_split_bytes(bytes); }
 
 void spec_verify_set_wait_limit(uint32_t polls) {
     g_wait_limit.store(polls, std::memory_order_relaxed);

@@ -127,6 +127,21 @@ uint32_t ring_wait_limit();
 // Upper ends of the lazy pass's position groups (host only; ends holds
 // kLazyGroups entries); returns their count.
 int lazy_groups_host(int B, int gamma, size_t rowbytes, int* ends);
+// Sets the bytes after a group boundary that make the lazy pass split there
+// (negative: the built-in figure).
+void set_lazy_split_bytes(double bytes);
+
+// Host-side checks of a sampling call's arguments that do not involve the
+// workspace (spec_verify_sample and its variants, spec_verify_sample_noalloc):
+// SPEC_OK, or the status to return before anything is launched.  `finish`:
+// the call takes decisions (draft tokens, uniforms and outputs required).
+// B = 0 passes; the caller returns SPEC_OK without launching.
+spec_status_t check_sample_args(const void* target_logits, const void* draft_logits,
+                                spec_dtype_t dtype, const int32_t* draft_tokens,
+                                const float* uniforms, float temperature, int B, int gamma, int V,
+                                const int32_t* out_tokens, const int32_t* out_num_accepted,
+                                bool finish);
+bool is_aligned(const void* p, size_t a);
 
 // ---- launchers (return the first CUDA error) ------------------------------
 // parts: kSampleStats (streaming row statistics), kSampleFinish (the accept

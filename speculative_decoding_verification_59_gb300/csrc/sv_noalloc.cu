@@ -58,18 +58,13 @@ extern "C" spec_status_t spec_verify_sample_noalloc(
     const int32_t* draft_tokens, const float* uniforms, float temperature, int B, int gamma, int V,
     int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprobs, cudaStream_t stream) {
     using namespace sv;
-    // Same argument rules as spec_verify_sample, checked on the host first.
-    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || gamma < 0 || gamma > 256 || V <= 0) return SPEC_ERR_INVALID_ARG;
-    if (!(temperature >= 1e-20f) || !(temperature < __builtin_huge_valf())) return SPEC_ERR_INVALID_ARG;
-    if (B == 0) return SPEC_OK;
-    if (!target_logits || !uniforms || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
-    if (gamma > 0 && (!draft_logits || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(target_logits) % 16) != 0 ||
-        (gamma > 0 && (reinterpret_cast<uintptr_t>(draft_logits) % 16) != 0))
-        return SPEC_ERR_MISALIGNED;
+    // The argument rules of spec_verify_sample (the same check), then the size
+    // of the fixed scratch.
+    const spec_status_t s = check_sample_args(target_logits, draft_logits, dtype, draft_tokens,
+                                              uniforms, temperature, B, gamma, V, out_tokens,
+                                              out_num_accepted, true);
+    if (s != SPEC_OK || B == 0) return s;
     if (ws_layout(B, gamma, V).total > kNoAllocScratchBytes) return SPEC_ERR_EXCEEDS_STATIC_SCRATCH;
-    if (!sample_supported_vocab(V)) return SPEC_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
     // Every region the kernels read is written earlier in the same call, so

@@ -36,6 +36,8 @@
 // puts CDF boundaries ~1e-7 apart.
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "sv_final.cuh"
 
 namespace sv {
@@ -236,16 +238,38 @@ __global__ void lazy_mask_logprobs_kernel(const VerifyArgs a) {
 // skip more HBM time than that; with half of them stopping, when the rows
 // after the boundary (for every sequence) hold at least 2 x 7 us x 6.7 TB/s,
 // about 96 MB.  Below that the group runs on to the end.  The environment
-// variable SPEC_VERIFY_LAZY_SPLIT_BYTES overrides the figure (0: always
-// split); outputs do not depend on it.
+// variable SPEC_VERIFY_LAZY_SPLIT_BYTES, read once per process, and
+// spec_verify_set_lazy_split_bytes override the figure (0: always split);
+// outputs do not depend on it.
 constexpr double kLazySplitBytes = 96.0 * (1 << 20);
 
-static double lazy_split_bytes() {
+// The initial figure: the environment variable, read once per process (at the
+// first lazy call or groups query), else kLazySplitBytes.
+static double lazy_split_from_env() {
     const char* e = getenv("SPEC_VERIFY_LAZY_SPLIT_BYTES");
     if (!e || !*e) return kLazySplitBytes;
     char* end = nullptr;
     const double v = strtod(e, &end);
     return (end && *end == '\0' && v >= 0.0) ? v : kLazySplitBytes;
+}
+
+// The current figure; spec_verify_set_lazy_split_bytes changes it.  A negative
+// value in the slot means "not yet read".
+static std::atomic<double> g_lazy_split{-1.0};
+
+static double lazy_split_bytes() {
+    double v = g_lazy_split.load(std::memory_order_relaxed);
+    if (v < 0.0) {
+        static const double from_env = lazy_split_from_env();   // thread-safe, once
+        double expect = v;
+        g_lazy_split.compare_exchange_strong(expect, from_env, std::memory_order_relaxed);
+        v = g_lazy_split.load(std::memory_order_relaxed);
+    }
+    return v;
+}
+
+void set_lazy_split_bytes(double bytes) {
+    g_lazy_split.store(bytes >= 0.0 ? bytes : kLazySplitBytes, std::memory_order_relaxed);
 }
 
 // Upper ends of the lazy position groups: sizes doubling from 2, a group

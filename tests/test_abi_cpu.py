@@ -37,22 +37,30 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in sv.SIGNATURES, n
 
 
-def test_lazy_groups_schedule(lib, monkeypatch):
+@pytest.fixture
+def split_bytes():
+    """Sets the lazy pass's split figure for one test, restoring the built-in
+    one afterwards."""
+    yield sv.spec_verify_set_lazy_split_bytes
+    sv.spec_verify_set_lazy_split_bytes(-1.0)
+
+
+def test_lazy_groups_schedule(lib, split_bytes):
     """The lazy pass's position groups, from the host-only schedule call: the
     benchmark workloads' groups, the doubling schedule with every boundary
     taken, and its invariants for every gamma."""
-    monkeypatch.delenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", raising=False)
+    split_bytes(-1.0)
     bf16, f32 = sv.SPEC_DTYPE_BF16, sv.SPEC_DTYPE_F32
     assert sv.lazy_groups(64, 7, 151936, bf16) == [(0, 2), (2, 8)]        # 58 MB after [2, 6)
     assert sv.lazy_groups(8, 7, 151936, bf16) == [(0, 8)]                 # 32 MB after [0, 2)
     assert sv.lazy_groups(256, 4, 128256, f32) == [(0, 2), (2, 5)]
     assert sv.lazy_groups(1, 0, 1000, f32) == [(0, 1)]
-    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", "0")
+    split_bytes(0)
     assert sv.lazy_groups(1, 7, 1000, f32) == [(0, 2), (2, 6), (6, 8)]
     assert sv.lazy_groups(1, 256, 1000, f32) == [(0, 2), (2, 6), (6, 14), (14, 30), (30, 62),
                                                  (62, 126), (126, 254), (254, 257)]
-    for split in ("0", "100000000000"):
-        monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", split)
+    for split in (0, 1e11):
+        split_bytes(split)
         for gamma in range(0, 257):
             gr = sv.lazy_groups(3, gamma, 4096, bf16)
             assert gr[0][0] == 0 and gr[-1][1] == gamma + 1 and len(gr) <= 8

@@ -99,10 +99,13 @@ def test_lazy_identical_models_read_every_position(sv):
 
 
 @pytest.fixture
-def every_group(monkeypatch):
+def every_group(sv):
     """Split at every group boundary whatever the sizes (the library otherwise
-    merges the groups of small problems into one pass)."""
-    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", "0")
+    merges the groups of small problems into one pass); the built-in figure
+    is restored afterwards."""
+    sv.spec_verify_set_lazy_split_bytes(0)
+    yield
+    sv.spec_verify_set_lazy_split_bytes(-1.0)
 
 
 @pytest.mark.parametrize("gamma", [1, 2, 5, 6, 13, 14, 30])
@@ -164,12 +167,15 @@ def test_lazy_empty_row_in_a_later_group(sv, every_group):
     assert ws.read_error() & sv.SPEC_DEVERR_EMPTY_ROW
 
 
-@pytest.mark.parametrize("split", ["0", "100000000000"])
-def test_lazy_schedule_does_not_change_results(sv, monkeypatch, split):
+@pytest.mark.parametrize("split", [0, 1e11])
+def test_lazy_schedule_does_not_change_results(sv, split):
     """chain-b64 at full size with every boundary taken (three groups) and with
     none (one group): the same tokens, counts and log-probabilities as the
     full pass either way."""
-    monkeypatch.setenv("SPEC_VERIFY_LAZY_SPLIT_BYTES", split)
-    x = W.make_chain("chain-b64")
-    full, lazy = both(sv, x)
-    check_same(full, lazy)
+    sv.spec_verify_set_lazy_split_bytes(split)
+    try:
+        x = W.make_chain("chain-b64")
+        full, lazy = both(sv, x)
+        check_same(full, lazy)
+    finally:
+        sv.spec_verify_set_lazy_split_bytes(-1.0)

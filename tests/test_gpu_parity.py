@@ -189,6 +189,29 @@ def test_sample_bad_inputs_flagged(sv):
     ws.read_error()
 
 
+@pytest.mark.parametrize("dtype,V", [("f32", 2), ("bf16", 16)])
+def test_sample_residual_without_mass(sv, dtype, V):
+    """Target [0, -58], draft [0, -46] on the first two tokens (the rest
+    masked): the drafted token 1 is rejected and the residual's exact mass
+    lies wholly on token 0, below what the working precision resolves.  Token
+    0 must come out, no error is flagged, and the oracle agrees."""
+    zt = np.full((1, 2, V), -np.inf, np.float32)
+    zd = np.full((1, 1, V), -np.inf, np.float32)
+    zt[0, 0, :2] = [0.0, -58.0]
+    zt[0, 1, :2] = [0.0, -3.0]
+    zd[0, 0, :2] = [0.0, -46.0]
+    x = W.make_chain("chain-small", B=1, gamma=1, V=V)
+    x.target, x.draft, x.dtype, x.T = zt, zd, dtype, 1.0
+    x.draft_tokens = np.array([[1]], np.int32)
+    ws = sv.Workspace()
+    for u_final in (0.0, 0.3, 0.999999):
+        x.uniforms = np.array([[0.5, u_final]], np.float32)
+        tok, acc, _ = run_sample(sv, x, ws=ws)
+        assert acc.tolist() == [0] and tok.tolist() == [[0, -1]]
+        check_sample(sv, x, ws=ws)
+    assert ws.read_error() == 0
+
+
 def test_masked_tokens(sv):
     """-inf logits are masked tokens: never chosen, and q(x) = 0 accepts."""
     x = W.make_chain("chain-b256", B=6, gamma=3, V=2048)
@@ -223,9 +246,13 @@ def test_repeat_calls_are_bitwise_identical(sv):
 # ------------------------------------------------------ full-size workloads
 @pytest.mark.parametrize("name", ["chain-small", "chain-b8", "chain-b64", "chain-b256"])
 def test_full_size_sample(sv, name):
+    """One call per workload at full size.  The rate itself is measured in
+    test_gpu_rate.py over many draws; a single call may show at most ten times
+    the count the rate bar allows on its rows, rounded down (0 for the three
+    smaller workloads, 1 for the 1280 rows of chain-b256)."""
     x = W.make_chain(name)
     res = check_sample(sv, x)
-    assert res["excused"] <= max(0, int(RATE_BAR * res["rows"])) or res["excused"] <= 1
+    assert res["excused"] <= int(10 * RATE_BAR * res["rows"]), res["events"]
 
 
 @pytest.mark.parametrize("name", ["chain-small", "chain-b8", "chain-b64", "chain-b256"])

@@ -117,3 +117,25 @@ def test_topk_workspace_reuse_and_repeat(sv):
         check(sv, z1, 4, exclusions(rng, z1, 4), "bf16", ws)
         check(sv, z2, 8, None, "f32", ws)
     assert ws.read_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topk_lanes_with_several_candidates(sv, dtype):
+    """Rows where some 16-byte vectors hold a cluster of 2 to 8 equal high
+    logits (one lane then marks several candidates in its chunk) and other
+    chunks of the same row hold only scattered singles: the chunks of one call
+    take the ballot count, the lane scan and, where more than 2K candidates
+    gather, the exact merge.  Bit-exact against the oracle, ties by index."""
+    rng = np.random.default_rng(5)
+    R, V, K = 24, 40000, 4
+    PV = 8 if dtype == "bf16" else 4
+    z = rng.standard_normal((R, V)).astype(np.float32)
+    for r in range(R):
+        for j in rng.choice(V, 6, replace=False):
+            z[r, j] = np.float32(6.0 + rng.random())
+        for _ in range(int(rng.integers(1, 4))):
+            v0 = int(rng.integers(0, V // PV)) * PV
+            n = int(rng.integers(2, PV + 1))
+            z[r, v0:v0 + n] = np.float32(6.5 if rng.random() < 0.5 else 7.5)
+    check(sv, z, K, exclusions(rng, z, K), dtype)
+    check(sv, z, K, None, dtype)

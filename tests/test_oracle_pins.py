@@ -515,6 +515,34 @@ def test_golden_tree(case):
     assert out["accepted"][0] == case["expect_accepted"]
 
 
+def residual_vanishing_case():
+    """Two tokens, T = 1: p = softmax([0, -58]) puts ~6.5e-26 on token 1,
+    q = softmax([0, -46]) ~1.1e-20.  Drafting token 1 gives r = p1/q1 ~ 6e-6,
+    so u0 = 0.5 rejects it; in exact arithmetic the residual max(0, p - q) is
+    (q1 - p1, 0): all of its mass sits on token 0, and the final token must be
+    0 whatever u_gamma is.  In double precision p0 and q0 both round to 1.0, so
+    the computed residual has no positive entry at all."""
+    zt = np.array([[[0.0, -58.0], [0.0, -3.0]]], np.float32)     # [B=1, gamma+1=2, V=2]
+    zd = np.array([[[0.0, -46.0]]], np.float32)                  # [B=1, gamma=1, V=2]
+    x = np.array([[1]], np.int32)
+    return zt, zd, x
+
+
+@pytest.mark.parametrize("u_final", [0.0, 0.3, 0.999999])
+def test_residual_without_double_mass_takes_token_zero(u_final):
+    """The oracle's fallback for a residual whose positive mass vanishes in
+    double precision (sample from p_k): here it must give token 0, the only
+    token the exact residual can produce."""
+    zt, zd, x = residual_vanishing_case()
+    p = softmax(zt[0, 0].astype(np.float64))
+    q = softmax(zd[0, 0].astype(np.float64))
+    assert p[1] / q[1] < 1e-5 and p[0] - q[0] == 0.0 and p[1] - q[1] < 0.0   # the case holds
+    u = np.array([[0.5, u_final]], np.float32)
+    out = oracle.verify_sample(zt, zd, x, u, 1.0)
+    assert out["accepted"].tolist() == [0]
+    assert out["tokens"].tolist() == [[0, -1]]
+
+
 def test_zero_mass_tokens_never_chosen_at_cdf_edges():
     """Inverse-CDF edge conventions: u = 0 picks the first token with positive
     mass (not a zero-mass token in front of it), and u = 1 (outside [0, 1),

@@ -85,3 +85,41 @@ def test_noalloc_rejects_problems_beyond_its_scratch(sv):
                                        V, fake, fake, None, None)
     assert st == sv.SPEC_ERR_EXCEEDS_STATIC_SCRATCH
     assert "scratch" in sv.spec_verify_status_string(st)
+
+
+def test_noalloc_bad_sequence_then_valid_call(sv):
+    """A draft token outside [0, V) marks only its own sequence (-1 count and
+    tokens); the shared array keeps the device error bits this entry point
+    never reads, and the next valid call on the same stream still equals
+    spec_verify_sample bit for bit."""
+    stream = torch.cuda.current_stream().cuda_stream
+    x = W.make_chain("chain-b64", B=6, V=20000)
+    x.draft_tokens = x.draft_tokens.copy()
+    x.draft_tokens[2, 3] = x.V
+    zt, zd, xt, u = _inputs(x)
+    tok, acc, lp = _outputs(x)
+    st = sv.spec_verify_sample_noalloc(zt.data_ptr(), zd.data_ptr(), _code(sv, x), xt.data_ptr(),
+                                       u.data_ptr(), x.T, x.B, x.gamma, x.V, tok.data_ptr(),
+                                       acc.data_ptr(), lp.data_ptr(), stream)
+    assert st == sv.SPEC_OK
+    torch.cuda.synchronize()
+    a = acc.cpu().numpy()
+    assert a[2] == -1 and (tok[2] == -1).all()
+    assert (np.delete(a, 2) >= 0).all()
+
+    y = W.make_chain("chain-b64", B=6, V=20000, seed=77)
+    zt, zd, xt, u = _inputs(y)
+    need = sv.spec_verify_workspace_size(y.B, y.gamma, y.V)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ref_tok, ref_acc, ref_lp = _outputs(y)
+    assert sv.spec_verify_sample(zt.data_ptr(), zd.data_ptr(), _code(sv, y), xt.data_ptr(),
+                                 u.data_ptr(), y.T, y.B, y.gamma, y.V, ref_tok.data_ptr(),
+                                 ref_acc.data_ptr(), ref_lp.data_ptr(), ws.data_ptr(), need,
+                                 stream) == sv.SPEC_OK
+    tok, acc, lp = _outputs(y)
+    assert sv.spec_verify_sample_noalloc(zt.data_ptr(), zd.data_ptr(), _code(sv, y),
+                                         xt.data_ptr(), u.data_ptr(), y.T, y.B, y.gamma, y.V,
+                                         tok.data_ptr(), acc.data_ptr(), lp.data_ptr(),
+                                         stream) == sv.SPEC_OK
+    torch.cuda.synchronize()
+    assert torch.equal(tok, ref_tok) and torch.equal(acc, ref_acc) and torch.equal(lp, ref_lp)
