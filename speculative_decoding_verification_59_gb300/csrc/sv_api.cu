@@ -30,6 +30,16 @@ static std::atomic<uint32_t> g_wait_limit{kWaitLimitDefault};
 
 uint32_t ring_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
+static std::atomic<uint64_t> g_launch_tag{0};
+uint64_t next_launch_tag() {
+    constexpr uint64_t mask = (1ull << kClaimTagBits) - 1;
+    uint64_t t;
+    do {
+        t = (g_launch_tag.fetch_add(1, std::memory_order_relaxed) + 1) & mask;
+    } while (t == 0);
+    return t;
+}
+
 bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 static bool aligned(const void* p, size_t a) { return is_aligned(p, a); }
 

@@ -86,6 +86,10 @@ struct VerifyArgs {
     // SPEC_DEVERR_TIMEOUT (kWaitLimit unless a test lowers it); the wait for a
     // CTA's own copies in flight before it exits always takes kWaitLimit.
     uint32_t wait_limit;
+    // Ring streams: the workspace's claim counter and this launch's tag,
+    // already shifted into place (tag << kClaimIdxBits); set by launch_stream.
+    unsigned long long* claim;
+    unsigned long long claim_tag;
 };
 
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

@@ -269,17 +269,30 @@ __device__ __forceinline__ void segment_sums(const VerifyArgs& a, const FinalRow
             f32x2 ea[NP], eb[NP];
             vec_exps<ELT, FAST>(qa[h], f.xa, k, a, ea);
             if (f.rej) vec_exps<ELT, FAST>(qb[h], f.xb, k, a, eb);
+            // A vector's NP terms per packed lane are summed plainly, then the
+            // sum enters the compensated running sum: each plain sum is off by
+            // at most (NP - 1) ulp of itself, independently from vector to
+            // vector, which leaves a segment total within ~u/8 of its value
+            // (u = 2^-24) -- far inside what the search needs -- for a
+            // quarter of the compensation work.
+            f32x2 sa = ea[0];
 #pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                ka.add(ea[i]);
-                if (f.rej) {
-                    kb.add(eb[i]);
+            for (int i = 1; i < NP; ++i) sa = f2_add(sa, ea[i]);
+            ka.add(sa);
+            if (f.rej) {
+                f32x2 sb = eb[0], sw = 0ull;
+#pragma unroll
+                for (int i = 1; i < NP; ++i) sb = f2_add(sb, eb[i]);
+                kb.add(sb);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
                     float t0, t1, b0, b1;
                     f2_unpack(f2_fma(nrt2, eb[i], ea[i]), t0, t1);
                     f2_unpack(eb[i], b0, b1);
-                    kw.add(f2_pack(fmaxf(t0, 0.f), fmaxf(t1, 0.f)));
+                    sw = f2_add(sw, f2_pack(fmaxf(t0, 0.f), fmaxf(t1, 0.f)));
                     d2 = f2_add(d2, f2_pack(t0 > 0.f ? b0 : 0.f, t1 > 0.f ? b1 : 0.f));
                 }
+                kw.add(sw);
             }
         }
     }
@@ -303,10 +316,11 @@ __device__ __forceinline__ void segment_sums_global(const VerifyArgs& a, const F
                                                     float rt, int lane) {
     FF za, zb, w;
     float dd;
+    const int j0 = sg * kSeg;
     auto ldA = [&](int j) { return load_vec<ELT, VEC>(f.ra, a.V, j); };
     auto ldB = [&](int j) { return load_vec<ELT, VEC>(f.rb, a.V, j); };
-    if (f.fast) segment_sums<ELT, true, 4>(a, f, sg * kSeg, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
-    else segment_sums<ELT, false, 1>(a, f, sg * kSeg, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
+    if (f.fast) segment_sums<ELT, true, 4>(a, f, j0, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
+    else segment_sums<ELT, false, 1>(a, f, j0, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
     if (lane == 0) {
         const size_t i = (size_t)b * a.C * kCW + sg;
         a.zsum[i] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
@@ -314,67 +328,57 @@ __device__ __forceinline__ void segment_sums_global(const VerifyArgs& a, const F
     }
 }
 
-// Inclusive scan of one float-float value per thread over the kCT-thread
-// group in thread order; *total receives the group total.  Deterministic: the
-// same inputs give the same bits in every group.
-__device__ __forceinline__ FF block_incl_scan_ff(FF v, FF* wtot, FF* total, int tid) {
+// Shared memory of a final-pass group.
+struct FinalSmem {
+    FF wv[kCW], wa[kCW], wb[kCW];   // per-warp totals: scanned sums, target and draft normalisers
+    float wd[kCW];                  // per-warp totals of the residual slopes
+    FF xs[kCT];                     // each thread's exclusive prefix (base of its segments)
+    FF P;                           // base of the owning segment (several segments per thread)
+    int sel, last, sel2, last2, seg;
+    int mine;                       // final-pass kernel: this CTA finished its sequence's last chunk
+};
+
+// Inclusive float-float and float prefixes of one value per thread over the
+// group, in thread order, from the per-warp totals in sm (written by each
+// warp's lane 31 before the group barrier): *excl and *incl tile the range
+// exactly -- thread t's incl and thread t+1's excl are the same bits -- and
+// the last thread's incl equals *tot.
+struct GroupPrefix {
+    FF excl, incl, tot;
+    float dexcl, dincl, dtot;
+};
+
+__device__ __forceinline__ GroupPrefix group_prefix(FF vin, float din, const FF* wv, const float* wd, int tid) {
     const int lane = tid & 31, warp = tid >> 5;
-    FF x = warp_incl_scan_ff(v);
-    if (lane == 31) wtot[warp] = x;
-    fin_sync();
-    if (warp == 0) {
-        FF y = lane < kCW ? wtot[lane] : FF{0.f, 0.f};
-        y = warp_incl_scan_ff(y);
-        if (lane < kCW) wtot[lane] = y;
+    FF acc{0.f, 0.f}, pre{0.f, 0.f};
+    float dacc = 0.f, dpre = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCW; ++i) {
+        if (i == warp) { pre = acc; dpre = dacc; }
+        acc = ff_combine(acc, wv[i]);
+        dacc += wd[i];
     }
-    fin_sync();
-    const FF r = warp > 0 ? ff_combine(wtot[warp - 1], x) : x;
-    *total = wtot[kCW - 1];
-    fin_sync();
-    return r;
+    const FF vex = ff_shfl_up(vin, 1);
+    const float dex = __shfl_up_sync(0xffffffffu, din, 1);
+    GroupPrefix g;
+    g.excl = lane > 0 ? ff_combine(pre, vex) : pre;
+    g.incl = ff_combine(pre, vin);
+    g.dexcl = lane > 0 ? dpre + dex : dpre;
+    g.dincl = dpre + din;
+    g.tot = acc;
+    g.dtot = dacc;
+    return g;
 }
 
-// Exclusive counterpart of an inclusive group scan result r (thread order).
-__device__ __forceinline__ FF block_excl_from_incl(FF r, const FF* wtot_scanned, int tid) {
-    const int lane = tid & 31, warp = tid >> 5;
-    const FF up = ff_shfl_up(r, 1);
-    if (lane > 0) return up;
-    return warp > 0 ? wtot_scanned[warp - 1] : FF{0.f, 0.f};
-}
-
-// The ratio Za / Zb of the two row normalisers of sequence b from each
-// thread's share of the segment sums (one group reduction of both).
-__device__ __forceinline__ FF normaliser_ratio_of(FF za, FF zb, FF* wtot, int tid) {
-    const int lane = tid & 31, warp = tid >> 5;
-    za = warp_sum_ff(za);
-    zb = warp_sum_ff(zb);
-    fin_sync();                                           // wtot may still be read by a caller's scan
-    if (lane == 0) {
-        wtot[warp] = za;
-        wtot[kCW + warp] = zb;
+// Inclusive warp scan of floats in lane order.
+__device__ __forceinline__ float warp_incl_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    fin_sync();
-    FF Za{0.f, 0.f}, Zb{0.f, 0.f};
-    for (int w = 0; w < kCW; ++w) {
-        Za = ff_combine(Za, wtot[w]);
-        Zb = ff_combine(Zb, wtot[kCW + w]);
-    }
-    fin_sync();
-    return ff_div(Za, Zb);
-}
-
-// The same from the segment sums in the workspace (thread t takes segments
-// t, t + kCT, ...).
-__device__ __forceinline__ FF normaliser_ratio(const VerifyArgs& a, int b, FF* wtot, int tid) {
-    const int ns = a.C * kCW;
-    const float4* zs = a.zsum + (size_t)b * ns;
-    FF za{0.f, 0.f}, zb{0.f, 0.f};
-    for (int s = tid; s < ns; s += kCT) {
-        const float4 q = __ldcg(&zs[s]);
-        za = ff_combine(za, FF{q.x, q.y});
-        zb = ff_combine(zb, FF{q.z, q.w});
-    }
-    return normaliser_ratio_of(za, zb, wtot, tid);
+    return x;
 }
 
 // The weights of the kSearchPT consecutive elements thread tid holds in
@@ -416,99 +420,153 @@ __device__ __forceinline__ void search_weights(const VerifyArgs& a, const FinalR
     }
 }
 
-// Shared memory of a final-pass group.
-struct FinalSmem {
-    FF wtot[2 * kCW];
-    FF lo;
-    int sel, last, seg;
-    int mine;                 // final-pass kernel: this CTA finished its sequence's last chunk
+// Segment totals of sequence b that thread tid sums: segments tid G ... tid G
+// + G - 1 of the ns in the row.  za and zb are the target and draft
+// normalisers' shares; v the quantity the search scans (the residual sums at
+// rt after a rejection, else the target sums) and dv its slope in the ratio.
+struct ThreadSums {
+    FF za, zb, v;
+    float dv;
 };
 
+__device__ __forceinline__ ThreadSums thread_sums(const VerifyArgs& a, int b, int ns, int G, bool rej, int tid) {
+    ThreadSums t{{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, 0.f};
+    for (int g = 0; g < G; ++g) {
+        const int s = tid * G + g;
+        if (s >= ns) break;
+        const float4 qz = __ldcg(&a.zsum[(size_t)b * ns + s]);
+        float4 qw = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rej) qw = __ldcg(&a.wsum[(size_t)b * ns + s]);
+        t.za = ff_combine(t.za, FF{qz.x, qz.y});
+        t.zb = ff_combine(t.zb, FF{qz.z, qz.w});
+        if (rej) {
+            t.v = ff_combine(t.v, FF{qw.x, qw.y});
+            t.dv += qw.z;
+        }
+    }
+    if (!rej) t.v = t.za;
+    return t;
+}
+
+// Group barrier phase of the search: the scanned quantity's prefixes and,
+// after a rejection, the normalisers' totals.  One barrier.
+__device__ __forceinline__ GroupPrefix scan_phase(const ThreadSums& t, bool rej, FinalSmem& sm, FF* Za,
+                                                  FF* Zb, int tid) {
+    const int lane = tid & 31, warp = tid >> 5;
+    const FF vin = warp_incl_scan_ff(t.v);
+    const float din = warp_incl_scan(rej ? t.dv : 0.f);
+    FF za{0.f, 0.f}, zb{0.f, 0.f};
+    if (rej) {
+        za = warp_sum_ff(t.za);
+        zb = warp_sum_ff(t.zb);
+    }
+    if (lane == 31) {
+        sm.wv[warp] = vin;
+        sm.wd[warp] = din;
+        sm.wa[warp] = za;
+        sm.wb[warp] = zb;
+    }
+    fin_sync();
+    *Za = *Zb = FF{0.f, 0.f};
+    if (rej)
+#pragma unroll
+        for (int i = 0; i < kCW; ++i) {
+            *Za = ff_combine(*Za, sm.wa[i]);
+            *Zb = ff_combine(*Zb, sm.wb[i]);
+        }
+    return group_prefix(vin, din, sm.wv, sm.wd, tid);
+}
+
+// x - d dR as float-float: a scanned residual sum moved from ratio rt to R
+// to first order (dR = R - rt).  The same bits for the same inputs in every
+// thread, so corrected prefixes still tile their range exactly.
+__device__ __forceinline__ FF at_ratio(FF x, float d, float dR) { return ff_combine(x, FF{-dR * d, 0.f}); }
+
 // The search of sequence b, by one final-pass group once every segment sum
-// of the row pair is in the workspace: the owning segment from the segment totals, then the
-// owning element from that segment's weights, recomputed with the same
-// arithmetic that produced its total.
+// of the row pair is in the workspace: the owning segment from the segment
+// totals, then the owning element from that segment's weights, recomputed
+// with the same arithmetic that produced its total.  u is the sequence's
+// uniform for the final token.  Four group barriers: segment prefixes and
+// normalisers together, the owning segment, the segment's weight prefixes,
+// the owning element.
 template <int ELT, bool VEC>
-__device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, const SampleDesc& d,
+__device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, const SampleDesc& d, float u,
                                                 FinalSmem& sm, int tid) {
-    FF* wtot = sm.wtot;
-    int& s_sel = sm.sel;
-    int& s_last = sm.last;
-    int& s_seg = sm.seg;
-    FF& s_lo = sm.lo;
     bool rej = d.k < a.gamma;
     const int ns = a.C * kCW;                             // segments in the row
     const int G = (ns + kCT - 1) / kCT;                   // consecutive segments per thread
-    // With one segment per thread (V <= kCT kSeg) each thread loads its
-    // segment's sums once, normaliser and residual sums together; otherwise
-    // they are read where needed.
-    const bool one = G == 1;
-    float4 qz = make_float4(0.f, 0.f, 0.f, 0.f), qw = qz;
-    if (one && tid < ns) {
-        qz = __ldcg(&a.zsum[(size_t)b * ns + tid]);
-        if (rej) qw = __ldcg(&a.wsum[(size_t)b * ns + tid]);
+    if (tid == 0) {
+        sm.sel = sm.sel2 = 0x7fffffff;
+        sm.last = sm.last2 = -1;
     }
-    FF R{0.f, 0.f};
-    if (rej) R = one ? normaliser_ratio_of(FF{qz.x, qz.y}, FF{qz.z, qz.w}, wtot, tid) : normaliser_ratio(a, b, wtot, tid);
-    // residual sums at the exact ratio: w(rt) - (R - rt) dd, to first order
-    const float dR = (R.hi - d.rt) + R.lo;
-    auto seg_total = [&](int s) -> FF {
-        const float4 q = one ? (rej ? qw : qz) : __ldcg(rej ? &a.wsum[(size_t)b * ns + s] : &a.zsum[(size_t)b * ns + s]);
-        return rej ? ff_combine(FF{q.x, q.y}, FF{-dR * q.z, 0.f}) : FF{q.x, q.y};
-    };
-
-    // Thread totals over its segments and their prefix; fall back to p_k if
-    // the residual is empty.
-    FF T{0.f, 0.f}, S{0.f, 0.f}, incl{0.f, 0.f};
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        T = FF{0.f, 0.f};
-        for (int g = 0; g < G; ++g) {
-            const int s = tid * G + g;
-            if (s < ns) T = ff_combine(T, seg_total(s));
-        }
-        incl = block_incl_scan_ff(T, wtot, &S, tid);
-        if (S.hi > 0.f || !rej) break;
-        rej = false;                                      // p_k equals q_k to rounding
+    ThreadSums t = thread_sums(a, b, ns, G, rej, tid);
+    FF Za, Zb, R{0.f, 0.f};
+    GroupPrefix g = scan_phase(t, rej, sm, &Za, &Zb, tid);
+    float dR = 0.f;
+    if (rej) {
+        R = ff_div(Za, Zb);
+        dR = (R.hi - d.rt) + R.lo;                        // residual sums at R: w(rt) - (R - rt) dd
+    }
+    FF S = rej ? at_ratio(g.tot, g.dtot, dR) : g.tot;
+    if (rej && !(S.hi > 0.f)) {
+        // p_k equals q_k to rounding: the residual has no mass, draw from p_k
+        rej = false;
+        dR = 0.f;
+        t.v = t.za;
+        t.dv = 0.f;
+        fin_sync();                                       // every thread has read the warp totals
+        g = scan_phase(t, false, sm, &Za, &Zb, tid);
+        S = g.tot;
     }
     if (!(S.hi > 0.f)) return;                            // unreachable for rows with a finite logit
-    const FF excl = block_excl_from_incl(incl, wtot, tid);
-    FF target = ff_scale(a.u[(size_t)b * (a.gamma + 1) + a.gamma], S);
+    const FF excl = rej ? at_ratio(g.excl, g.dexcl, dR) : g.excl;
+    const FF incl = rej ? at_ratio(g.incl, g.dincl, dR) : g.incl;
+    FF target = ff_scale(u, S);
     if (!ff_lt(target, S))                                // u >= 1 clamps to the last token with mass
         target = ff_norm(FF{S.hi, S.lo - fabsf(S.hi) * 1.4210855e-14f});
 
-    // The owning thread: the one whose interval [excl, incl) holds the target
-    // (the intervals tile [0, S) exactly; the last thread with mass stands in
-    // should rounding ever leave a gap), then its owning segment.
-    if (tid == 0) { s_sel = -1; s_last = -1; }
+    // The owning thread: the first whose interval [excl, incl) holds the
+    // target (the intervals tile [0, S), so one does; the last thread with
+    // mass stands in should that ever fail), then its owning segment.
+    sm.xs[tid] = excl;
+    const bool has = ff_lt(excl, incl);
+    if (has && !ff_lt(target, excl) && ff_lt(target, incl)) atomicMin(&sm.sel, tid);
+    if (has) atomicMax(&sm.last, tid);
     fin_sync();
-    bool has = T.hi > 0.f;
-    if (has && !ff_lt(target, excl) && ff_lt(target, incl)) s_sel = tid;
-    if (has) atomicMax(&s_last, tid);
-    fin_sync();
-    if (tid == (s_sel >= 0 ? s_sel : s_last)) {
-        FF run = excl;
-        int pick = -1, last = -1;
-        FF plo = excl, llo = excl;
-        for (int g = 0; g < G; ++g) {
-            const int s = tid * G + g;
-            if (s >= ns) break;
-            const FF t = seg_total(s);
-            const FF nxt = ff_combine(run, t);
-            if (t.hi > 0.f) {
-                last = s;
-                llo = run;
-                if (pick < 0 && ff_lt(target, nxt)) { pick = s; plo = run; }
+    const int owner = sm.sel != 0x7fffffff ? sm.sel : sm.last;
+    if (owner < 0) return;
+    int sg;
+    FF P;
+    if (G == 1) {
+        sg = owner;
+        P = sm.xs[owner];
+    } else {
+        if (tid == owner) {
+            FF run = excl;
+            int pick = -1, last = -1;
+            FF plo = excl, llo = excl;
+            for (int gg = 0; gg < G; ++gg) {
+                const int s = tid * G + gg;
+                if (s >= ns) break;
+                const float4 q = __ldcg(rej ? &a.wsum[(size_t)b * ns + s] : &a.zsum[(size_t)b * ns + s]);
+                const FF ts = rej ? at_ratio(FF{q.x, q.y}, q.z, dR) : FF{q.x, q.y};
+                const FF nxt = ff_combine(run, ts);
+                if (ts.hi > 0.f) {
+                    last = s;
+                    llo = run;
+                    if (pick < 0 && ff_lt(target, nxt)) { pick = s; plo = run; }
+                }
+                run = nxt;
             }
-            run = nxt;
+            if (pick < 0) { pick = last; plo = llo; }
+            sm.seg = pick;
+            sm.P = plo;
         }
-        if (pick < 0) { pick = last; plo = llo; }
-        s_seg = pick;
-        s_lo = plo;
+        fin_sync();
+        sg = sm.seg;
+        P = sm.P;
+        if (sg < 0) return;
     }
-    fin_sync();
-    const int sg = s_seg;
-    const FF P = s_lo;
-    fin_sync();
 
     // Inside the segment: kSearchPT consecutive elements per thread.
     const FinalRows f = final_rows<ELT>(a, b, d);
@@ -519,18 +577,21 @@ __device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, cons
 #pragma unroll
     for (int e = 0; e < kSearchPT; ++e) ff_add(ts, w[e]);
     ts = ff_norm(ts);
-    FF tot;
-    const FF ti = block_incl_scan_ff(ts, wtot, &tot, tid);
-    const FF te = block_excl_from_incl(ti, wtot, tid);
-    const FF lo = ff_combine(P, te), hi = ff_combine(P, ti);
-    if (tid == 0) { s_sel = -1; s_last = -1; }
+    const int lane = tid & 31, warp = tid >> 5;
+    const FF tin = warp_incl_scan_ff(ts);
+    if (lane == 31) {
+        sm.wv[warp] = tin;                                // the scan phase's reads ended at the barrier above
+        sm.wd[warp] = 0.f;
+    }
     fin_sync();
-    has = ts.hi > 0.f;
-    if (has && !ff_lt(target, lo) && ff_lt(target, hi)) s_sel = tid;
-    if (has) atomicMax(&s_last, tid);
+    const GroupPrefix h = group_prefix(tin, 0.f, sm.wv, sm.wd, tid);
+    const FF lo = ff_combine(P, h.excl), hi = ff_combine(P, h.incl);
+    const bool has2 = ts.hi > 0.f;
+    if (has2 && !ff_lt(target, lo) && ff_lt(target, hi)) atomicMin(&sm.sel2, tid);
+    if (has2) atomicMax(&sm.last2, tid);
     fin_sync();
-    const int owner = s_sel >= 0 ? s_sel : s_last;
-    if (tid == owner) {
+    const int owner2 = sm.sel2 != 0x7fffffff ? sm.sel2 : sm.last2;
+    if (tid == owner2) {
         // first element whose inclusive prefix exceeds the target; the last
         // element with mass if rounding leaves none
         FF run{0.f, 0.f};

@@ -51,21 +51,30 @@ struct SampleDesc {
 // decide step of group g - 1 writes.
 constexpr int kLazyGroups = 8;
 
-// Workspace: [error word (256 bytes reserved) | per-warp row partials |
+// Workspace: [error word and the streams' claim counter (256 bytes
+// reserved) | per-warp row partials |
 // SampleDesc[B] | per-sequence finish tickets | per-segment normaliser sums |
 // per-segment residual sums and slopes | lazy survivor counts (256 bytes) and
 // lists [kLazyGroups, B]].
-// Every region after the error word is rewritten by the kernels of a call
-// before another kernel of that call reads it (the tickets are zeroed by the
-// kernel that writes the SampleDesc, the survivor counts by the first lazy
+// Every region after the first 256 bytes is rewritten by the kernels of a
+// call before another kernel of that call reads it (the tickets are zeroed by
+// the kernel that writes the SampleDesc, the survivor counts by the first lazy
 // stream), so a workspace carries nothing from one call to the next except
 // the error word, which only accumulates error bits until
-// spec_verify_read_error clears it.
+// spec_verify_read_error clears it, and the claim counter (kClaimOff), whose
+// launch tag makes every stream launch start it afresh whatever it holds.
 struct WsLayout {
     size_t err_off, part_off, part_count, desc_off, tick_off, zsum_off, wsum_off, lz_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offset of the streams' 64-bit claim counter inside the first 256
+// bytes of a workspace (the error word is at offset 0).
+constexpr size_t kClaimOff = 128;
+// The counter holds (launch tag << kClaimIdxBits) | next chunk index.
+constexpr int kClaimIdxBits = 24;
+constexpr int kClaimTagBits = 64 - kClaimIdxBits;
 
 inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     WsLayout L;
@@ -123,6 +132,9 @@ inline cudaError_t device_once(DeviceSlots& slots, int* out, F setup) {
 // default, unless spec_verify_set_wait_limit changed it.
 constexpr uint32_t kWaitLimitDefault = 1u << 24;
 uint32_t ring_wait_limit();
+// A fresh nonzero launch tag (kClaimTagBits bits; process-wide, increasing
+// until it wraps) for the claim counter of one stream launch.
+uint64_t next_launch_tag();
 
 // Upper ends of the lazy pass's position groups (host only; ends holds
 // kLazyGroups entries); returns their count.

@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
     pdl_wait();
     const SampleDesc d = a.desc[b];
     if (d.k < 0) return;
+    // the final token's uniform, loaded now so that its latency is not the search's
+    const float u = a.u[(size_t)b * (a.gamma + 1) + a.gamma];
     {
         const FinalRows f = final_rows<ELT>(a, b, d);
         segment_sums_global<ELT, VEC>(a, f, b, c * kCW + (threadIdx.x >> 5), d.rt, threadIdx.x & 31);
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
     }
     __syncthreads();
     if (!sm.mine) return;
-    search_sequence<ELT, VEC>(a, b, d, sm, threadIdx.x);
+    search_sequence<ELT, VEC>(a, b, d, u, sm, threadIdx.x);
 }
 
 // ------------------------------------------------ lazy (early-exit) pass 1

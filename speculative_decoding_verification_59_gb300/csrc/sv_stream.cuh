@@ -400,10 +400,105 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
     thr = fmaxf(thr, ov[K - 1]);                          // more than 2K marked: K of them reach it
 }
 
+// Stage marker of the end of a CTA's chunks.
+constexpr unsigned kNoChunk = 0xffffffffu;
+
+// The block chunks that one CTA of a ring stream takes, in order.  Three
+// quarters of a stream's chunks are dealt out statically, a contiguous range
+// per CTA; the rest are claimed one at a time from the workspace's counter,
+// so CTAs that stream faster (the rate differs by SM and by die) take more
+// of them and the stream ends together instead of with its slowest CTA.
+// Each claim is issued one chunk ahead of its use, so its round trip
+// overlaps the copies in flight.
+//
+// The counter holds (launch tag << kClaimIdxBits) | next index.  Every CTA
+// first raises it to (tag << kClaimIdxBits) | (first dynamic index) with an
+// atomic max: tags increase from launch to launch, so the first such max of
+// a launch restarts the count and the others change nothing, and a CTA's own
+// max precedes its claims, which therefore always see this launch's tag --
+// except after the process's tag count wrapped (once in 2^40 launches), when
+// the first claim that finds an older tag installs this one by compare-and-swap.
+struct ChunkSource {
+    unsigned s, s_end, total, first_dyn;
+    bool dyn, have;
+    unsigned long long* ctr;
+    unsigned long long tag, pending;
+    uint32_t limit;
+    int* err;
+
+    __device__ __forceinline__ ChunkSource(const VerifyArgs& a, unsigned total_) {
+        total = total_;
+        ctr = a.claim;
+        tag = a.claim_tag;
+        limit = a.wait_limit;
+        err = a.err;
+        have = false;
+        pending = 0ull;
+        const unsigned q = (unsigned)(((unsigned long long)total * 3ull / 4ull) / gridDim.x);
+        dyn = q >= 2 && total < (1u << (kClaimIdxBits - 1));
+        if (dyn) {
+            first_dyn = q * gridDim.x;
+            s = blockIdx.x * q;
+            s_end = s + q;
+            asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(ctr), "l"(tag | first_dyn)
+                         : "memory");
+        } else {
+            first_dyn = total;
+            cta_range(total, blockIdx.x, gridDim.x, &s, &s_end);
+        }
+    }
+
+    __device__ __forceinline__ void claim() {
+        asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(pending) : "l"(ctr) : "memory");
+        have = true;
+    }
+
+    // A claim that found another launch's tag: install this launch's with
+    // compare-and-swap (taking the first dynamic index), or, if another CTA
+    // already did, claim again.
+    __device__ unsigned long long reclaim(unsigned long long v) {
+        const unsigned long long tmask = ~((1ull << kClaimIdxBits) - 1ull);
+        for (uint32_t i = 0; i < limit; ++i) {
+            if ((v & tmask) == tag) {
+                asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(ctr) : "memory");
+                if ((v & tmask) == tag) return v;
+                continue;
+            }
+            unsigned long long old;
+            asm volatile("atom.relaxed.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                         : "=l"(old)
+                         : "l"(ctr), "l"(v), "l"(tag | (first_dyn + 1ull))
+                         : "memory");
+            if (old == v) return tag | first_dyn;
+            v = old;
+        }
+        atomicOr(err, SPEC_DEVERR_TIMEOUT);
+        return tag | total;                               // gives up: no further chunks
+    }
+
+    // The next chunk index, kNoChunk at the end.
+    __device__ __forceinline__ unsigned next() {
+        if (s < s_end) {
+            const unsigned c = s++;
+            if (s == s_end && dyn) claim();
+            return c;
+        }
+        if (!have) return kNoChunk;
+        have = false;
+        unsigned long long v = pending;
+        if ((v & ~((1ull << kClaimIdxBits) - 1ull)) != tag) v = reclaim(v);
+        const unsigned c = (unsigned)(v & ((1ull << kClaimIdxBits) - 1ull));
+        if (c >= total) return kNoChunk;
+        claim();
+        return c;
+    }
+};
+
 template <int ELT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ unsigned stage_chunk[kStages];          // chunk index each stage holds
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int KT = topk_of(MODE);
     const size_t rowbytes = (size_t)a.V * ELT;
@@ -426,28 +521,49 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     StreamRows rows;
 
     if (warp == 0) {
-        // ---- producer: one lane issues the bulk copies
+        // ---- producer: one lane issues the bulk copies and hands each
+        // stage's chunk index to the consumers (kNoChunk ends the stream)
         if (lane == 0) {
-            unsigned c0, c1, issued = 0;
-            cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
-            bool ok = true;
-            for (unsigned c = c0; c < c1; ++c, ++issued) {
+            ChunkSource src(a, total);
+            unsigned issued = 0;
+            bool ok = true, ended = false, triggered = false;
+            for (;; ++issued) {
                 const int st = (int)(issued % kStages);
                 const unsigned use = issued / kStages;
                 if (use > 0 && !wait_bounded(&empty[st], (use - 1) & 1u, a.wait_limit)) { ok = false; break; }
+                const unsigned c = src.next();
+                if (c == kNoChunk) {
+                    if (!triggered) pdl_trigger();
+                    stage_chunk[st] = kNoChunk;
+                    mbar_arrive(&full[st]);                   // releases the consumers' last wait
+                    ended = true;
+                    break;
+                }
                 const unsigned rr = c / (unsigned)a.nseg;
                 const int seg = (int)(c - rr * (unsigned)a.nseg);
                 const size_t off = (size_t)seg * kStageBytes;
                 const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
-                if (c + 1 == c1) pdl_trigger();
                 const unsigned pr = rows.part_row<MODE>(a, rr);
+                if (!triggered && src.s == src.s_end) {
+                    // static share issued: the next kernel may start launching
+                    pdl_trigger();
+                    triggered = true;
+                }
+                stage_chunk[st] = c;
                 mbar_arrive_expect_tx(&full[st], bytes);
                 bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, pr, rowbytes) + off, bytes,
                          &full[st]);
             }
-            if (!ok) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
-            // Do not leave while a copy may still be writing this CTA's shared memory.
-            const unsigned first = issued > kStages ? issued - kStages : 0;
+            if (!ok) {
+                if (!triggered) pdl_trigger();
+                atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+            }
+            // Do not leave while a copy may still be writing this CTA's shared
+            // memory.  The end marker reused the stage of copy issued - kStages
+            // after its consumers had released it (that copy is complete, and
+            // its barrier has moved two phases on), so the check starts after it.
+            unsigned first = issued > kStages ? issued - kStages : 0;
+            if (ended && issued >= kStages) first = issued - kStages + 1;
             for (unsigned i = first; i < issued; ++i)
                 if (!wait_bounded(&full[i % kStages], (i / kStages) & 1u)) {
                     atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
@@ -462,19 +578,20 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     const int cw = warp - 1;
     unsigned tk_row = 0xffffffffu;                        // top-K: row of the carried bound
     float tk_thr = kNegInf;
-    unsigned c0, c1, it = 0;
-    cta_range(total, blockIdx.x, gridDim.x, &c0, &c1);
     bool ok = true;
-    for (unsigned c = c0; c < c1; ++c, ++it) {
+    for (unsigned it = 0;; ++it) {
         const int st = (int)(it % kStages);
-        if (ok && !wait_bounded(&full[st], (it / kStages) & 1u, a.wait_limit)) ok = false;
+        if (!wait_bounded(&full[st], (it / kStages) & 1u, a.wait_limit)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const unsigned c = stage_chunk[st];
+        if (c == kNoChunk) break;
         const unsigned rr = c / (unsigned)a.nseg;
         const int seg = (int)(c - rr * (unsigned)a.nseg);
         const unsigned pr = rows.part_row<MODE>(a, rr);
         const size_t off = (size_t)seg * kStageBytes;
         const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
         const int wb = bytes - cw * (32 * kLaneBytes);            // valid bytes of this warp chunk
-        const bool use = __all_sync(0xffffffffu, ok) && wb > 0;
+        const bool use = wb > 0;
         float2 part = make_float2(0.f, 0.f);
         if (use) {
             uint4 v[kVecPerLane];
@@ -504,7 +621,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         }
         __syncwarp();
         if (lane == 0) {
-            if (ok) mbar_arrive(&empty[st]);
+            mbar_arrive(&empty[st]);
             if constexpr (KT == 0) a.parts[(size_t)pr * P + seg * kWarps + cw] = part;
         }
     }
@@ -620,7 +737,10 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
 // Launches the streaming pass of MODE over the rows of a (persistent grid):
 // the bulk-copy ring for 16-byte rows, the register path otherwise.
 template <int ELT, int MODE>
-cudaError_t launch_stream(const VerifyArgs& a, const DeviceInfo& di, cudaStream_t st) {
+cudaError_t launch_stream(const VerifyArgs& args, const DeviceInfo& di, cudaStream_t st) {
+    VerifyArgs a = args;
+    a.claim = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(a.err) + kClaimOff);
+    a.claim_tag = next_launch_tag() << kClaimIdxBits;
     if (((size_t)a.V * ELT) % 16 == 0) {
         auto kfn = ring_stream_kernel<ELT, MODE>;
         const int smem = kStages * kStageBytes;
