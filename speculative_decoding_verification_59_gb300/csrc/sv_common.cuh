@@ -242,6 +242,29 @@ __device__ __forceinline__ FF warp_incl_scan_ff(FF a) {
     return a;
 }
 
+// ---- tagged words --------------------------------------------------------------
+// A value that a kernel may read while its writer (another kernel of the same
+// call, running beside it) may not have written it yet travels as 64-bit
+// words, each holding 32 bits of data in its low half and the call's tag in
+// its high half.  Aligned 64-bit words are written and read whole, so a
+// reader that sees its call's tag in a word has that word's data from its
+// call -- no fence on either side; an older call's data carries another tag.
+// Stored and loaded in pairs (16 bytes, each word whole).
+__device__ __forceinline__ void st_tagged2(unsigned long long* p, uint32_t v0, uint32_t v1, uint32_t tag) {
+    const unsigned long long t = (unsigned long long)tag << 32;
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(t | v0), "l"(t | v1) : "memory");
+}
+
+// Loads a pair; true when both words carry tag.
+__device__ __forceinline__ bool ld_tagged2(const unsigned long long* p, uint32_t tag, uint32_t* v0,
+                                           uint32_t* v1) {
+    unsigned long long x, y;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+    *v0 = (uint32_t)x;
+    *v1 = (uint32_t)y;
+    return (uint32_t)(x >> 32) == tag && (uint32_t)(y >> 32) == tag;
+}
+
 // ---- programmatic dependent launch -------------------------------------------
 // The kernels of the library are launched with programmatic stream
 // serialisation (launch_pdl): a kernel may begin launching once every CTA of

@@ -60,11 +60,16 @@ struct VerifyArgs {
     int early_inputs;          // sampling: the decide kernel follows this call's own stream, so it
                                // may load the call's inputs before griddepcontrol.wait
     float2* parts;             // per-warp-chunk partials
-    SampleDesc* desc;          // sampling: rejection index and row maxima
-    unsigned* tick;            // sampling: per-sequence count of finished final-pass chunks
-    float4* zsum;              // sampling: [B, C, 8] (Za.hi, Za.lo, Zb.hi, Zb.lo) per segment
-    float4* wsum;              // sampling: [B, C, 8] (W.hi, W.lo, D, 0) per segment, rejections:
-                               // residual sum at the desc's ratio rt and its slope
+    unsigned long long* desc;  // sampling: [B] SampleDescs as kDescWords tagged words
+    unsigned long long epoch;  // sampling: this call's launch tag (kClaimTagBits bits, nonzero)
+    uint32_t ptag;             // sampling: this call's tag for tagged words (nonzero)
+    int poll_parts;            // sampling: the decide step runs beside the stream and waits for
+                               // each sequence's tagged partials instead of the whole stream
+    unsigned long long* tick;  // sampling: per-sequence count of finished final-pass chunks,
+                               // (epoch << kClaimIdxBits) | count
+    unsigned long long* sums;  // sampling: [B, C, 8] segments' sums as kSumWords tagged words:
+                               // Za, Zb (float-float), and after a rejection the residual sum W
+                               // at the desc's ratio rt (float-float) and its slope D
     int* err;
     int32_t* out_tok;
     int32_t* out_acc;
@@ -91,6 +96,19 @@ struct VerifyArgs {
     unsigned long long* claim;
     unsigned long long claim_tag;
 };
+
+// Partial i of a row-statistics stream: sampling stores them as tagged
+// 64-bit word pairs (the float in each word's low half), the other modes as
+// float2.
+template <bool TAGGED>
+__device__ __forceinline__ float2 load_part(const VerifyArgs& a, size_t i) {
+    if constexpr (TAGGED) {
+        const ulonglong2 q = __ldcg(reinterpret_cast<const ulonglong2*>(a.parts) + i);
+        return make_float2(__uint_as_float((uint32_t)q.x), __uint_as_float((uint32_t)q.y));
+    } else {
+        return __ldcg(a.parts + i);
+    }
+}
 
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier for a group of NT threads.
@@ -119,28 +137,28 @@ struct SampleDecideSmem {
 // registers, all rows' loads in flight together, and adds a row's partials in
 // increasing p whatever RB and KH are, so every row's result is bit-identical
 // across batch shapes.  lnZ is 0 for a row without a finite logit.
-template <int RB, int KH>
+template <int RB, int KH, bool TAGGED = false>
 __device__ __forceinline__ void merge_rows_stats(const VerifyArgs& a, int b, const int (&r)[RB], int lane,
                                                  float (&Mout)[RB], float (&lnZout)[RB]) {
     const int P = a.nseg * kWarps;
     float2 q[RB][KH];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
-        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r[j]) * P;
+        const size_t pr = ((size_t)b * a.rows_per_seq + r[j]) * P;
 #pragma unroll
         for (int h = 0; h < KH; ++h) {
             const int p = lane + 32 * h;
-            q[j][h] = (r[j] < a.rows_per_seq && p < P) ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
+            q[j][h] = (r[j] < a.rows_per_seq && p < P) ? load_part<TAGGED>(a, pr + p) : make_float2(kNegInf, 0.f);
         }
     }
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
         if (r[j] >= a.rows_per_seq) continue;             // warp-uniform
-        const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r[j]) * P;
+        const size_t pr = ((size_t)b * a.rows_per_seq + r[j]) * P;
         float m = kNegInf;
 #pragma unroll
         for (int h = 0; h < KH; ++h) m = fmaxf(m, q[j][h].x);
-        for (int p = lane + 32 * KH; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
+        for (int p = lane + 32 * KH; p < P; p += 32) m = fmaxf(m, load_part<TAGGED>(a, pr + p).x);
         m = warp_max(m);
         FF z{0.f, 0.f};
         if (m != kNegInf) {
@@ -149,7 +167,7 @@ __device__ __forceinline__ void merge_rows_stats(const VerifyArgs& a, int b, con
                 if (q[j][h].x != kNegInf)
                     ff_add(z, q[j][h].y * ex2_approx(fmaf(q[j][h].x - m, a.s, -partial_residual(q[j][h].x, a.s))));
             for (int p = lane + 32 * KH; p < P; p += 32) {
-                const float2 t = __ldcg(&pr[p]);
+                const float2 t = load_part<TAGGED>(a, pr + p);
                 if (t.x != kNegInf)
                     ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
             }
@@ -164,21 +182,22 @@ __device__ __forceinline__ void merge_rows_stats(const VerifyArgs& a, int b, con
 // merge_rows_stats, written out for the sampling decide (a template-built
 // version of this one-row merge measured 4 us slower in the chained
 // chain-b64 step, with the same registers and shared memory).
+template <bool TAGGED = false>
 __device__ __forceinline__ void merge_row_stats(const VerifyArgs& a, int b, int r, int lane,
                                                 float* Mout, float* lnZout) {
     constexpr int kHeld = 8;
     const int P = a.nseg * kWarps;
-    const float2* pr = a.parts + ((size_t)b * a.rows_per_seq + r) * P;
+    const size_t pr = ((size_t)b * a.rows_per_seq + r) * P;
     float2 q[kHeld];
 #pragma unroll
     for (int h = 0; h < kHeld; ++h) {
         const int p = lane + 32 * h;
-        q[h] = p < P ? __ldcg(&pr[p]) : make_float2(kNegInf, 0.f);
+        q[h] = p < P ? load_part<TAGGED>(a, pr + p) : make_float2(kNegInf, 0.f);
     }
     float m = kNegInf;
 #pragma unroll
     for (int h = 0; h < kHeld; ++h) m = fmaxf(m, q[h].x);
-    for (int p = lane + 32 * kHeld; p < P; p += 32) m = fmaxf(m, __ldcg(&pr[p]).x);
+    for (int p = lane + 32 * kHeld; p < P; p += 32) m = fmaxf(m, load_part<TAGGED>(a, pr + p).x);
     m = warp_max(m);
     FF z{0.f, 0.f};
     if (m != kNegInf) {
@@ -187,7 +206,7 @@ __device__ __forceinline__ void merge_row_stats(const VerifyArgs& a, int b, int 
             if (q[h].x != kNegInf)
                 ff_add(z, q[h].y * ex2_approx(fmaf(q[h].x - m, a.s, -partial_residual(q[h].x, a.s))));
         for (int p = lane + 32 * kHeld; p < P; p += 32) {
-            const float2 t = __ldcg(&pr[p]);
+            const float2 t = load_part<TAGGED>(a, pr + p);
             if (t.x != kNegInf)
                 ff_add(z, t.y * ex2_approx(fmaf(t.x - m, a.s, -partial_residual(t.x, a.s))));
         }
@@ -242,6 +261,43 @@ __device__ __forceinline__ bool accept_draft(float lp, float lq, float u) {
     return u < r;
 }
 
+// Sampling call whose decide kernel runs beside the stream: wait (bounded)
+// until every partial of sequence b carries this call's tag.  One thread
+// first polls the partial the stream reaches last for this sequence (the
+// last warp of its last chunk: the stream advances through the chunks in
+// index order), then every thread checks its share and the check repeats
+// until no partial is stale.  The whole CTA (NT threads) takes part.
+template <int NT>
+__device__ void wait_seq_parts(const VerifyArgs& a, int b, int gt) {
+    const size_t n = (size_t)a.rows_per_seq * a.nseg * kWarps;
+    const unsigned long long* base = reinterpret_cast<const unsigned long long*>(a.parts) + 2 * (size_t)b * n;
+    const unsigned long long tag = (unsigned long long)a.ptag;
+    auto fresh = [&](size_t i) {
+        unsigned long long x, y;
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(base + 2 * i) : "memory");
+        return (x >> 32) == tag && (y >> 32) == tag;
+    };
+    if (gt == 0)
+        for (uint32_t i = 0; !fresh(n - 1); ++i) {
+            if (i >= a.wait_limit) {
+                atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(200);
+        }
+    __syncthreads();
+    for (uint32_t round = 0;; ++round) {
+        int stale = 0;
+        for (size_t i = gt; i < n; i += NT) stale |= !fresh(i);
+        if (!__syncthreads_or(stale)) break;
+        if (round >= a.wait_limit) {
+            if (gt == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+            break;
+        }
+        __nanosleep(200);
+    }
+}
+
 // Row statistics from the partials (M = max m_p, Z = sum Z_p 2^((m_p - M) s),
 // float-float) and the accept decisions u_i < p_i(x_i)/q_i(x_i) in single
 // precision (GB300's double-precision rate is a small fraction of its float
@@ -271,16 +327,23 @@ __device__ int decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSme
         sm.k = a.gamma;
     }
     // Everything above reads inputs only; the partials below come from the
-    // stream, which may still be finishing.
-    pdl_wait();
+    // stream, which may still be running.
+    if (a.poll_parts) wait_seq_parts<NT>(a, b, gt);
+    else pdl_wait();
     group_sync_n<NT>();
-    for (int r = (gt >> 5); r < a.rows_per_seq; r += NT / 32) {
-        float M, lnZ;
-        merge_row_stats(a, b, r, gt & 31, &M, &lnZ);
-        if ((gt & 31) == 0) {
-            sm.M[r] = M;
-            sm.lnZ[r] = lnZ;
-        }
+    // two rows per warp and round, both rows' loads in flight together
+    constexpr int NW = NT / 32;
+    for (int r0 = (gt >> 5); r0 < a.rows_per_seq; r0 += 2 * NW) {
+        const int rr[2] = {r0, r0 + NW};
+        float M[2], lnZ[2];
+        merge_rows_stats<2, 4, true>(a, b, rr, gt & 31, M, lnZ);
+        if ((gt & 31) == 0)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (rr[j] < a.rows_per_seq) {
+                    sm.M[rr[j]] = M[j];
+                    sm.lnZ[rr[j]] = lnZ[j];
+                }
     }
     group_sync_n<NT>();
     for (int i = gt; i < a.gamma; i += NT) {
@@ -309,6 +372,38 @@ __device__ int decide_sample(const VerifyArgs& a, int b, int gt, SampleDecideSme
     return sm.bad ? -1 : sm.k;
 }
 
+// The SampleDesc of sequence b as this call's tagged words: the final pass,
+// which may already run, starts on the sequence when it reads them.
+__device__ __forceinline__ void publish_desc(const VerifyArgs& a, int b, const SampleDesc& d) {
+    unsigned long long* p = a.desc + (size_t)kDescWords * b;
+    st_tagged2(p, (uint32_t)d.k, __float_as_uint(d.mt), a.ptag);
+    st_tagged2(p + 2, __float_as_uint(d.md), __float_as_uint(d.rt), a.ptag);
+}
+
+// Waits (bounded) for this call's SampleDesc of sequence b; k = -1 after a
+// timeout (SPEC_DEVERR_TIMEOUT set).  One thread.
+__device__ __forceinline__ SampleDesc wait_desc(const VerifyArgs& a, int b) {
+    const unsigned long long* p = a.desc + (size_t)kDescWords * b;
+    SampleDesc d;
+    uint32_t k, mt, md, rt;
+    for (uint32_t i = 0;; ++i) {
+        const bool h0 = ld_tagged2(p, a.ptag, &k, &mt);
+        const bool h1 = ld_tagged2(p + 2, a.ptag, &md, &rt);
+        if (h0 && h1) break;
+        if (i >= a.wait_limit) {
+            atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+            k = 0xffffffffu;
+            break;
+        }
+        __nanosleep(100);
+    }
+    d.k = (int)k;
+    d.mt = __uint_as_float(mt);
+    d.md = __uint_as_float(md);
+    d.rt = __uint_as_float(rt);
+    return d;
+}
+
 // Every output of the sampling decision but the final token, and the
 // SampleDesc the final-sample kernels read.
 template <int NT>
@@ -322,8 +417,7 @@ static __device__ void write_sample_decision(const VerifyArgs& a, int b, int gt,
         d.mt = k >= 0 ? sm.M[k] : 0.f;
         d.md = (k >= 0 && k < a.gamma) ? sm.M[a.gamma + 1 + k] : 0.f;
         d.rt = (k >= 0 && k < a.gamma) ? expf(sm.lnZ[k] - sm.lnZ[a.gamma + 1 + k]) : 0.f;
-        a.desc[b] = d;
-        a.tick[b] = 0u;
+        publish_desc(a, b, d);
     }
     // accepted drafts and padding; slot k belongs to the final-pass search
     for (int i = gt; i <= a.gamma; i += NT)

@@ -322,10 +322,43 @@ __device__ __forceinline__ void segment_sums_global(const VerifyArgs& a, const F
     if (f.fast) segment_sums<ELT, true, 4>(a, f, j0, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
     else segment_sums<ELT, false, 1>(a, f, j0, lane, rt, ldA, ldB, &za, &zb, &w, &dd);
     if (lane == 0) {
-        const size_t i = (size_t)b * a.C * kCW + sg;
-        a.zsum[i] = make_float4(za.hi, za.lo, zb.hi, zb.lo);
-        if (f.rej) a.wsum[i] = make_float4(w.hi, w.lo, dd, 0.f);
+        unsigned long long* p = a.sums + ((size_t)b * a.C * kCW + sg) * kSumWords;
+        st_tagged2(p, __float_as_uint(za.hi), __float_as_uint(za.lo), a.ptag);
+        st_tagged2(p + 2, __float_as_uint(zb.hi), __float_as_uint(zb.lo), a.ptag);
+        st_tagged2(p + 4, __float_as_uint(w.hi), __float_as_uint(w.lo), a.ptag);
+        st_tagged2(p + 6, __float_as_uint(dd), 0u, a.ptag);
     }
+}
+
+// The sums of segment s of sequence b, once they carry this call's tag
+// (waiting, bounded, for a writer that may still run): za, zb, the residual
+// sum w and its slope dd.
+struct SegSums {
+    FF za, zb, w;
+    float dd;
+};
+
+__device__ __forceinline__ SegSums seg_sums(const VerifyArgs& a, size_t i) {
+    const unsigned long long* p = a.sums + i * kSumWords;
+    uint32_t v[8];
+    for (uint32_t n = 0;; ++n) {
+        bool ok = ld_tagged2(p, a.ptag, &v[0], &v[1]);
+        ok &= ld_tagged2(p + 2, a.ptag, &v[2], &v[3]);
+        ok &= ld_tagged2(p + 4, a.ptag, &v[4], &v[5]);
+        ok &= ld_tagged2(p + 6, a.ptag, &v[6], &v[7]);
+        if (ok) break;
+        if (n >= a.wait_limit) {
+            atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+            break;
+        }
+        __nanosleep(100);
+    }
+    SegSums r;
+    r.za = FF{__uint_as_float(v[0]), __uint_as_float(v[1])};
+    r.zb = FF{__uint_as_float(v[2]), __uint_as_float(v[3])};
+    r.w = FF{__uint_as_float(v[4]), __uint_as_float(v[5])};
+    r.dd = __uint_as_float(v[6]);
+    return r;
 }
 
 // Shared memory of a final-pass group.
@@ -336,6 +369,7 @@ struct FinalSmem {
     FF P;                           // base of the owning segment (several segments per thread)
     int sel, last, sel2, last2, seg;
     int mine;                       // final-pass kernel: this CTA finished its sequence's last chunk
+    SampleDesc desc;                // final-pass kernel: the sequence's SampleDesc
 };
 
 // Inclusive float-float and float prefixes of one value per thread over the
@@ -434,14 +468,12 @@ __device__ __forceinline__ ThreadSums thread_sums(const VerifyArgs& a, int b, in
     for (int g = 0; g < G; ++g) {
         const int s = tid * G + g;
         if (s >= ns) break;
-        const float4 qz = __ldcg(&a.zsum[(size_t)b * ns + s]);
-        float4 qw = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (rej) qw = __ldcg(&a.wsum[(size_t)b * ns + s]);
-        t.za = ff_combine(t.za, FF{qz.x, qz.y});
-        t.zb = ff_combine(t.zb, FF{qz.z, qz.w});
+        const SegSums q = seg_sums(a, (size_t)b * ns + s);
+        t.za = ff_combine(t.za, q.za);
+        t.zb = ff_combine(t.zb, q.zb);
         if (rej) {
-            t.v = ff_combine(t.v, FF{qw.x, qw.y});
-            t.dv += qw.z;
+            t.v = ff_combine(t.v, q.w);
+            t.dv += q.dd;
         }
     }
     if (!rej) t.v = t.za;
@@ -548,8 +580,8 @@ __device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, cons
             for (int gg = 0; gg < G; ++gg) {
                 const int s = tid * G + gg;
                 if (s >= ns) break;
-                const float4 q = __ldcg(rej ? &a.wsum[(size_t)b * ns + s] : &a.zsum[(size_t)b * ns + s]);
-                const FF ts = rej ? at_ratio(FF{q.x, q.y}, q.z, dR) : FF{q.x, q.y};
+                const SegSums q = seg_sums(a, (size_t)b * ns + s);
+                const FF ts = rej ? at_ratio(q.w, q.dd, dR) : q.za;
                 const FF nxt = ff_combine(run, ts);
                 if (ts.hi > 0.f) {
                     last = s;
@@ -610,12 +642,37 @@ __device__ __forceinline__ void search_sequence(const VerifyArgs& a, int b, cons
     }
 }
 
-// Ticket of a finished chunk: a gpu-scope acquire-release increment, so the
-// CTA that draws the last ticket sees every other chunk's segment sums.
-__device__ __forceinline__ unsigned take_ticket(unsigned* t) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
-    return old;
+// Ticket of a finished chunk of sequence b: this call's count of the
+// sequence's finished chunks before this one.  The counter holds
+// (launch tag << kClaimIdxBits) | count; each CTA raises it to
+// (tag << kClaimIdxBits) before its increment, which therefore sees this
+// call's tag (launch tags increase from call to call) except after the
+// process's tag count wrapped, when the first increment that finds an older
+// tag installs this one by compare-and-swap.  No fence: the segment sums are
+// tagged words that the search waits for.
+__device__ unsigned take_ticket(const VerifyArgs& a, int b) {
+    unsigned long long* t = a.tick + b;
+    const unsigned long long tag = a.epoch << kClaimIdxBits;
+    const unsigned long long tmask = ~((1ull << kClaimIdxBits) - 1ull);
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(t), "l"(tag) : "memory");
+    unsigned long long v;
+    asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(t) : "memory");
+    for (uint32_t i = 0; (v & tmask) != tag; ++i) {
+        if (i >= a.wait_limit) {
+            atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+            return 0u;
+        }
+        unsigned long long old;
+        asm volatile("atom.relaxed.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                     : "=l"(old)
+                     : "l"(t), "l"(v), "l"(tag | 1ull)
+                     : "memory");
+        if (old == v) return 0u;
+        v = old;
+        if ((v & tmask) == tag)
+            asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(t) : "memory");
+    }
+    return (unsigned)(v & ~tmask);
 }
 
 }  // namespace sv

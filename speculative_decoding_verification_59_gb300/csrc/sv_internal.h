@@ -37,6 +37,11 @@ inline int final_chunks(int V) { return (V + kFinalChunk - 1) / kFinalChunk; }
 // consecutive elements; the workspace keeps one total per segment.
 constexpr int kFinalSegs = kFinalChunkThreads / 32;
 
+// Tagged 64-bit words per SampleDesc (k, mt, md, rt) and per segment's sums
+// (Za, Zb, W as float-float pairs, D, and a pad word).
+constexpr int kDescWords = 4;
+constexpr int kSumWords = 8;
+
 // Per-sequence result of the accept decisions, read by the final-sample kernels.
 struct SampleDesc {
     int k;        // rejection index (< gamma), gamma when all drafts were accepted, -1: bad input
@@ -52,19 +57,18 @@ struct SampleDesc {
 constexpr int kLazyGroups = 8;
 
 // Workspace: [error word and the streams' claim counter (256 bytes
-// reserved) | per-warp row partials |
-// SampleDesc[B] | per-sequence finish tickets | per-segment normaliser sums |
-// per-segment residual sums and slopes | lazy survivor counts (256 bytes) and
+// reserved) | per-warp row partials | SampleDesc[B] (kDescWords tagged
+// words each) | per-sequence finish tickets (tagged counts) | per-segment
+// sums (kSumWords tagged words each) | lazy survivor counts (256 bytes) and
 // lists [kLazyGroups, B]].
-// Every region after the first 256 bytes is rewritten by the kernels of a
-// call before another kernel of that call reads it (the tickets are zeroed by
-// the kernel that writes the SampleDesc, the survivor counts by the first lazy
-// stream), so a workspace carries nothing from one call to the next except
-// the error word, which only accumulates error bits until
-// spec_verify_read_error clears it, and the claim counter (kClaimOff), whose
-// launch tag makes every stream launch start it afresh whatever it holds.
+// A call's sampling partials, SampleDescs and segment sums are tagged words
+// (sv_common.cuh) carrying the call's tag, and the tickets carry its launch
+// tag; the lazy survivor counts are zeroed by the call's first lazy stream.
+// So a workspace carries nothing from one call to the next except the error
+// word, which only accumulates error bits until spec_verify_read_error clears
+// it, whatever an earlier call (finished or not) left in it.
 struct WsLayout {
-    size_t err_off, part_off, part_count, desc_off, tick_off, zsum_off, wsum_off, lz_off, total;
+    size_t err_off, part_off, part_count, desc_off, tick_off, sum_off, lz_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -84,12 +88,12 @@ inline WsLayout ws_layout(int B, int gamma_or_nodes, int V) {
     size_t rows = (size_t)B * (size_t)(2 * (size_t)gamma_or_nodes + 1);
     // fp32 has the smaller warp chunk, hence the most partials per row
     L.part_count = rows * (size_t)nseg(V, 4) * kWarps;
-    L.desc_off = L.part_off + align256(sizeof(float2) * L.part_count);
+    // 16 bytes a partial: sampling stores them as tagged 64-bit word pairs
+    L.desc_off = L.part_off + align256(2 * sizeof(float2) * L.part_count);
     const size_t segs = (size_t)B * (size_t)final_chunks(V) * kFinalSegs;
-    L.tick_off = L.desc_off + align256(sizeof(SampleDesc) * (size_t)B);
-    L.zsum_off = L.tick_off + align256(sizeof(int) * (size_t)B);
-    L.wsum_off = L.zsum_off + align256(4 * sizeof(float) * segs);
-    L.lz_off = L.wsum_off + align256(4 * sizeof(float) * segs);
+    L.tick_off = L.desc_off + align256(kDescWords * sizeof(unsigned long long) * (size_t)B);
+    L.sum_off = L.tick_off + align256(sizeof(unsigned long long) * (size_t)B);
+    L.lz_off = L.sum_off + align256(kSumWords * sizeof(unsigned long long) * segs);
     L.total = L.lz_off + 256 + align256(sizeof(int) * (size_t)kLazyGroups * (size_t)B);
     return L;
 }

@@ -44,17 +44,22 @@ namespace sv {
 
 
 // One CTA per sequence: the accept decisions and every output but the final
-// token, and the SampleDesc the chunk kernels read.
-// 16 warps: one row's partials per warp for gamma <= 7 (15 rows), so the
-// merge is a single round of loads.
-constexpr int kSampleDecideThreads = 512;
+// token, and the SampleDesc the chunk kernels read.  In a whole sampling call
+// this kernel starts with the stream and runs beside it (8 warps of at most
+// 48 registers: two stream CTAs, one of these and a final-pass CTA fill an
+// SM's 64K registers exactly): each CTA takes its sequence's
+// decision once that sequence's partials are in, and the last CTA waits for
+// the stream to complete before exiting, so that this kernel's completion
+// covers the stream's for the kernels after it.
+constexpr int kSampleDecideThreads = 256;
 
 template <int ELT>
-__global__ void __launch_bounds__(kSampleDecideThreads) sample_decide_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kSampleDecideThreads, 5) sample_decide_kernel(const VerifyArgs a) {
     __shared__ SampleDecideSmem dsm;
     pdl_trigger();
     const int k = decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
     write_sample_decision<kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, k, dsm);
+    if (a.poll_parts && blockIdx.x == gridDim.x - 1) pdl_wait();
 }
 
 // Per (chunk, sequence): the sums of the exponentials of target row k and
@@ -68,8 +73,13 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
     __shared__ FinalSmem sm;
     const int b = blockIdx.x / a.C, c = blockIdx.x - b * a.C;   // chunks of a sequence adjacent
     pdl_trigger();
-    pdl_wait();
-    const SampleDesc d = a.desc[b];
+    // The last CTA waits for the decide kernel to complete, so that this
+    // kernel's completion covers it; the others start on their sequence as
+    // soon as its SampleDesc of this call is published.
+    if (blockIdx.x == gridDim.x - 1) pdl_wait();
+    if (threadIdx.x == 0) sm.desc = wait_desc(a, b);
+    __syncthreads();
+    const SampleDesc d = sm.desc;
     if (d.k < 0) return;
     // the final token's uniform, loaded now so that its latency is not the search's
     const float u = a.u[(size_t)b * (a.gamma + 1) + a.gamma];
@@ -77,14 +87,11 @@ __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a
         const FinalRows f = final_rows<ELT>(a, b, d);
         segment_sums_global<ELT, VEC>(a, f, b, c * kCW + (threadIdx.x >> 5), d.rt, threadIdx.x & 31);
     }
-    // The CTA's sums, ordered before the ticket by the barrier, are published
-    // at gpu scope by the ticket thread's fence (the pattern of a grid-wide
-    // barrier: bar.sync, then one thread fences and increments).
+    // The last of the sequence's chunk CTAs to take a ticket runs the
+    // search; it waits there for any other chunk's tagged sums still on
+    // their way.
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        sm.mine = take_ticket(&a.tick[b]) == (unsigned)(a.C - 1);
-    }
+    if (threadIdx.x == 0) sm.mine = take_ticket(a, b) == (unsigned)(a.C - 1);
     __syncthreads();
     if (!sm.mine) return;
     search_sequence<ELT, VEC>(a, b, d, u, sm, threadIdx.x);
@@ -206,8 +213,7 @@ __global__ void __launch_bounds__(kLazyDecideThreads) lazy_decide_kernel(const V
         d.mt = k >= 0 ? sm.M[k - lo] : 0.f;
         d.md = (k >= 0 && k < a.gamma) ? sm.M[nt + k - lo] : 0.f;
         d.rt = (k >= 0 && k < a.gamma) ? expf(sm.lnZ[k - lo] - sm.lnZ[nt + k - lo]) : 0.f;   // as the decide step
-        a.desc[b] = d;
-        a.tick[b] = 0u;
+        publish_desc(a, b, d);
     }
     // accepted drafts and padding; slot k belongs to the final-pass search
     for (int i = gt; i <= a.gamma; i += kLazyDecideThreads)
@@ -329,13 +335,32 @@ static cudaError_t launch_lazy(VerifyArgs a, const DeviceInfo& di, cudaStream_t 
 }
 
 // ---------------------------------------------------------------- launch
+// The decide and final-pass kernels prefer the whole carveout as shared
+// memory, as the ring stream does: SMs that hold stream CTAs can then take
+// theirs too (an SM runs CTAs of several kernels only under one carveout).
+template <typename K>
+static cudaError_t prefer_max_shared(K kfn, DeviceSlots& slots) {
+    int unused = 0;
+    return device_once(slots, &unused, [&](int, int* o) {
+        *o = 1;
+        return cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
+    });
+}
+
 template <int ELT, bool VEC>
 static cudaError_t launch_final_t(const VerifyArgs& a, cudaStream_t st, bool decide = true) {
     cudaError_t e = cudaSuccess;
     if (decide) {
+        static DeviceSlots dslots = {};
+        e = prefer_max_shared(sample_decide_kernel<ELT>, dslots);
+        if (e != cudaSuccess) return e;
         e = launch_pdl(sample_decide_kernel<ELT>, dim3(a.B), kSampleDecideThreads, 0, st, a);
         if (e != cudaSuccess) return e;
     }
+    static DeviceSlots fslots = {};
+    e = prefer_max_shared(sample_final_kernel<ELT, VEC>, fslots);
+    if (e != cudaSuccess) return e;
     return launch_pdl(sample_final_kernel<ELT, VEC>, dim3((unsigned)a.C * (unsigned)a.B), kCT, 0, st,
                       a);
 }
@@ -371,10 +396,11 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
     a.B = B;
     a.C = final_chunks(V);
     a.parts = reinterpret_cast<float2*>(w + L.part_off);
-    a.desc = reinterpret_cast<SampleDesc*>(w + L.desc_off);
-    a.tick = reinterpret_cast<unsigned*>(w + L.tick_off);
-    a.zsum = reinterpret_cast<float4*>(w + L.zsum_off);
-    a.wsum = reinterpret_cast<float4*>(w + L.wsum_off);
+    a.desc = reinterpret_cast<unsigned long long*>(w + L.desc_off);
+    a.epoch = next_launch_tag();
+    a.ptag = (uint32_t)a.epoch ? (uint32_t)a.epoch : 1u;
+    a.tick = reinterpret_cast<unsigned long long*>(w + L.tick_off);
+    a.sums = reinterpret_cast<unsigned long long*>(w + L.sum_off);
     a.err = reinterpret_cast<int*>(w + L.err_off);
     a.out_tok = out_tok;
     a.out_acc = out_acc;
@@ -393,6 +419,9 @@ cudaError_t launch_sample(const void* zt, const void* zd, spec_dtype_t dt, const
         a.early_inputs = 1;
         mask_lp = out_lp != nullptr;
     }
+    // A whole call on 16-byte rows: the decide kernel runs beside the ring
+    // stream and waits for each sequence's tagged partials.
+    a.poll_parts = (parts & kSampleStats) && (parts & kSampleFinish) && vec ? 1 : 0;
     if (parts & kSampleStats) {
         e = elt == 2 ? launch_stream<2, kModeSample>(a, di, st) : launch_stream<4, kModeSample>(a, di, st);
         if (e != cudaSuccess) return e;

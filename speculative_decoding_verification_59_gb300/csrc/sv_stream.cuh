@@ -400,6 +400,14 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
     thr = fmaxf(thr, ov[K - 1]);                          // more than 2K marked: K of them reach it
 }
 
+// A sampling partial (m, s) stored as a pair of tagged words (sv_common.cuh),
+// so that the decide kernel, running beside the stream, can tell a partial of
+// this call from an older one without any fence.
+__device__ __forceinline__ void store_tagged_part(const VerifyArgs& a, size_t i, float2 v) {
+    st_tagged2(reinterpret_cast<unsigned long long*>(a.parts) + 2 * i, __float_as_uint(v.x),
+               __float_as_uint(v.y), a.ptag);
+}
+
 // Stage marker of the end of a CTA's chunks.
 constexpr unsigned kNoChunk = 0xffffffffu;
 
@@ -419,15 +427,20 @@ constexpr unsigned kNoChunk = 0xffffffffu;
 // except after the process's tag count wrapped (once in 2^40 launches), when
 // the first claim that finds an older tag installs this one by compare-and-swap.
 struct ChunkSource {
-    unsigned s, s_end, total, first_dyn;
+    unsigned s, s_end, step, total, first_dyn;
     bool dyn, have;
     unsigned long long* ctr;
     unsigned long long tag, pending;
     uint32_t limit;
     int* err;
 
-    __device__ __forceinline__ ChunkSource(const VerifyArgs& a, unsigned total_) {
+    // round_robin: the static share is dealt chunk by chunk (CTA i takes
+    // chunks i, i + G, i + 2G, ... of G CTAs), so the stream advances through
+    // the chunks -- and the sequences -- in index order; otherwise each CTA
+    // takes a contiguous range.
+    __device__ __forceinline__ ChunkSource(const VerifyArgs& a, unsigned total_, bool round_robin) {
         total = total_;
+        step = 1;
         ctr = a.claim;
         tag = a.claim_tag;
         limit = a.wait_limit;
@@ -438,8 +451,14 @@ struct ChunkSource {
         dyn = q >= 2 && total < (1u << (kClaimIdxBits - 1));
         if (dyn) {
             first_dyn = q * gridDim.x;
-            s = blockIdx.x * q;
-            s_end = s + q;
+            if (round_robin) {
+                s = blockIdx.x;
+                step = gridDim.x;
+                s_end = blockIdx.x + q * gridDim.x;
+            } else {
+                s = blockIdx.x * q;
+                s_end = s + q;
+            }
             asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(ctr), "l"(tag | first_dyn)
                          : "memory");
         } else {
@@ -479,8 +498,9 @@ struct ChunkSource {
     // The next chunk index, kNoChunk at the end.
     __device__ __forceinline__ unsigned next() {
         if (s < s_end) {
-            const unsigned c = s++;
-            if (s == s_end && dyn) claim();
+            const unsigned c = s;
+            s += step;
+            if (s >= s_end && dyn) claim();
             return c;
         }
         if (!have) return kNoChunk;
@@ -495,7 +515,7 @@ struct ChunkSource {
 };
 
 template <int ELT, int MODE>
-__global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const VerifyArgs a) {
+__device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
     __shared__ unsigned stage_chunk[kStages];          // chunk index each stage holds
@@ -513,6 +533,10 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
     }
     __syncthreads();
     pdl_wait();                 // the kernel before may still read this workspace or write the rows
+    // Sampling: the decide kernel may start now.  It runs beside the stream
+    // and takes each sequence's decision once that sequence's partials all
+    // carry this call's tag.
+    if (MODE == kModeSample && threadIdx.x == 0) pdl_trigger();
     unsigned total = (unsigned)a.total_chunks;
     if constexpr (MODE == kModeLazy) {
         if (a.lz_count) total = (unsigned)__ldcg(a.lz_count) * (unsigned)(a.lz_nt + a.lz_nd) * (unsigned)a.nseg;
@@ -524,9 +548,9 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         // ---- producer: one lane issues the bulk copies and hands each
         // stage's chunk index to the consumers (kNoChunk ends the stream)
         if (lane == 0) {
-            ChunkSource src(a, total);
+            ChunkSource src(a, total, MODE == kModeSample);
             unsigned issued = 0;
-            bool ok = true, ended = false, triggered = false;
+            bool ok = true, ended = false, triggered = MODE == kModeSample;
             for (;; ++issued) {
                 const int st = (int)(issued % kStages);
                 const unsigned use = issued / kStages;
@@ -544,7 +568,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
                 const size_t off = (size_t)seg * kStageBytes;
                 const uint32_t bytes = (uint32_t)min((size_t)kStageBytes, rowbytes - off);
                 const unsigned pr = rows.part_row<MODE>(a, rr);
-                if (!triggered && src.s == src.s_end) {
+                if (!triggered && src.s >= src.s_end) {
                     // static share issued: the next kernel may start launching
                     pdl_trigger();
                     triggered = true;
@@ -622,10 +646,24 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const Veri
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&empty[st]);
-            if constexpr (KT == 0) a.parts[(size_t)pr * P + seg * kWarps + cw] = part;
+            if constexpr (MODE == kModeSample) store_tagged_part(a, (size_t)pr * P + seg * kWarps + cw, part);
+            else if constexpr (KT == 0) a.parts[(size_t)pr * P + seg * kWarps + cw] = part;
         }
     }
     if (!ok && lane == 0) atomicOr(a.err, SPEC_DEVERR_TIMEOUT);
+}
+
+template <int ELT, int MODE>
+__global__ void __launch_bounds__(kRingThreads, 2) ring_stream_kernel(const VerifyArgs a) {
+    ring_stream_body<ELT, MODE>(a);
+}
+
+// The sampling stream, held to 64 registers a thread: two of its CTAs, a
+// decide CTA and a final-pass CTA then fit on one SM's registers together,
+// as they run in a whole sampling call.
+template <int ELT>
+__global__ void __maxnreg__(64) ring_sample_kernel(const VerifyArgs a) {
+    ring_stream_body<ELT, kModeSample>(a);
 }
 
 template <int ELT, bool VEC, int MODE>
@@ -730,7 +768,10 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
             }
             part = make_float2(bv, __int_as_float(bi));
         }
-        if (lane == 0) a.parts[(size_t)rr * P + seg * kWarps + warp] = part;
+        if (lane == 0) {
+            if constexpr (MODE == kModeSample) store_tagged_part(a, (size_t)rr * P + seg * kWarps + warp, part);
+            else a.parts[(size_t)rr * P + seg * kWarps + warp] = part;
+        }
     }
 }
 
@@ -742,13 +783,18 @@ cudaError_t launch_stream(const VerifyArgs& args, const DeviceInfo& di, cudaStre
     a.claim = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(a.err) + kClaimOff);
     a.claim_tag = next_launch_tag() << kClaimIdxBits;
     if (((size_t)a.V * ELT) % 16 == 0) {
-        auto kfn = ring_stream_kernel<ELT, MODE>;
+        auto kfn = MODE == kModeSample ? ring_sample_kernel<ELT> : ring_stream_kernel<ELT, MODE>;
         const int smem = kStages * kStageBytes;
         // once per device: the shared-memory opt-in, then the occupancy it allows
         static DeviceSlots slots = {};
         int occ = 0;
         cudaError_t e = device_once(slots, &occ, [&](int, int* o) {
             cudaError_t r = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (r != cudaSuccess) return r;
+            // the whole carveout as shared memory, as the kernels that run
+            // beside this one prefer it too, so an SM can hold both
+            r = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
             if (r != cudaSuccess) return r;
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(o, kfn, kRingThreads, smem);
         });
