@@ -470,7 +470,7 @@ def run_own(args):
             "rounds_per_s": job_rate(world, x.B, K, ms_max),
             "tau": {"sample": tau_sample, "greedy": tau_greedy},
             "roofline": {
-                "kernel": "ring_stream_kernel<bf16, sample> (spec_verify_sample_stats)",
+                "kernel": "ring_sample_kernel<bf16> (spec_verify_sample_stats)",
                 "bound": "hbm",
                 "achieved": achieved,
                 "peak": peak,
