@@ -315,12 +315,12 @@ spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype
  * results are those of spec_verify_sample without the workspace; the same
  * kernels run.  The call allocates nothing and calls no allocating routine.
  *
- * Scratch: a fixed array of SPEC_VERIFY_NOALLOC_SCRATCH_BYTES (4 MiB) that the
+ * Scratch: a fixed array of SPEC_VERIFY_NOALLOC_SCRATCH_BYTES (8 MiB) that the
  * library places in the device memory of every GPU it is loaded on, held
  * until the process exits.  Problems whose scratch need,
  * spec_verify_workspace_size(B, gamma, V), exceeds it are rejected with
  * SPEC_ERR_EXCEEDS_STATIC_SCRATCH before anything is launched (B = 256
- * sequences of 4 drafts over 128256 fp32 logits need 3.4 MB).
+ * sequences of 4 drafts over 128256 fp32 logits need 6.8 MB).
  *
  * The first call on each device, made while that device is current, looks up
  * the array's device address (cudaGetSymbolAddress, which may also load the
@@ -333,7 +333,7 @@ spec_status_t spec_cosine_topk(const void* hidden, const void* query, spec_dtype
  * Bad input is reported per sequence (num_accepted = -1, tokens -1) only: the
  * device error word of the workspace calls is not readable for this entry.
  */
-#define SPEC_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+#define SPEC_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 spec_status_t spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
                                          spec_dtype_t dtype, const int32_t* draft_tokens,
                                          const float* uniforms, float temperature, int B,

@@ -30,7 +30,7 @@ SPEC_ERR_WORKSPACE_TOO_SMALL = 4
 SPEC_ERR_CUDA = 5
 SPEC_ERR_DEVICE_INPUT = 6
 SPEC_ERR_EXCEEDS_STATIC_SCRATCH = 7
-SPEC_VERIFY_NOALLOC_SCRATCH_BYTES = 4 << 20
+SPEC_VERIFY_NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
 SPEC_DEVERR_TOKEN_RANGE = 1

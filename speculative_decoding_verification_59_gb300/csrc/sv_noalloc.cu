@@ -7,7 +7,7 @@
 // allowed to call cudaMalloc/cudaFree (both can synchronise the device) in
 // the middle of a step.  For them this entry point runs exactly the kernels
 // of spec_verify_sample, with the scratch taken from a fixed array that the
-// library itself places in device memory (kNoAllocScratchBytes, 4 MiB).
+// library itself places in device memory (kNoAllocScratchBytes, 8 MiB).
 // Every GPU that loads the library holds that array until the process exits.
 //
 // The array's host-side name is only a stand-in; its device address is looked

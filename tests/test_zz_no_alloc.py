@@ -49,7 +49,7 @@ def test_noalloc_matches_workspace_entry_point_twice(sv):
     accept counts equal, log-probabilities within the 1e-5 relative bar of
     the parity tests (the same kernels run, so they are in fact identical)."""
     stream = torch.cuda.current_stream().cuda_stream
-    cases = [W.make_chain("chain-b64", B=8, V=151936), W.make_chain("chain-b256", B=16, V=128256)]
+    cases = [W.make_chain("chain-b64", B=8, V=151936), W.make_chain("chain-b256", B=256, V=128256)]
     for x in cases:
         zt, zd, xt, u = _inputs(x)
         need = sv.spec_verify_workspace_size(x.B, x.gamma, x.V)
