@@ -1,8 +1,7 @@
 // The final sample of stochastic verification: the sums of the exponentials
 // of one target row (and, after a rejection, one draft row) over 1024-element
-// segments, and the inverse-CDF search over those segment sums.  Shared by
-// the standalone final-pass kernel (sv_sample.cu) and the consumer warps of
-// the fused sampling kernel (sv_fused.cu).
+// segments, and the inverse-CDF search over those segment sums, for the
+// final-pass kernel (sv_sample.cu).
 //
 // Source: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", section "What happens in one round", step 4 (after a
@@ -10,10 +9,8 @@
 // bonus token from p_gamma), and section "Why fixing wrong guesses does not
 // leave the target distribution" (residual p'(x) = norm(max(0, p(x) - q(x)))).
 //
-// Every function here runs in a group of kCT = 256 threads (tid 0..255) that
-// synchronises on named barrier 1 (fin_sync): a whole final-pass CTA, or the
-// eight consumer warps of a fused-kernel CTA, whose producer warp never joins
-// that barrier.
+// Every group function here runs in a final-pass CTA of kCT = 256 threads
+// (tid 0..255), which synchronises on named barrier 1 (fin_sync).
 #pragma once
 
 #include "sv_stream.cuh"
@@ -235,9 +232,7 @@ __device__ __forceinline__ void fin_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // 16-byte vectors (vector h of lane l starts at element j0 + (l + 32 h) 16/ELT),
 // so every load instruction of a warp reads 512 contiguous bytes.  ldA(j) and
 // ldB(j) return the 16-byte vector of the target and draft row starting at
-// element j (-inf at or past V): plain global loads in the final-pass kernel,
-// shared-memory stages in the fused kernel -- the same values either way, and
-// the same arithmetic in the same order, so both give the same bits.
+// element j (-inf at or past V).
 // Per segment: za = sum ea, and after a rejection zb = sum eb, w = sum max(0,
 // ea - rt eb) at the approximate normaliser ratio rt, and dd = sum of eb over
 // the elements with ea > rt eb -- minus the slope of w in the ratio.  The

@@ -13,19 +13,23 @@
 // of every sequence from the single row pair it comes from -- target and
 // draft row k after a rejection at k (weights max(0, p_k - q_k)), target row
 // gamma when every draft was accepted (weights p_gamma) -- by inverse CDF in
-// index order.  Two kernels, chained with programmatic dependent launch,
-// keep every sequence in flight at once:
+// index order.  Two kernels, launched with programmatic dependent launch,
+// keep every sequence in flight at once; in a whole sampling call both start
+// with the pass-1 stream and work beside it, each on a sequence as soon as
+// that sequence's data carries the call's tag (tagged words, sv_common.cuh):
 //   sample_decide_kernel  one CTA per sequence: row statistics from the
 //                         partials, the accept decisions, every output but
 //                         the final token, and the approximate normaliser
-//                         ratio rt = Z_t/Z_d of row k from those statistics;
+//                         ratio rt = Z_t/Z_d of row k from those statistics,
+//                         published in the tagged SampleDesc;
 //   sample_final_kernel   one CTA per 8192-element chunk of row k, one warp
 //                         per 1024-element segment: sums of the exponentials
 //                         of the target and draft segment and, after a
 //                         rejection, the residual sum at ratio rt with its
-//                         slope.  The sequence's last chunk CTA to finish (a
-//                         ticket count) then runs the search: the exact ratio
-//                         R from the exponential sums, the segment residual
+//                         slope, stored as tagged words.  The sequence's
+//                         chunk CTA that takes the last ticket (a tagged
+//                         count) then runs the search: the exact ratio R
+//                         from the exponential sums, the segment residual
 //                         sums moved from rt to R to first order, prefix over
 //                         them, the owning segment, its 1024 weights
 //                         recomputed at R and scanned, the owning element.
@@ -57,7 +61,7 @@ template <int ELT>
 __global__ void __launch_bounds__(kSampleDecideThreads, 5) sample_decide_kernel(const VerifyArgs a) {
     __shared__ SampleDecideSmem dsm;
     pdl_trigger();
-    const int k = decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for the stream's partials
+    const int k = decide_sample<ELT, kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, dsm);  // waits for its partials
     write_sample_decision<kSampleDecideThreads>(a, blockIdx.x, threadIdx.x, k, dsm);
     if (a.poll_parts && blockIdx.x == gridDim.x - 1) pdl_wait();
 }
@@ -65,9 +69,9 @@ __global__ void __launch_bounds__(kSampleDecideThreads, 5) sample_decide_kernel(
 // Per (chunk, sequence): the sums of the exponentials of target row k and
 // (after a rejection) draft row k over each of the chunk's segments, and the
 // residual sums at the approximate ratio with their slopes; then, in the
-// last of the sequence's C chunk CTAs to finish, the search.  The decide
-// kernel (or the lazy pass) zeroes the sequence's ticket count before this
-// kernel's wait returns.
+// last of the sequence's C chunk CTAs to take a ticket, the search.  Each CTA
+// starts once its sequence's SampleDesc of this call is published (by the
+// decide kernel or the lazy pass).
 template <int ELT, bool VEC>
 __global__ void __launch_bounds__(kCT, 4) sample_final_kernel(const VerifyArgs a) {
     __shared__ FinalSmem sm;
