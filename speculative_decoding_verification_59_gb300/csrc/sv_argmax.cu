@@ -1,7 +1,9 @@
 // Greedy verification of draft chains and of draft trees: one streaming
-// argmax pass over the target logits (sv_stream.cuh), then one CTA per
-// sequence that merges its row partials and decides (sv_decide.cuh), chained
-// with programmatic dependent launch.
+// argmax pass over the target logits (sv_stream.cuh), and one CTA per
+// sequence that merges its row partials and decides (sv_decide.cuh).  On
+// 16-byte rows the decide kernel starts with the stream and runs beside it,
+// taking each sequence once that sequence's (tagged) partials are in; on other
+// rows it follows the stream with programmatic dependent launch.
 //
 // Sources: "Speculative decoding: guess a few tokens first - why the answer
 // stays the same", greedy paragraph (accept while the draft equals the target
@@ -16,28 +18,52 @@
 
 namespace sv {
 
-// One CTA per sequence, chained behind the argmax stream (waits in hardware
-// until the stream's partials are visible).  32 warps: a row's partials per
-// warp and round of loads (a 36-node tree takes two rounds).
+// One CTA per sequence.  Beside the stream: 8 warps of at most 80 registers
+// (one CTA fits on an SM with two argmax-stream CTAs), waiting for the
+// sequence's tagged partials; the last CTA then waits for the stream to
+// complete, so that this kernel's completion covers it.  Behind the stream
+// (rows that take the register path, trees of more than 32 nodes): 32 warps,
+// a row's partials per warp and round of loads, after the stream completes.
 constexpr int kArgmaxDecideThreads = 1024;
+constexpr int kArgmaxBesideThreads = 256;
 
-__global__ void __launch_bounds__(kArgmaxDecideThreads) greedy_decide_kernel(const VerifyArgs a) {
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == kArgmaxBesideThreads ? 3 : 1) greedy_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
-    prefetch_tokens<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
-    pdl_wait();
-    decide_greedy<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm);
+    prefetch_tokens<NT>(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
+    if (a.poll_parts) wait_seq_parts<NT>(a, blockIdx.x, threadIdx.x);
+    else pdl_wait();
+    decide_greedy<NT>(a, blockIdx.x, threadIdx.x, sm);
+    if (a.poll_parts && blockIdx.x == gridDim.x - 1) pdl_wait();
 }
 
-__global__ void __launch_bounds__(kArgmaxDecideThreads) tree_decide_kernel(const VerifyArgs a) {
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == kArgmaxBesideThreads ? 3 : 1) tree_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
     __shared__ TreeWalkSmem tw;
-    prefetch_tokens<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, true, sm);
-    pdl_wait();
-    decide_tree<kArgmaxDecideThreads>(a, blockIdx.x, threadIdx.x, sm, tw);
+    prefetch_tokens<NT>(a, blockIdx.x, threadIdx.x, true, sm);
+    if (a.poll_parts) wait_seq_parts<NT>(a, blockIdx.x, threadIdx.x);
+    else pdl_wait();
+    decide_tree<NT>(a, blockIdx.x, threadIdx.x, sm, tw);
+    if (a.poll_parts && blockIdx.x == gridDim.x - 1) pdl_wait();
 }
 
-static cudaError_t launch_decide(void (*kfn)(VerifyArgs), const VerifyArgs& a, int B, cudaStream_t st) {
-    return launch_pdl(kfn, dim3(B), kArgmaxDecideThreads, 0, st, a);
+// The decide kernel beside the stream prefers the whole carveout as shared
+// memory, as the ring stream does: an SM runs CTAs of several kernels only
+// under one carveout.
+template <int NT>
+static cudaError_t launch_decide(void (*kfn)(VerifyArgs), const VerifyArgs& a, int B, cudaStream_t st,
+                                 DeviceSlots& slots) {
+    if (NT == kArgmaxBesideThreads) {
+        int unused = 0;
+        cudaError_t e = device_once(slots, &unused, [&](int, int* o) {
+            *o = 1;
+            return cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared);
+        });
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(kfn, dim3(B), NT, 0, st, a);
 }
 
 static VerifyArgs argmax_args(const void* zt, int elt, int B, int rows, int V, void* ws) {
@@ -53,6 +79,9 @@ static VerifyArgs argmax_args(const void* zt, int elt, int B, int rows, int V, v
     a.B = B;
     a.parts = reinterpret_cast<float2*>(w + L.part_off);
     a.err = reinterpret_cast<int*>(w + L.err_off);
+    const uint64_t tag = next_launch_tag();
+    a.ptag = (uint32_t)tag ? (uint32_t)tag : 1u;
+    a.poll_parts = ((size_t)V * elt) % 16 == 0 ? 1 : 0;  // ring stream: the decide runs beside it
     return a;
 }
 
@@ -69,7 +98,10 @@ cudaError_t launch_greedy(const void* zt, spec_dtype_t dt, const int32_t* x, int
     a.out_acc = out_acc;
     e = elt == 2 ? launch_stream<2, kModeGreedy>(a, di, st) : launch_stream<4, kModeGreedy>(a, di, st);
     if (e != cudaSuccess) return e;
-    return launch_decide(greedy_decide_kernel, a, B, st);
+    static DeviceSlots slots = {};
+    if (a.poll_parts)
+        return launch_decide<kArgmaxBesideThreads>(greedy_decide_kernel<kArgmaxBesideThreads>, a, B, st, slots);
+    return launch_decide<kArgmaxDecideThreads>(greedy_decide_kernel<kArgmaxDecideThreads>, a, B, st, slots);
 }
 
 cudaError_t launch_tree(const void* zt, spec_dtype_t dt, const int32_t* tok, const int32_t* par,
@@ -85,9 +117,16 @@ cudaError_t launch_tree(const void* zt, spec_dtype_t dt, const int32_t* tok, con
     a.out_nodes = out_nodes;
     a.out_tok = out_tok;
     a.out_acc = out_acc;
+    // Beside the stream only while the 8 warps merge every row in one round
+    // (four rows a warp): larger trees are decided faster by 32 warps after
+    // the stream (a 36-node tree: 56.5 against 58.1 us per call).
+    if (N > 4 * kArgmaxBesideThreads / 32) a.poll_parts = 0;
     e = elt == 2 ? launch_stream<2, kModeTree>(a, di, st) : launch_stream<4, kModeTree>(a, di, st);
     if (e != cudaSuccess) return e;
-    return launch_decide(tree_decide_kernel, a, B, st);
+    static DeviceSlots slots = {};
+    if (a.poll_parts)
+        return launch_decide<kArgmaxBesideThreads>(tree_decide_kernel<kArgmaxBesideThreads>, a, B, st, slots);
+    return launch_decide<kArgmaxDecideThreads>(tree_decide_kernel<kArgmaxDecideThreads>, a, B, st, slots);
 }
 
 }  // namespace sv

@@ -473,7 +473,7 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
     constexpr int NW = NT / 32;
     const int P = a.nseg * kWarps, np = P;              // row stride and partials
     const int R = a.rows_per_seq;
-    const float2* base = a.parts + (size_t)b * R * P;
+    const size_t base = (size_t)b * R * P;                // the row partials, tagged pairs
     if (np <= 32) {
         int G = 1;
         while (G < np) G <<= 1;
@@ -483,7 +483,7 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
             float bv = kNegInf;
             int bi = 0x7fffffff;
             if (r < R && li < np) {
-                const float2 q = __ldcg(base + (size_t)r * P + li);
+                const float2 q = load_part<true>(a, base + (size_t)r * P + li);
                 bv = q.x;
                 bi = __float_as_int(q.y);
             }
@@ -496,7 +496,7 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
         }
     } else if (!MANY_ROWS || R <= NW) {                   // a row per warp and round
         for (int r = gw; r < R; r += NW) {
-            const float2* pr = base + (size_t)r * P;
+            const size_t pr = base + (size_t)r * P;
             float bv = kNegInf;
             int bi = 0x7fffffff;
             constexpr int kHeld = 4;                       // loads in flight per lane
@@ -505,7 +505,7 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
 #pragma unroll
                 for (int h = 0; h < kHeld; ++h) {
                     const int p = p0 + 32 * h;
-                    q[h] = p < np ? __ldcg(&pr[p]) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+                    q[h] = p < np ? load_part<true>(a, pr + p) : make_float2(kNegInf, __int_as_float(0x7fffffff));
                 }
 #pragma unroll
                 for (int h = 0; h < kHeld; ++h) {
@@ -530,7 +530,7 @@ __device__ __forceinline__ void merge_argmax_rows(const VerifyArgs& a, int b, in
 #pragma unroll
                     for (int h = 0; h < kHeld; ++h) {
                         const int r = r0 + NW * j, p = p0 + 32 * h;
-                        q[j][h] = (r < R && p < np) ? __ldcg(base + (size_t)r * P + p)
+                        q[j][h] = (r < R && p < np) ? load_part<true>(a, base + (size_t)r * P + p)
                                                     : make_float2(kNegInf, __int_as_float(0x7fffffff));
                     }
 #pragma unroll

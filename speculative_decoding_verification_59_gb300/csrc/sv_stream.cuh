@@ -400,9 +400,10 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
     thr = fmaxf(thr, ov[K - 1]);                          // more than 2K marked: K of them reach it
 }
 
-// A sampling partial (m, s) stored as a pair of tagged words (sv_common.cuh),
-// so that the decide kernel, running beside the stream, can tell a partial of
-// this call from an older one without any fence.
+// A partial of a sampling, greedy or tree stream -- (m, s), or (value,
+// index) -- stored as a pair of tagged words (sv_common.cuh), so that the
+// decide kernel, running beside the stream, can tell a partial of this call
+// from an older one without any fence.
 __device__ __forceinline__ void store_tagged_part(const VerifyArgs& a, size_t i, float2 v) {
     st_tagged2(reinterpret_cast<unsigned long long*>(a.parts) + 2 * i, __float_as_uint(v.x),
                __float_as_uint(v.y), a.ptag);
@@ -533,10 +534,11 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     }
     __syncthreads();
     pdl_wait();                 // the kernel before may still read this workspace or write the rows
-    // Sampling: the decide kernel may start now.  It runs beside the stream
-    // and takes each sequence's decision once that sequence's partials all
-    // carry this call's tag.
-    if (MODE == kModeSample && threadIdx.x == 0) pdl_trigger();
+    // Sampling, greedy and tree verification: the decide kernel may start
+    // now.  It runs beside the stream and takes each sequence's decision once
+    // that sequence's partials all carry this call's tag.
+    constexpr bool kBeside = MODE == kModeSample || MODE == kModeGreedy || MODE == kModeTree;
+    if (kBeside && threadIdx.x == 0) pdl_trigger();
     unsigned total = (unsigned)a.total_chunks;
     if constexpr (MODE == kModeLazy) {
         if (a.lz_count) total = (unsigned)__ldcg(a.lz_count) * (unsigned)(a.lz_nt + a.lz_nd) * (unsigned)a.nseg;
@@ -548,9 +550,9 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
         // ---- producer: one lane issues the bulk copies and hands each
         // stage's chunk index to the consumers (kNoChunk ends the stream)
         if (lane == 0) {
-            ChunkSource src(a, total, MODE == kModeSample);
+            ChunkSource src(a, total, kBeside);
             unsigned issued = 0;
-            bool ok = true, ended = false, triggered = MODE == kModeSample;
+            bool ok = true, ended = false, triggered = kBeside;
             for (;; ++issued) {
                 const int st = (int)(issued % kStages);
                 const unsigned use = issued / kStages;
@@ -646,7 +648,7 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&empty[st]);
-            if constexpr (MODE == kModeSample) store_tagged_part(a, (size_t)pr * P + seg * kWarps + cw, part);
+            if constexpr (kBeside) store_tagged_part(a, (size_t)pr * P + seg * kWarps + cw, part);
             else if constexpr (KT == 0) a.parts[(size_t)pr * P + seg * kWarps + cw] = part;
         }
     }
@@ -769,7 +771,8 @@ __global__ void __launch_bounds__(kThreads) reg_stream_kernel(const VerifyArgs a
             part = make_float2(bv, __int_as_float(bi));
         }
         if (lane == 0) {
-            if constexpr (MODE == kModeSample) store_tagged_part(a, (size_t)rr * P + seg * kWarps + warp, part);
+            if constexpr (MODE == kModeSample || MODE == kModeGreedy || MODE == kModeTree)
+                store_tagged_part(a, (size_t)rr * P + seg * kWarps + warp, part);
             else a.parts[(size_t)rr * P + seg * kWarps + warp] = part;
         }
     }
