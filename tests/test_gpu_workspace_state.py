@@ -99,6 +99,27 @@ def test_greedy_after_spoiled_workspace(sv, fill):
         assert ws.read_error() == 0
 
 
+def tree(sv, t, ws):
+    out = sv.verify_tree_greedy(dev_logits(t.target, t.dtype), dev(t.node_tokens), dev(t.parents),
+                                workspace=ws)
+    torch.cuda.synchronize()
+    return [q.cpu() for q in out]
+
+
+@pytest.mark.parametrize("fill", [0xFF, "random"])
+def test_tree_after_spoiled_workspace(sv, fill):
+    """Trees decided beside the stream (up to 32 nodes) and after it (more)."""
+    for kw in (dict(B=6, V=30000, depth=3, branches=1), dict(B=4, V=30000),
+               dict(B=3, V=151936, depth=2, branches=0)):
+        t = W.make_tree("tree-b32", **kw)
+        ref = tree(sv, t, sv.Workspace())
+        ws = sv.Workspace()
+        ws.get(t.B, t.N, t.V)
+        spoil(ws, fill)
+        assert same(ref, tree(sv, t, ws)), (kw, fill)
+        assert ws.read_error() == 0
+
+
 def test_one_workspace_across_shapes_and_modes(sv):
     """One workspace, calls of changing shape and mode in turn: each result
     equals the same call on a fresh workspace."""
