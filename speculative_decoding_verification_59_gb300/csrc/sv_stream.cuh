@@ -230,6 +230,22 @@ __device__ __forceinline__ float2 warp_argmax_chunk(const uint4 (&v)[kVecPerLane
     return make_float2(m + 0.0f, __int_as_float(bi));
 }
 
+// Bit e set for every element e of a bfloat16 vector that is >= the bf16 value
+// in both halves of t2.  A packed compare gives 0xffff per element that
+// reaches it; byte-permutes keep one byte per element (elements 0-3, then
+// 4-7), each masked to its own bit, and a multiply by 0x01010101 adds the
+// four bytes into the top byte (every bit distinct, so no carries).
+__device__ __forceinline__ unsigned vec_ge_bits_bf16(const uint4& q, uint32_t t2) {
+    uint32_t m0, m1, m2, m3;
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(q.x), "r"(t2));
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(q.y), "r"(t2));
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(q.z), "r"(t2));
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(m3) : "r"(q.w), "r"(t2));
+    const uint32_t x = __byte_perm(m0, m1, 0x6420);
+    const uint32_t y = __byte_perm(m2, m3, 0x6420);
+    return ((x & 0x08040201u) | (y & 0x80402010u)) * 0x01010101u >> 24;
+}
+
 // ---- top-K lists (branch tokens of a draft tree) -----------------------------
 // The K best (value, index) pairs seen by a lane, best first: larger value
 // first, lower index first among equal values (am_better).  Empty slots hold
@@ -288,15 +304,15 @@ __host__ __device__ constexpr int topk_slots(int K) { return 2 * K; }
 // chunk of a row (have_thr false) the K-th largest of the 32 lane maxima
 // (K distinct elements of the row), afterwards the bound carried from the
 // warp's earlier chunks of the same row, which skips the K warp-max rounds.
-// Only vectors whose maximum reaches thr are opened: each lane marks its
-// elements >= thr in a 64-bit mask (bit 8 t + e for element e of vector t).
-// When the warp marks at most 2K elements (nearly always: a few more than K)
-// they are written as they are, unsorted, into the chunk's 2K slots -- the
-// merge orders them.  Otherwise the lanes insert their marked elements into
-// sorted lists and the warp merges the lists into the chunk's exact top K,
-// whose K-th value then raises thr.  Marked elements are read back from
-// shared memory in one loop, which keeps the kernel's instruction footprint
-// small.
+// Each lane marks its elements >= thr in a 64-bit mask (bit 8 t + e for
+// element e of vector t): for bfloat16 with packed compares of every element,
+// no branch.  When the warp marks at most 2K elements (nearly always: a few
+// more than K) they are written as they are, unsorted, into the chunk's 2K
+// slots -- the merge orders them.  Otherwise the lanes insert their marked
+// elements into sorted lists and the warp merges the lists into the chunk's
+// exact top K, whose K-th value then raises thr.  Marked elements are read
+// back from shared memory in one loop, which keeps the kernel's instruction
+// footprint small.
 template <int ELT, int K>
 __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
                                                 const unsigned char* chunk, int valid_bytes,
@@ -304,15 +320,8 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
     const int lane = threadIdx.x & 31;
     constexpr int PV = 16 / ELT;
     constexpr int KS = topk_slots(K);
-    float vm[kVecPerLane];
-    float lm = kNegInf;
-#pragma unroll
-    for (int t = 0; t < kVecPerLane; ++t) {
-        vm[t] = vec_max_value<ELT>(vec_max_bits<ELT>(v[t]));
-        lm = fmaxf(lm, vm[t]);
-    }
     if (!have_thr) {                                       // warp-uniform
-        float x = lm;
+        float x = lane_max<ELT>(v);
         thr = kNegInf;
 #pragma unroll
         for (int r = 0; r < K; ++r) {
@@ -322,23 +331,36 @@ __device__ __forceinline__ void warp_topk_chunk(const uint4 (&v)[kVecPerLane],
         }
     }
     unsigned long long mask = 0ull;
+    if constexpr (ELT == 2) {
+        // thr is a logit of the row (or -inf), so exact in bfloat16
+        const uint32_t tb = __float_as_uint(thr) >> 16;
+        const uint32_t t2 = tb | (tb << 16);
+        uint32_t lo = 0u, hi = 0u;
 #pragma unroll
-    for (int t = 0; t < kVecPerLane; ++t) {
-        if ((lane + 32 * t) * 16 < valid_bytes && vm[t] >= thr) {
-            unsigned bits = 0u;
-#pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                float y;
-                if constexpr (ELT == 4) {
-                    y = __uint_as_float(u4_get(v[t], e));
-                } else {
-                    const uint32_t w = u4_get(v[t], e >> 1);
-                    y = (e & 1) ? bf16_hi(w) : bf16_lo(w);
-                }
-                bits |= (y >= thr ? 1u : 0u) << e;
-            }
-            mask |= (unsigned long long)bits << (8 * t);
+        for (int t = 0; t < kVecPerLane; ++t) {
+            const uint32_t b = vec_ge_bits_bf16(v[t], t2);
+            if (t < 4) lo |= b << (8 * t);
+            else hi |= b << (8 * (t - 4));
         }
+        mask = (unsigned long long)hi << 32 | lo;
+    } else {
+#pragma unroll
+        for (int t = 0; t < kVecPerLane; ++t) {
+            if (vec_max_value<ELT>(vec_max_bits<ELT>(v[t])) >= thr) {
+                unsigned bits = 0u;
+#pragma unroll
+                for (int e = 0; e < PV; ++e)
+                    bits |= (__uint_as_float(u4_get(v[t], e)) >= thr ? 1u : 0u) << e;
+                mask |= (unsigned long long)bits << (8 * t);
+            }
+        }
+    }
+    if (valid_bytes < 32 * kLaneBytes) {                   // warp-uniform
+        // vectors past the row's end read as -inf in v but hold stale bytes
+        // in shared memory; they reach thr = -inf, so unmark them
+#pragma unroll
+        for (int t = 0; t < kVecPerLane; ++t)
+            if ((lane + 32 * t) * 16 >= valid_bytes) mask &= ~(0xffull << (8 * t));
     }
     auto element = [&](int bit, float* y, int* j) {
         const int t = bit >> 3, e = bit & 7;
@@ -519,7 +541,7 @@ template <int ELT, int MODE>
 __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ unsigned stage_chunk[kStages];          // chunk index each stage holds
+    __shared__ uint4 stage_info[kStages];              // (row, partial row, segment, bytes) a stage holds
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int KT = topk_of(MODE);
     const size_t rowbytes = (size_t)a.V * ELT;
@@ -548,7 +570,8 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
 
     if (warp == 0) {
         // ---- producer: one lane issues the bulk copies and hands each
-        // stage's chunk index to the consumers (kNoChunk ends the stream)
+        // stage's row, partial row, segment and length to the consumers (row
+        // kNoChunk ends the stream), so that they divide no chunk index
         if (lane == 0) {
             ChunkSource src(a, total, kBeside);
             unsigned issued = 0;
@@ -560,7 +583,7 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
                 const unsigned c = src.next();
                 if (c == kNoChunk) {
                     if (!triggered) pdl_trigger();
-                    stage_chunk[st] = kNoChunk;
+                    stage_info[st] = make_uint4(kNoChunk, 0u, 0u, 0u);
                     mbar_arrive(&full[st]);                   // releases the consumers' last wait
                     ended = true;
                     break;
@@ -575,7 +598,7 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
                     pdl_trigger();
                     triggered = true;
                 }
-                stage_chunk[st] = c;
+                stage_info[st] = make_uint4(rr, pr, (unsigned)seg, bytes);
                 mbar_arrive_expect_tx(&full[st], bytes);
                 bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, pr, rowbytes) + off, bytes,
                          &full[st]);
@@ -609,13 +632,14 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
         const int st = (int)(it % kStages);
         if (!wait_bounded(&full[st], (it / kStages) & 1u, a.wait_limit)) ok = false;
         if (!__all_sync(0xffffffffu, ok)) break;
-        const unsigned c = stage_chunk[st];
-        if (c == kNoChunk) break;
-        const unsigned rr = c / (unsigned)a.nseg;
-        const int seg = (int)(c - rr * (unsigned)a.nseg);
-        const unsigned pr = rows.part_row<MODE>(a, rr);
+        // the producer's division of the chunk index, row mapping and length
+        const uint4 si = stage_info[st];
+        const unsigned rr = si.x;
+        if (rr == kNoChunk) break;
+        const unsigned pr = si.y;
+        const int seg = (int)si.z;
         const size_t off = (size_t)seg * kStageBytes;
-        const int bytes = (int)min((size_t)kStageBytes, rowbytes - off);
+        const int bytes = (int)si.w;
         const int wb = bytes - cw * (32 * kLaneBytes);            // valid bytes of this warp chunk
         const bool use = wb > 0;
         float2 part = make_float2(0.f, 0.f);

@@ -21,6 +21,21 @@
 namespace sv {
 
 constexpr int kTopkRowsPerCta = kThreads / 32;
+constexpr int kOnePass = 24;          // candidates a lane holds in registers (640 a row for V = 151936 bf16)
+
+// The KC-th largest of the 32 lanes' x (K rounds of a warp maximum, the
+// lowest lane holding it dropping out), -inf when fewer lanes hold values.
+template <int KC>
+__device__ __forceinline__ float kth_lane_max(float x, int lane) {
+    float thr = kNegInf;
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+        thr = warp_max(x);
+        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
+        if (lane == __ffs(own) - 1) x = kNegInf;
+    }
+    return thr;
+}
 
 template <int KC>
 __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a, int K,
@@ -31,42 +46,54 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kTopkRowsPerCta + (threadIdx.x >> 5);
     if (r >= a.B) return;                                 // warp-uniform
-    // The row's candidates are one contiguous array of n entries.  Pass 1:
-    // each lane's largest; the row's top KC are all at least thr, the KC-th
-    // largest of those 32 maxima.  Pass 2 inserts only entries >= thr.
+    // The row's candidates are one contiguous array of n entries.  The row's
+    // top KC are all at least thr, the KC-th largest of the 32 lane maxima;
+    // only entries >= thr are inserted into the lane's sorted list.  When the
+    // row's entries fit kOnePass a lane, they are loaded in one round and
+    // kept in registers; otherwise pass 1 finds thr and pass 2 reloads them.
     const int n = a.nseg * kWarps * KS;
     const float2* pr = a.parts + (size_t)r * n;
-    constexpr int kBatch = 8;                             // loads in flight per lane
-    float x = kNegInf;
-    for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
-        float2 e[kBatch];
-#pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-            const int i = q0 + 32 * q;
-            e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, 0.f);
-        }
-#pragma unroll
-        for (int q = 0; q < kBatch; ++q) x = fmaxf(x, e[q].x);
-    }
-    float thr = kNegInf;
-#pragma unroll
-    for (int k = 0; k < KC; ++k) {
-        thr = warp_max(x);
-        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
-        if (lane == __ffs(own) - 1) x = kNegInf;
-    }
     TopList<KC> L;
     L.init();
-    for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
-        float2 e[kBatch];
+    if (n <= 32 * kOnePass) {                             // warp-uniform
+        float2 e[kOnePass];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-            const int i = q0 + 32 * q;
+        for (int q = 0; q < kOnePass; ++q) {
+            const int i = lane + 32 * q;
             e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, __int_as_float(0x7fffffff));
         }
+        float x = kNegInf;
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q)
+        for (int q = 0; q < kOnePass; ++q) x = fmaxf(x, e[q].x);
+        const float thr = kth_lane_max<KC>(x, lane);
+#pragma unroll
+        for (int q = 0; q < kOnePass; ++q)
             if (e[q].x >= thr) L.insert(e[q].x, __float_as_int(e[q].y));
+    } else {
+        constexpr int kBatch = 8;                         // loads in flight per lane
+        float x = kNegInf;
+        for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
+            float2 e[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int i = q0 + 32 * q;
+                e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) x = fmaxf(x, e[q].x);
+        }
+        const float thr = kth_lane_max<KC>(x, lane);
+        for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
+            float2 e[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int i = q0 + 32 * q;
+                e[q] = i < n ? __ldcg(pr + i) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q)
+                if (e[q].x >= thr) L.insert(e[q].x, __float_as_int(e[q].y));
+        }
     }
     float ov[KC];
     int oi[KC];
@@ -97,6 +124,17 @@ static cudaError_t launch_topk_t(const VerifyArgs& a, int elt, int K, const int3
                                  float* out_val, const DeviceInfo& di, cudaStream_t st) {
     constexpr int MODE = KC == 2 ? kModeTopK2 : KC == 4 ? kModeTopK4 : kModeTopK8;
     cudaError_t e = elt == 2 ? launch_stream<2, MODE>(a, di, st) : launch_stream<4, MODE>(a, di, st);
+    if (e != cudaSuccess) return e;
+    // the merge prefers the whole carveout as shared memory, as the ring
+    // stream does, so that its CTAs can wait on SMs that hold stream CTAs
+    // (an SM runs CTAs of several kernels only under one carveout)
+    static DeviceSlots slots = {};
+    int unused = 0;
+    e = device_once(slots, &unused, [&](int, int* o) {
+        *o = 1;
+        return cudaFuncSetAttribute(topk_merge_kernel<KC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
+    });
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_merge_kernel<KC>, dim3((a.B + kTopkRowsPerCta - 1) / kTopkRowsPerCta),
                       kThreads, 0, st, a, K, exclude, out_val);
