@@ -139,3 +139,24 @@ def test_topk_lanes_with_several_candidates(sv, dtype):
             z[r, v0:v0 + n] = np.float32(6.5 if rng.random() < 0.5 else 7.5)
     check(sv, z, K, exclusions(rng, z, K), dtype)
     check(sv, z, K, None, dtype)
+
+
+@pytest.mark.parametrize("dtype,K", [("bf16", 2), ("bf16", 4), ("bf16", 8), ("f32", 4)])
+def test_topk_tiny_last_segment(sv, dtype, K):
+    """Rows of 65552 bytes: two full 32 KB segments and a last segment of 16
+    bytes (8 bf16 or 4 fp32 logits, one lane of one warp).  With 600 rows the
+    streaming CTAs' chunk ranges start at every segment, so some warps meet a
+    row first at its 16-byte tail: fewer than K lanes hold logits there, the
+    bound the chunk starts from is -inf, and only the row's own elements may
+    become candidates (the padding vectors read as -inf, and the shared memory
+    behind them holds bytes of another chunk).  Half of the rows keep their
+    largest logits in that tail, the other half their smallest."""
+    rng = np.random.default_rng(17 + K)
+    PV = 8 if dtype == "bf16" else 4
+    V = 2 * (32768 // (2 if dtype == "bf16" else 4)) + PV
+    R = 600
+    z = rng.standard_normal((R, V)).astype(np.float32)
+    z[0::2, V - PV:] = np.float32(9.0) + rng.random((R // 2, PV)).astype(np.float32)
+    z[1::2, V - PV:] = np.float32(-9.0) - rng.random((R // 2, PV)).astype(np.float32)
+    check(sv, z, K, exclusions(rng, z, K), dtype)
+    check(sv, z, K, None, dtype)
