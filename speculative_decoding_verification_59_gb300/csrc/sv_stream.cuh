@@ -573,6 +573,12 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
         // stage's row, partial row, segment and length to the consumers (row
         // kNoChunk ends the stream), so that they divide no chunk index
         if (lane == 0) {
+            // The stream reads each logit once: its lines go first when L2
+            // needs room, which keeps the partials, decisions and candidates
+            // that the kernels beside and after it poll and read (same-box,
+            // chain-b64: sampling 61.5 -> 60.4 us, greedy 26.6 -> 26.3, top-K
+            // 30.9 -> 30.0 per call).
+            const uint64_t evict_first = l2_evict_first_policy();
             ChunkSource src(a, total, kBeside);
             unsigned issued = 0;
             bool ok = true, ended = false, triggered = kBeside;
@@ -601,7 +607,7 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
                 stage_info[st] = make_uint4(rr, pr, (unsigned)seg, bytes);
                 mbar_arrive_expect_tx(&full[st], bytes);
                 bulk_g2s(ring + (size_t)st * kStageBytes, stream_row<MODE>(a, pr, rowbytes) + off, bytes,
-                         &full[st]);
+                         &full[st], evict_first);
             }
             if (!ok) {
                 if (!triggered) pdl_trigger();

@@ -23,18 +23,47 @@ namespace sv {
 constexpr int kTopkRowsPerCta = kThreads / 32;
 constexpr int kOnePass = 24;          // candidates a lane holds in registers (640 a row for V = 151936 bf16)
 
-// The KC-th largest of the 32 lanes' x (K rounds of a warp maximum, the
-// lowest lane holding it dropping out), -inf when fewer lanes hold values.
+// Order-preserving integer key of a float: a larger float has a larger key,
+// so that a warp maximum is one redux.sync.  -0.0 falls below +0.0; the
+// candidates carry no -0.0 (the stream adds 0.0 to every value it stores).
+__device__ __forceinline__ int ord_key(float v) {
+    const int b = __float_as_int(v);
+    return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float key_value(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+constexpr int kNoKey = (int)0x80000000;                 // below every float's key
+
+// The KC-th largest of the 32 lanes' x (KC rounds of a warp maximum of the
+// keys, the lowest lane holding it dropping out): KC values of distinct lanes.
 template <int KC>
 __device__ __forceinline__ float kth_lane_max(float x, int lane) {
-    float thr = kNegInf;
+    int k = ord_key(x), t = kNoKey;
 #pragma unroll
-    for (int k = 0; k < KC; ++k) {
-        thr = warp_max(x);
-        const unsigned own = __ballot_sync(0xffffffffu, x == thr);
-        if (lane == __ffs(own) - 1) x = kNegInf;
+    for (int r = 0; r < KC; ++r) {
+        t = __reduce_max_sync(0xffffffffu, k);
+        const unsigned own = __ballot_sync(0xffffffffu, k == t);
+        if (lane == __ffs(own) - 1) k = kNoKey;
     }
-    return thr;
+    return key_value(t);
+}
+
+// The KC best of at most 32 entries held one to a lane (c, present when
+// has), best first: KC rounds of the largest key, then the lowest index among
+// the lanes holding it (larger value first, lower index first among equal
+// values); (-inf, INT_MAX) once none is left.
+template <int KC>
+__device__ __forceinline__ void lanes_topk(float2 c, bool has, float (&ov)[KC], int (&oi)[KC]) {
+    int ck = has ? ord_key(c.x) : kNoKey;
+    const unsigned ci = has ? (unsigned)__float_as_int(c.y) : 0xffffffffu;
+#pragma unroll
+    for (int r = 0; r < KC; ++r) {
+        const int t = __reduce_max_sync(0xffffffffu, ck);
+        const unsigned j = __reduce_min_sync(0xffffffffu, ck == t ? ci : 0xffffffffu);
+        const bool none = t == kNoKey;
+        ov[r] = none ? kNegInf : key_value(t);
+        oi[r] = none ? 0x7fffffff : (int)j;
+        if (ck == t && ci == j) ck = kNoKey;
+    }
 }
 
 template <int KC>
@@ -42,19 +71,23 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a
                                                               const int32_t* exclude,
                                                               float* out_val) {
     constexpr int KS = topk_slots(KC);
+    __shared__ float2 tk_pool[kTopkRowsPerCta][32];      // a warp's entries that reach thr
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kTopkRowsPerCta + (threadIdx.x >> 5);
     if (r >= a.B) return;                                 // warp-uniform
     // The row's candidates are one contiguous array of n entries.  The row's
-    // top KC are all at least thr, the KC-th largest of the 32 lane maxima;
-    // only entries >= thr are inserted into the lane's sorted list.  When the
-    // row's entries fit kOnePass a lane, they are loaded in one round and
-    // kept in registers; otherwise pass 1 finds thr and pass 2 reloads them.
+    // top KC are all at least thr, the KC-th largest of the 32 lane maxima.
+    // When the row's entries fit kOnePass a lane, they are loaded in one round
+    // and kept in registers; the few that reach thr (at least KC, a handful
+    // more as a rule) go one to a lane through shared memory and lanes_topk
+    // orders them.  Otherwise (more than 32 reach thr, or longer rows) the
+    // lanes insert them into sorted lists, merged by warp_merge_topk; longer
+    // rows take a pass for thr and a second pass that reloads them.
     const int n = a.nseg * kWarps * KS;
     const float2* pr = a.parts + (size_t)r * n;
-    TopList<KC> L;
-    L.init();
+    float ov[KC];
+    int oi[KC];
     if (n <= 32 * kOnePass) {                             // warp-uniform
         float2 e[kOnePass];
 #pragma unroll
@@ -66,10 +99,42 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a
 #pragma unroll
         for (int q = 0; q < kOnePass; ++q) x = fmaxf(x, e[q].x);
         const float thr = kth_lane_max<KC>(x, lane);
+        unsigned sel = 0u;                                // bit q: e[q] reaches thr
 #pragma unroll
-        for (int q = 0; q < kOnePass; ++q)
-            if (e[q].x >= thr) L.insert(e[q].x, __float_as_int(e[q].y));
+        for (int q = 0; q < kOnePass; ++q) sel |= (e[q].x >= thr ? 1u : 0u) << q;
+        const int cnt = __popc(sel);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total <= 32) {                                // warp-uniform: nearly always
+            float2* pool = tk_pool[threadIdx.x >> 5];
+            int pos = incl - cnt;
+#pragma unroll
+            for (int q = 0; q < kOnePass; ++q)
+                if ((sel >> q) & 1u) pool[pos++] = e[q];
+            __syncwarp();
+            lanes_topk<KC>(pool[lane], lane < total, ov, oi);
+        } else {
+            // rare (many equal values): the marked entries are reloaded, so
+            // that e stays in registers
+            TopList<KC> L;
+            L.init();
+#pragma unroll 1
+            for (int q = 0; q < kOnePass; ++q)
+                if ((sel >> q) & 1u) {
+                    const int i = lane + 32 * q;
+                    const float2 t = i < n ? __ldcg(pr + i) : make_float2(kNegInf, __int_as_float(0x7fffffff));
+                    L.insert(t.x, __float_as_int(t.y));
+                }
+            warp_merge_topk<KC>(L, ov, oi);
+        }
     } else {
+        TopList<KC> L;
+        L.init();
         constexpr int kBatch = 8;                         // loads in flight per lane
         float x = kNegInf;
         for (int q0 = lane; q0 < n; q0 += 32 * kBatch) {
@@ -94,10 +159,8 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a
             for (int q = 0; q < kBatch; ++q)
                 if (e[q].x >= thr) L.insert(e[q].x, __float_as_int(e[q].y));
         }
+        warp_merge_topk<KC>(L, ov, oi);
     }
-    float ov[KC];
-    int oi[KC];
-    warp_merge_topk<KC>(L, ov, oi);
     if (lane == 0) {
         const int ex = exclude ? exclude[r] : -1;
         int o = 0;
