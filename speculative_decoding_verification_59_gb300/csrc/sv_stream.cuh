@@ -461,33 +461,42 @@ struct ChunkSource {
     // chunks i, i + G, i + 2G, ... of G CTAs), so the stream advances through
     // the chunks -- and the sequences -- in index order; otherwise each CTA
     // takes a contiguous range.
+    // This CTA's static share: chunks s, s + step, ... below s_end; dyn when
+    // the rest, from first_dyn on, is claimed from the counter.
+    __device__ __forceinline__ static void static_share(unsigned total, bool round_robin, unsigned* s,
+                                                        unsigned* s_end, unsigned* step, bool* dyn,
+                                                        unsigned* first_dyn) {
+        const unsigned q = (unsigned)(((unsigned long long)total * 3ull / 4ull) / gridDim.x);
+        *step = 1;
+        *dyn = q >= 2 && total < (1u << (kClaimIdxBits - 1));
+        if (*dyn) {
+            *first_dyn = q * gridDim.x;
+            if (round_robin) {
+                *s = blockIdx.x;
+                *step = gridDim.x;
+                *s_end = blockIdx.x + q * gridDim.x;
+            } else {
+                *s = blockIdx.x * q;
+                *s_end = *s + q;
+            }
+        } else {
+            *first_dyn = total;
+            cta_range(total, blockIdx.x, gridDim.x, s, s_end);
+        }
+    }
+
     __device__ __forceinline__ ChunkSource(const VerifyArgs& a, unsigned total_, bool round_robin) {
         total = total_;
-        step = 1;
         ctr = a.claim;
         tag = a.claim_tag;
         limit = a.wait_limit;
         err = a.err;
         have = false;
         pending = 0ull;
-        const unsigned q = (unsigned)(((unsigned long long)total * 3ull / 4ull) / gridDim.x);
-        dyn = q >= 2 && total < (1u << (kClaimIdxBits - 1));
-        if (dyn) {
-            first_dyn = q * gridDim.x;
-            if (round_robin) {
-                s = blockIdx.x;
-                step = gridDim.x;
-                s_end = blockIdx.x + q * gridDim.x;
-            } else {
-                s = blockIdx.x * q;
-                s_end = s + q;
-            }
+        static_share(total, round_robin, &s, &s_end, &step, &dyn, &first_dyn);
+        if (dyn)
             asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(ctr), "l"(tag | first_dyn)
                          : "memory");
-        } else {
-            first_dyn = total;
-            cta_range(total, blockIdx.x, gridDim.x, &s, &s_end);
-        }
     }
 
     __device__ __forceinline__ void claim() {
@@ -537,6 +546,34 @@ struct ChunkSource {
     }
 };
 
+// Chunks of its static share that a ring CTA prefetches into L2 before it
+// waits for the kernel before it.
+constexpr int kPrefetchChunks = 3;
+
+// The L2 prefetch of this CTA's first static chunks, issued before the wait
+// on the kernel before (one thread): the HBM latency of the stream's first
+// copies then overlaps that kernel's tail.  Only the logits are touched, never
+// the workspace the kernel before may still use; a kernel before that writes
+// the logits writes them through L2, where the copies issued after the wait
+// find them current.  Lazy groups after the first take their rows and chunk
+// count from the workspace and prefetch nothing.
+template <int MODE>
+__device__ __forceinline__ void prefetch_first_chunks(const VerifyArgs& a, size_t rowbytes, bool round_robin) {
+    if constexpr (MODE == kModeLazy)
+        if (a.lz_list != nullptr || a.lz_count != nullptr) return;
+    unsigned s, s_end, step, first_dyn;
+    bool dyn;
+    ChunkSource::static_share((unsigned)a.total_chunks, round_robin, &s, &s_end, &step, &dyn, &first_dyn);
+    StreamRows rows;
+    for (int i = 0; i < kPrefetchChunks && s < s_end; ++i, s += step) {
+        const unsigned rr = s / (unsigned)a.nseg;
+        const int seg = (int)(s - rr * (unsigned)a.nseg);
+        const size_t off = (size_t)seg * kStageBytes;
+        bulk_prefetch_l2(stream_row<MODE>(a, rows.part_row<MODE>(a, rr), rowbytes) + off,
+                         (uint32_t)min((size_t)kStageBytes, rowbytes - off));
+    }
+}
+
 template <int ELT, int MODE>
 __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     extern __shared__ __align__(128) unsigned char ring[];
@@ -547,7 +584,9 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     const size_t rowbytes = (size_t)a.V * ELT;
     const int P = a.nseg * kWarps;
 
+    constexpr bool kBeside = MODE == kModeSample || MODE == kModeGreedy || MODE == kModeTree;
     if (threadIdx.x == 0) {
+        prefetch_first_chunks<MODE>(a, rowbytes, kBeside);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
@@ -559,7 +598,6 @@ __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     // Sampling, greedy and tree verification: the decide kernel may start
     // now.  It runs beside the stream and takes each sequence's decision once
     // that sequence's partials all carry this call's tag.
-    constexpr bool kBeside = MODE == kModeSample || MODE == kModeGreedy || MODE == kModeTree;
     if (kBeside && threadIdx.x == 0) pdl_trigger();
     unsigned total = (unsigned)a.total_chunks;
     if constexpr (MODE == kModeLazy) {
