@@ -466,7 +466,7 @@ struct ChunkSource {
     __device__ __forceinline__ static void static_share(unsigned total, bool round_robin, unsigned* s,
                                                         unsigned* s_end, unsigned* step, bool* dyn,
                                                         unsigned* first_dyn) {
-        const unsigned q = (unsigned)(((unsigned long long)total * 3ull / 4ull) / gridDim.x);
+        const unsigned q = (3u * (total >> 2) + ((3u * (total & 3u)) >> 2)) / gridDim.x;   // floor(3 total / 4) / G
         *step = 1;
         *dyn = q >= 2 && total < (1u << (kClaimIdxBits - 1));
         if (*dyn) {
@@ -547,8 +547,12 @@ struct ChunkSource {
 };
 
 // Chunks of its static share that a ring CTA prefetches into L2 before it
-// waits for the kernel before it.
+// waits for the kernel before it, on streams of at least kPrefetchMinChunks
+// chunks (32 MB).  Measured on GB300: shorter streams (chain-b8's 640-chunk
+// argmax streams, chain-small's 9 chunks) lost 0.3-0.5 us a call to the
+// prefetch, longer ones gained 1.3-3.3 us.
 constexpr int kPrefetchChunks = 3;
+constexpr long long kPrefetchMinChunks = 1024;
 
 // The L2 prefetch of this CTA's first static chunks, issued before the wait
 // on the kernel before (one thread): the HBM latency of the stream's first
@@ -559,6 +563,7 @@ constexpr int kPrefetchChunks = 3;
 // count from the workspace and prefetch nothing.
 template <int MODE>
 __device__ __forceinline__ void prefetch_first_chunks(const VerifyArgs& a, size_t rowbytes, bool round_robin) {
+    if (a.total_chunks < kPrefetchMinChunks) return;
     if constexpr (MODE == kModeLazy)
         if (a.lz_list != nullptr || a.lz_count != nullptr) return;
     unsigned s, s_end, step, first_dyn;
