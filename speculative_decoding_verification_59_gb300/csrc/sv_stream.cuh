@@ -13,9 +13,12 @@
 // reg_stream_kernel (any row alignment): the same partials from register
 // loads, one CTA of kThreads per block chunk in a persistent loop.
 //
-// Each CTA streams one contiguous range of block chunks (measured faster on
-// GB300 than dealing chunks round-robin).  Nothing here waits on another CTA:
-// the decisions run in the next kernel of the stream.
+// Which chunks a ring CTA streams is ChunkSource's: three quarters dealt
+// statically, the rest claimed one at a time from a tagged counter.  The
+// bulk copies carry an evict-first L2 policy, and a CTA prefetches its first
+// chunks into L2 before it waits on the kernel before.  No CTA waits on
+// another; the decisions run in the kernels launched beside or after the
+// stream.
 #pragma once
 
 #include "sv_common.cuh"
@@ -583,7 +586,7 @@ template <int ELT, int MODE>
 __device__ __forceinline__ void ring_stream_body(const VerifyArgs& a) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ uint4 stage_info[kStages];              // (row, partial row, segment, bytes) a stage holds
+    __shared__ uint4 stage_info[kStages];              // (row, partial row, segment, length) a stage holds
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int KT = topk_of(MODE);
     const size_t rowbytes = (size_t)a.V * ELT;
