@@ -30,6 +30,7 @@ constexpr int kArgmaxBesideThreads = 256;
 template <int NT>
 __global__ void __launch_bounds__(NT, NT == kArgmaxBesideThreads ? 3 : 1) greedy_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
+    pdl_trigger();
     prefetch_tokens<NT>(a, blockIdx.x, threadIdx.x, false, sm);   // inputs: before the wait
     if (a.poll_parts) wait_seq_parts<NT>(a, blockIdx.x, threadIdx.x);
     else pdl_wait();
@@ -41,6 +42,7 @@ template <int NT>
 __global__ void __launch_bounds__(NT, NT == kArgmaxBesideThreads ? 3 : 1) tree_decide_kernel(const VerifyArgs a) {
     __shared__ ArgmaxDecideSmem sm;
     __shared__ TreeWalkSmem tw;
+    pdl_trigger();
     prefetch_tokens<NT>(a, blockIdx.x, threadIdx.x, true, sm);
     if (a.poll_parts) wait_seq_parts<NT>(a, blockIdx.x, threadIdx.x);
     else pdl_wait();

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const VerifyArgs a
                                                               float* out_val) {
     constexpr int KS = topk_slots(KC);
     __shared__ float2 tk_pool[kTopkRowsPerCta][32];      // a warp's entries that reach thr
+    pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kTopkRowsPerCta + (threadIdx.x >> 5);
