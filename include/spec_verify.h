@@ -24,7 +24,13 @@
  * Conventions shared by every call
  *   - Every pointer is a DEVICE pointer owned by the caller; the library never
  *     allocates and keeps no per-call state.  Calls are asynchronous on
- *     `stream`; results are valid once the stream reaches them.
+ *     `stream`; results are valid once the stream reaches them.  The
+ *     library's kernels are launched with programmatic dependent launch: a
+ *     call's first kernel may start while the kernel before it on `stream`
+ *     finishes, and may then prefetch logits into L2, but it reads the
+ *     inputs and the workspace only after that kernel has completed.  Inputs
+ *     written by the kernel just before the call on the same stream are
+ *     therefore read as written.
  *   - Logits are row-major with V contiguous, dtype SPEC_DTYPE_F32 or
  *     SPEC_DTYPE_BF16.  Logit base pointers must be 16-byte aligned
  *     (SPEC_ERR_MISALIGNED otherwise).  V need not be a multiple of anything.
