@@ -133,10 +133,18 @@ struct LaneChunk<ELT, false> {
 };
 
 // ---- warp reductions -------------------------------------------------------
+// Order-preserving integer key of a float: a larger float has a larger key
+// (-0.0 falls just below +0.0), so that a warp maximum is one redux.sync.
+__device__ __forceinline__ int ord_key(float v) {
+    const int b = __float_as_int(v);
+    return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float key_value(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+constexpr int kNoKey = (int)0x80000000;                 // below every float's key
+
+// The largest v of the warp (of -0.0 and +0.0, +0.0; NaN logits are undefined).
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    return key_value(__reduce_max_sync(0xffffffffu, ord_key(v)));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -23,15 +23,8 @@ namespace sv {
 constexpr int kTopkRowsPerCta = kThreads / 32;
 constexpr int kOnePass = 24;          // candidates a lane holds in registers (640 a row for V = 151936 bf16)
 
-// Order-preserving integer key of a float: a larger float has a larger key,
-// so that a warp maximum is one redux.sync.  -0.0 falls below +0.0; the
-// candidates carry no -0.0 (the stream adds 0.0 to every value it stores).
-__device__ __forceinline__ int ord_key(float v) {
-    const int b = __float_as_int(v);
-    return b >= 0 ? b : b ^ 0x7fffffff;
-}
-__device__ __forceinline__ float key_value(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
-constexpr int kNoKey = (int)0x80000000;                 // below every float's key
+// The candidates carry no -0.0 (the stream adds 0.0 to every value it
+// stores), so ordering them by ord_key (sv_common.cuh) is ordering them by value.
 
 // The KC-th largest of the 32 lanes' x (KC rounds of a warp maximum of the
 // keys, the lowest lane holding it dropping out): KC values of distinct lanes.
