@@ -164,13 +164,14 @@ __device__ __forceinline__ bool am_better(float v1, int i1, float v2, int i2) {
     return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// The warp's best (v, i) in am_better's order, in every lane: the largest
+// value (-0.0 and +0.0 equal), then the lowest index among the lanes holding
+// it -- two redux.sync.  Indices are non-negative (INT_MAX for none).
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (am_better(ov, oi, v, i)) { v = ov; i = oi; }
-    }
+    const int k = ord_key(v + 0.0f);
+    const int t = __reduce_max_sync(0xffffffffu, k);
+    i = (int)__reduce_min_sync(0xffffffffu, k == t ? (unsigned)i : 0xffffffffu);
+    v = key_value(t);
 }
 
 // ---- float-float accumulation (Knuth's TwoSum) -----------------------------
