@@ -108,13 +108,17 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = ("sv_common.cuh", "sv_internal.h", "sv_tma.cuh", "sv_decide.cuh", "sv_stream.cuh")
+
+
+def kernel_source_hash(csrc=None):
     """Hash of the code that defines the row-statistics stream kernel (its sources with
     comments and blank lines removed, so that an edit of comments alone keeps it); ncu
     traffic figures recorded under profiles/ are only reported while it matches."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_decoding_verification_59_gb300", "csrc")
-    for f in ("sv_common.cuh", "sv_internal.h", "sv_tma.cuh", "sv_decide.cuh", "sv_stream.cuh"):
+    if csrc is None:
+        csrc = os.path.join(ROOT, "speculative_decoding_verification_59_gb300", "csrc")
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             for line in fh:
                 code = line.split("//", 1)[0].strip()

@@ -101,3 +101,28 @@ def test_lazy_rows_read_accounting():
     assert all(bench.lazy_rows_read(k, groups) == 4 + 6 + 5 for k in range(2, 8))
     assert bench.lazy_rows_read(0, [(0, 1)]) == 1       # gamma = 0: the bonus row only
     assert bench.lazy_rows_read(4, [(0, 2), (2, 5)]) == 4 + 3 + 2
+
+
+def test_kernel_hash_ignores_comments_but_not_code(tmp_path):
+    """The traffic figure recorded under profiles/ stays valid across an edit of comments
+    alone, and is dropped after any change of the streaming kernel's code."""
+    import shutil
+    src = os.path.join(bench.ROOT, "speculative_decoding_verification_59_gb300", "csrc")
+    for f in bench.KERNEL_SOURCES:
+        shutil.copy(os.path.join(src, f), tmp_path / f)
+    h0 = bench.kernel_source_hash(str(tmp_path))
+    assert h0 == bench.kernel_source_hash()
+    p = tmp_path / "sv_stream.cuh"
+    text = p.read_text(encoding="utf-8")
+    p.write_text("// a new comment line\n\n" + text.replace("namespace sv {", "namespace sv {  // same code"),
+                 encoding="utf-8")
+    assert bench.kernel_source_hash(str(tmp_path)) == h0
+    p.write_text(text.replace("constexpr int kStages = 3;", "constexpr int kStages = 4;"), encoding="utf-8")
+    assert bench.kernel_source_hash(str(tmp_path)) != h0
+
+
+def test_recorded_traffic_matches_the_committed_kernel():
+    """profiles/stats_traffic.txt carries the hash of the code it was captured on; the
+    bench line reports its traffic only while that hash is the current one."""
+    t = bench.recorded_traffic("chain-b64")
+    assert t is None or t >= 291717120
